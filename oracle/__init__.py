@@ -1,0 +1,238 @@
+"""Oracle for the speculative-decoding round math -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, single-threaded fp64 C++ implementation (``oracle.cpp``) of the
+draft / confidence / schedule / verify definitions, wrapped here with ctypes
+and numpy.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this package.  It shares no code with the CUDA
+library in ``verify_sampling_gb300``.
+
+Each wrapper cites the passage of the pages it follows (see ``oracle.cpp``):
+  * draft      -- DSpark summary, "第二阶段：轻量顺序头"; history article "杀招一"
+  * confidence -- DSpark summary, "2.1 置信度头" (+ sequential temperature scaling)
+  * schedule   -- DSpark summary, "2.2 硬件感知前缀调度器" and "挑战2"; history "杀招三"
+  * verify     -- history article, "1.1运行机制" (rejection sampling); DSpark Figure 1
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+DRAFT_GUMBEL, ACCEPT_U, RESIDUAL_GUMBEL, BONUS_GUMBEL = 0, 1, 2, 3
+MODE_SAMPLE, MODE_GREEDY = 0, 1
+SCHED_EARLY_STOP, SCHED_GLOBAL = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with g++ (fp contraction off, so x86 and Arm agree)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, u32, u64, f64 = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
+                                   ctypes.c_uint64, ctypes.c_double)
+        L.orc_philox4x32_10.argtypes = [P, P, P]
+        L.orc_philox4x32_10.restype = None
+        L.orc_uniform.argtypes = [u64, u32, u32, u32, u32]
+        L.orc_uniform.restype = f64
+        L.orc_gumbel_argmax.argtypes = [i32, P, u64, u32, u32, u32, P]
+        L.orc_gumbel_argmax.restype = i32
+        L.orc_sps_lookup.argtypes = [P, i32, f64, f64, f64]
+        L.orc_sps_lookup.restype = f64
+        L.orc_draft.argtypes = [i32, i32, i32, i32, P, i64, P, P, P, P, u64, u32, P, P, P, P, P, P]
+        L.orc_draft.restype = i32
+        L.orc_confidence.argtypes = [i32, i32, i32, i32, i32, P, i64, P, P, P, P, P, P, P]
+        L.orc_confidence.restype = i32
+        L.orc_schedule.argtypes = [i32, i32, P, P, i32, f64, f64, i32, i32, P, P, P, P, P, P]
+        L.orc_schedule.restype = i32
+        L.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, P, i64, P, P, i32, P, P,
+                                 u64, u32, P, P, P, P, P]
+        L.orc_verify.restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+# ---------------------------------------------------------------- random ----
+def philox4x32_10(counter, key) -> np.ndarray:
+    c = np.asarray(counter, dtype=np.uint32).copy()
+    k = np.asarray(key, dtype=np.uint32).copy()
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, v: int, j: int, rid: int, purpose: int) -> float:
+    return lib().orc_uniform(seed, v, j, rid, purpose)
+
+
+def gumbel_argmax(logw, seed: int, j: int, rid: int, purpose: int):
+    lw = _f64(logw)
+    gap = ctypes.c_double()
+    idx = lib().orc_gumbel_argmax(lw.size, _ptr(lw), seed, j, rid, purpose, ctypes.byref(gap))
+    return idx, gap.value
+
+
+def sps_lookup(sps, b_lo: float, b_step: float, B: float) -> float:
+    s = _f64(sps)
+    return lib().orc_sps_lookup(_ptr(s), s.size, b_lo, b_step, B)
+
+
+# ----------------------------------------------------------------- draft ----
+@dataclass
+class DraftOut:
+    x: np.ndarray       # [R, gamma] int32
+    q_tok: np.ndarray   # [R, gamma] f64
+    lse: np.ndarray     # [R, gamma] f64
+    gap: np.ndarray     # [R, gamma] f64 Gumbel top-2 score gap
+    P: np.ndarray | None
+
+
+def draft(U, A, Ct, x0, draft_temp, seed: int, rid_base: int = 0, x_cond=None,
+          want_P: bool = False) -> DraftOut:
+    """U [R, gamma, V]; A, Ct [gamma, V, r]; x0 [R]; draft_temp [gamma]."""
+    U = _f32(U)
+    R, gamma, V = U.shape
+    A, Ct = _f32(A), _f32(Ct)
+    r = A.shape[2]
+    assert A.shape == (gamma, V, r) and Ct.shape == (gamma, V, r)
+    x0, temp = _i32(x0), _f32(draft_temp)
+    xc = None if x_cond is None else _i32(x_cond)
+    x = np.zeros((R, gamma), np.int32)
+    q, l, g = (np.zeros((R, gamma)) for _ in range(3))
+    P = np.zeros((R, gamma, V)) if want_P else None
+    rc = lib().orc_draft(R, gamma, V, r, _ptr(U), gamma * V, _ptr(A), _ptr(Ct), _ptr(x0),
+                         _ptr(temp), seed, rid_base, _ptr(xc), _ptr(x), _ptr(q), _ptr(l),
+                         _ptr(g), _ptr(P))
+    if rc != 0:
+        raise ValueError(f"orc_draft failed ({rc})")
+    return DraftOut(x, q, l, g, P)
+
+
+# ------------------------------------------------------------ confidence ----
+def confidence(h, W1, w, x0, x, sts_temp):
+    """h [R, gamma, d]; W1 [V, e]; w [d + e]; x0 [R]; x [R, gamma] -> (c, a) f64."""
+    h = _f32(h)
+    R, gamma, d = h.shape
+    W1, w = _f32(W1), _f32(w)
+    V, e = W1.shape
+    assert w.size == d + e
+    x0, x, t = _i32(x0), _i32(x), _f32(sts_temp)
+    c = np.zeros((R, gamma))
+    a = np.zeros((R, gamma))
+    rc = lib().orc_confidence(R, gamma, d, e, V, _ptr(h), gamma * d, _ptr(W1), _ptr(w), _ptr(x0),
+                              _ptr(x), _ptr(t), _ptr(c), _ptr(a))
+    if rc != 0:
+        raise ValueError(f"orc_confidence failed ({rc})")
+    return c, a
+
+
+# -------------------------------------------------------------- schedule ----
+@dataclass
+class ScheduleOut:
+    ell: np.ndarray
+    row_off: np.ndarray
+    n: int
+    B: int
+    tau: float
+    theta: float
+    margin: float
+    order: np.ndarray
+    theta_seq: np.ndarray
+
+
+def schedule(a, sps, b_lo: float, b_step: float, K: int, mode: int = SCHED_EARLY_STOP) -> ScheduleOut:
+    """a [R, gamma] survival probabilities; sps table at B_i = b_lo + i*b_step."""
+    a = _f64(a)
+    R, gamma = a.shape
+    s = _f64(sps)
+    ell = np.zeros(R, np.int32)
+    row_off = np.zeros(R + 1, np.int32)
+    stats = np.zeros(4)
+    mg = ctypes.c_double()
+    order = np.zeros(R * gamma, np.int32)
+    nmax = min(K, R * gamma)
+    th = np.zeros(nmax + 1)
+    rc = lib().orc_schedule(R, gamma, _ptr(a), _ptr(s), s.size, b_lo, b_step, K, mode, _ptr(ell),
+                            _ptr(row_off), _ptr(stats), ctypes.byref(mg), _ptr(order), _ptr(th))
+    if rc != 0:
+        raise ValueError(f"orc_schedule failed ({rc})")
+    return ScheduleOut(ell, row_off, int(stats[0]), int(stats[1]), float(stats[2]),
+                       float(stats[3]), mg.value, order, th)
+
+
+# ---------------------------------------------------------------- verify ----
+@dataclass
+class VerifyOut:
+    accept_len: np.ndarray
+    out_tok: np.ndarray
+    n_out: np.ndarray
+    margin: np.ndarray
+    jstar: np.ndarray
+
+
+def verify(mode: int, tgt, row_off, ell, x, q_tok, target_temp: float, U, A, Ct, x0, draft_temp,
+           seed: int, rid_base: int = 0) -> VerifyOut:
+    """tgt [rows, V]; row (r, j) = row_off[r] + j - 1.  U [R, gamma, V]; A, Ct [gamma, V, r]."""
+    tgt = _f32(tgt)
+    V = tgt.shape[-1]
+    tgt = tgt.reshape(-1, V)
+    x = _i32(x)
+    R, gamma = x.shape
+    row_off, ell, x0 = _i32(row_off), _i32(ell), _i32(x0)
+    q = _f64(q_tok)
+    temp = _f32(draft_temp)
+    if U is None:  # greedy mode never reads the draft rows
+        assert mode == MODE_GREEDY
+        A = Ct = None
+        r = 0
+    else:
+        U, A, Ct = _f32(U), _f32(A), _f32(Ct)
+        r = A.shape[2]
+    acc = np.zeros(R, np.int32)
+    out = np.zeros((R, gamma + 1), np.int32)
+    n_out = np.zeros(R, np.int32)
+    mg = np.zeros(R)
+    js = np.zeros(R, np.int32)
+    rc = lib().orc_verify(mode, R, gamma, V, _ptr(tgt), _ptr(row_off), _ptr(ell), _ptr(x), _ptr(q),
+                          target_temp, _ptr(U), gamma * V, _ptr(A), _ptr(Ct), r, _ptr(x0),
+                          _ptr(temp), seed, rid_base, _ptr(acc), _ptr(out), _ptr(n_out), _ptr(mg),
+                          _ptr(js))
+    if rc != 0:
+        raise ValueError(f"orc_verify failed ({rc})")
+    return VerifyOut(acc, out, n_out, mg, js)
