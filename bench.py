@@ -1,0 +1,371 @@
+"""Benchmark of one speculative-decoding round on GB300.
+
+A step is one full round over one batch: draft (gamma Markov-head sampling
+steps + confidence head), prefix schedule, verification (rejection sampling,
+residual, bonus).  Default workload: R=512 requests, gamma=11, V=129280, r=128,
+fp32 logits, bf16 factors, top-K cap 2048 (the largest configuration).
+Inputs are synthetic and seeded (synth/), resident in HBM, larger than L2.
+
+Metric: draft+verified positions per second = (R * gamma + B) / step time,
+B = sum_r (1 + l_r) verify rows, summed over ranks (one replica per GPU).
+Also reported: logit bytes per second of the dominant kernel against the
+measured HBM copy bandwidth, the oracle on the host cores, an end-to-end
+figure through host buffers, and SM clocks sampled during the timed region.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c5]
+Under torchrun every rank runs its own replica (weak scaling, no collective on
+the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="c5", choices=["c2", "c3", "c5", "greedy"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_QUERY}", "--format=csv",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        with open(self.path) as f:
+            lines = f.read().strip().splitlines()[1:]
+        for ln in lines:
+            c = [x.strip() for x in ln.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1].split()[0]))
+                mx.append(float(c[2].split()[0]))
+            except ValueError:
+                continue
+            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6),
+                              ("sw_thermal_slowdown", 7), ("sw_power_cap", 8)):
+                if c[col].lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- reference ----
+def _oracle_round(wl, inp_cpu, seed: int, n_req: int) -> tuple[int, float]:
+    """The oracle as it stands on a sub-batch of n_req requests of the workload:
+    draft, confidence, schedule over the sub-batch, verify.  Returns
+    (positions, seconds)."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    f = lambda t: t.float().numpy()
+    U = f(inp_cpu["U"][:n_req])
+    A, Ct = inp_cpu["A_np"], inp_cpu["Ct_np"]
+    x0 = inp_cpu["x0"][:n_req].numpy()
+    temps = inp_cpu["draft_temp"].numpy()
+    d = oracle.draft(U, A, Ct, x0, temps, seed)
+    _, a = oracle.confidence(f(inp_cpu["h"][:n_req]), inp_cpu["W1_np"], inp_cpu["w_np"], x0, d.x,
+                             inp_cpu["sts_temp"].numpy())
+    K = max(1, round(wl.K * n_req / wl.R))
+    s = oracle.schedule(a, inp_cpu["sps"].numpy(), inp_cpu["b_lo"], inp_cpu["b_step"], K,
+                        wl.sched_mode)
+    G = wl.gamma
+    rows = f(inp_cpu["tgt"][:n_req]).reshape(-1, wl.V)
+    oracle.verify(oracle.MODE_SAMPLE, rows, (np.arange(n_req) * (G + 1)).astype(np.int32), s.ell,
+                  d.x, d.q_tok, 1.0, U, A, Ct, x0, temps, seed)
+    return n_req * G + s.B, time.perf_counter() - t0
+
+
+def _cpu_inputs(wl):
+    import synth
+    small = wl.scaled(R=min(wl.R, 8), K=max(1, round(wl.K * min(wl.R, 8) / wl.R)))
+    inp = synth.make_inputs(small, "cpu", seed=wl.seed)
+    inp["A_np"] = inp["A"].float().numpy()
+    inp["Ct_np"] = inp["Ct"].float().numpy()
+    inp["W1_np"] = inp["W1"].float().numpy()
+    inp["w_np"] = inp["w"].float().numpy()
+    return inp
+
+
+def cpu_baseline(wl, budget_s: float = 15.0) -> dict:
+    inp = _cpu_inputs(wl)
+    pos, sec = _oracle_round(wl, inp, 1, 1)
+    n = max(1, min(8, int(budget_s / max(sec, 1e-3))))
+    pos, sec = _oracle_round(wl, inp, 2, n)
+    return {"value": pos / sec, "unit": "positions/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {wl.R} requests of the same workload, one full round "
+                      f"(draft, confidence, schedule over the {n}, verify), single-threaded fp64",
+            "seconds": round(sec, 3)}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = _cpu_inputs(wl)
+    n = 2
+    for i in range(args.warmup):
+        _oracle_round(wl, inp, 100 + i, 1)
+    tot_pos, tot_sec = 0, 0.0
+    for i in range(args.steps):
+        p, s = _oracle_round(wl, inp, 1000 + i, n)
+        tot_pos += p
+        tot_sec += s
+    value = tot_pos / tot_sec
+    line = {"metric": "draft+verified positions/s", "value": value, "unit": "positions/s",
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * tot_sec / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "R": wl.R, "gamma": wl.gamma, "V": wl.V, "r": wl.r},
+            "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} of {wl.R} requests per step, full round"},
+            "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours ----
+def main():
+    args = _args()
+    import synth
+    wl = synth.WORKLOADS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+    import verify_sampling_gb300 as vs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    g = synth.make_inputs(wl, dev, seed=wl.seed + rank)
+    rid_base = rank * wl.R
+    greedy = wl.mode == "greedy"
+    din = None if greedy else synth.draft_inputs(g, request_id_base=rid_base)
+    R, G, V = wl.R, wl.gamma, wl.V
+    stats_hist = torch.zeros(max(1, args.steps), 4, dtype=torch.float64, device=dev)
+
+    bufs = {}
+    if not greedy:
+        bufs["draft"] = vs.draft_outputs(R, G, V, dev)
+        bufs["ws_draft"] = torch.empty(vs.workspace_bytes(vs.STAGE_DRAFT, R, G, V, wl.r),
+                                       dtype=torch.uint8, device=dev)
+    bufs["ws_verify"] = torch.empty(vs.workspace_bytes(vs.STAGE_VERIFY, R, G, V), dtype=torch.uint8,
+                                    device=dev)
+    stream = torch.cuda.current_stream()
+    nev = max(1, args.steps)
+    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+          for k in ("d0", "d1", "s1", "v1")}
+
+    def step(i: int, timed: bool):
+        seed = 7000 + i
+        if greedy:
+            bufs["verify"] = vs.verify(vs.VERIFY_GREEDY, g["tgt"].view(-1, V), g["tgt_row_off"],
+                                       g["ell"], g["x"], seed, out=bufs.get("verify"),
+                                       workspace=bufs["ws_verify"])
+            return
+        if timed:
+            ev["d0"][i].record(stream)
+        d = vs.draft_sample(din, seed, out=bufs["draft"], workspace=bufs["ws_draft"])
+        if timed:
+            ev["d1"][i].record(stream)
+        s = vs.schedule(d["a"], g["sps"], g["b_lo"], g["b_step"], wl.K, wl.sched_mode,
+                        out=bufs.get("sched"))
+        bufs["sched"] = s
+        if timed:
+            ev["s1"][i].record(stream)
+        v = vs.verify(vs.VERIFY_SAMPLE, g["tgt"].view(-1, V), g["tgt_row_off"], s["ell"], d["x"],
+                      seed, q_tok=d["q_tok"], lse_q=d["lse_q"], draft=din,
+                      request_id_base=rid_base, out=bufs.get("verify"),
+                      workspace=bufs["ws_verify"])
+        bufs["verify"] = v
+        if timed:
+            ev["v1"][i].record(stream)
+            stats_hist[i].copy_(s["stats"], non_blocking=True)
+
+    for i in range(args.warmup):
+        step(-1 - i, False)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local) if rank == 0 else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    ms = t0.elapsed_time(t1)
+    stage_ms = {"draft": 0.0, "schedule": 0.0, "verify": 0.0}
+    if not greedy:
+        for i in range(args.steps):
+            stage_ms["draft"] += ev["d0"][i].elapsed_time(ev["d1"][i])
+            stage_ms["schedule"] += ev["d1"][i].elapsed_time(ev["s1"][i])
+            stage_ms["verify"] += ev["s1"][i].elapsed_time(ev["v1"][i])
+    if greedy:
+        B_sum = float(args.steps * R * (G + 1))
+        positions = B_sum
+    else:
+        B_sum = float(stats_hist[:, 1].sum())
+        positions = args.steps * R * G + B_sum
+    t = torch.tensor([ms, positions], dtype=torch.float64, device=dev)
+    if world > 1:
+        tm = t[:1].clone()
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        tp = t[1:].clone()
+        dist.all_reduce(tp, op=dist.ReduceOp.SUM)
+        ms_max, pos_all = float(tm), float(tp)
+    else:
+        ms_max, pos_all = ms, positions
+    value = pos_all / (ms_max / 1000.0)
+
+    # ------------------------------------------------ roofline (rank 0) ----
+    hbm, peak_kind = _peaks()
+    es_u = 4 if wl.logit_dtype == torch.float32 else 2
+    es_f = 4 if wl.fac_dtype == torch.float32 else 2
+    if greedy:
+        per_launch = R * (G + 1) * V * es_u
+        dur_ms = ms / args.steps
+        kernel = "verify_rows (greedy argmax, all R*(gamma+1) rows)"
+        launches = 1
+    else:
+        # dominant kernel: the draft step, gamma launches per round; one launch
+        # streams the R backbone rows of position k and the factor C_k.
+        per_launch = R * V * es_u + V * wl.r * es_f
+        dur_ms = stage_ms["draft"] / (args.steps * G)
+        kernel = "draft_step (one launch per position k)"
+        launches = G + 1 + 1 + 2
+    achieved = per_launch / (dur_ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": None,
+                "algorithmic_bytes_per_launch": per_launch}
+
+    line = {"metric": "draft+verified positions/s", "value": value, "unit": "positions/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if es_u == 4 else "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "R": R, "gamma": G, "V": V, "r": wl.r, "K": wl.K,
+                       "logits": str(wl.logit_dtype).replace("torch.", ""),
+                       "factors": str(wl.fac_dtype).replace("torch.", ""),
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "stage_ms_per_step": {k: round(v / args.steps, 4) for k, v in stage_ms.items()},
+            "mean_verify_rows": B_sum / args.steps,
+            "roofline": roofline, "gpu_launches": launches * args.steps, "clocks": clk}
+
+    # ----------------------------------------------------- e2e (rank 0) ----
+    if rank == 0 and not args.no_e2e and not greedy:
+        line["e2e"] = _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 5))
+    if rank == 0 and not args.no_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
+    """Same round through the public API with the per-step inputs (U, h, x0,
+    target logits) copied from pinned host memory each step and the results
+    (tokens, lengths, stats) copied back; the model weights (A, Ct, W1, w) stay
+    resident."""
+    names = ["U", "h", "x0", "tgt"]
+    host = {n: g[n].cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(g[n]) for n in names}
+    outs = {"out_tok": torch.empty(wl.R, wl.gamma + 1, dtype=torch.int32).pin_memory(),
+            "accept_len": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
+            "n_out": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
+            "stats": torch.empty(4, dtype=torch.float64).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    d_in = vs.DraftInputs(U=devb["U"], A=g["A"], Ct=g["Ct"], x0=devb["x0"],
+                          draft_temp=g["draft_temp"], h=devb["h"], W1=g["W1"], w=g["w"],
+                          sts_temp=g["sts_temp"], request_id_base=rid_base)
+
+    def one(i):
+        for n in names:
+            devb[n].copy_(host[n], non_blocking=True)
+        res = vs.run_round(d_in, devb["tgt"].view(-1, wl.V), g["tgt_row_off"], g["sps"],
+                           g["b_lo"], g["b_step"], wl.K, 9000 + i, sched_mode=wl.sched_mode,
+                           bufs={"draft": bufs["draft"], "ws_draft": bufs["ws_draft"],
+                                 "ws_verify": bufs["ws_verify"]})
+        v, s = res["verify"], res["sched"]
+        outs["out_tok"].copy_(v["out_tok"], non_blocking=True)
+        outs["accept_len"].copy_(v["accept_len"], non_blocking=True)
+        outs["n_out"].copy_(v["n_out"], non_blocking=True)
+        outs["stats"].copy_(s["stats"], non_blocking=True)
+        torch.cuda.synchronize()
+        return wl.R * wl.gamma + float(outs["stats"][1])
+
+    one(-1)
+    t0 = time.perf_counter()
+    pos = sum(one(i) for i in range(steps))
+    sec = time.perf_counter() - t0
+    return {"value": pos / sec, "unit": "positions/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

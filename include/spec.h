@@ -1,0 +1,252 @@
+/*
+ * spec.h -- C ABI of the GB300 speculative-decoding round library (libspec.so).
+ *
+ * One speculative round for R concurrent requests and a draft block of gamma
+ * positions over a vocabulary of V tokens, in three stages:
+ *
+ *   spec_draft_sample  semi-autoregressive Markov draft head, sampling,
+ *                      confidence head with sequential temperature scaling and
+ *                      survival products
+ *   spec_schedule      hardware-aware prefix scheduler (sorted survivals,
+ *                      greedy admission while tau * SPS(B) rises, top-K cap)
+ *   spec_verify        lossless rejection-sampling verification (residual
+ *                      resample, bonus token) or greedy argmax matching
+ *
+ * Sources: "DSpark: Confidence-Scheduled Speculative Decoding with
+ * Semi-Autoregressive Generation" (summary article, adg.csdn.net) and the
+ * speculative-decoding history article (wzjinhao.cn/news/15713); the citations
+ * at each entry point name the section.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers to caller-owned memory, row-major,
+ *    index order (request, position, vocabulary).  Positions j are 1-based in
+ *    the text and 0-based in memory (slot j-1).
+ *  - Argument structs are HOST memory, read only during the call.
+ *  - Every call is asynchronous on `stream`; none synchronises the host and
+ *    none allocates device memory.  Scratch memory is the caller's `workspace`
+ *    buffer of at least spec_workspace_bytes(...) bytes, 256-byte aligned; two
+ *    calls that run at the same time need separate workspaces.
+ *  - Return value: SPEC_OK or an SPEC_ERR_* code.  Argument errors are found
+ *    on the host before anything is launched.  SPEC_ERR_CUDA reports a launch
+ *    error (cudaGetLastError) -- the stream may hold a partial round then.
+ *  - Data errors found on the device (a token id outside [0, V), an l_r outside
+ *    [0, gamma], a non-finite survival) set bits in the optional device word
+ *    `status` (OR-ed, never cleared by the library); the kernels clamp the bad
+ *    value and carry on, so a bad input never faults the GPU.
+ *  - Randomness: one counter-based Philox-4x32-10 stream (Salmon et al., SC'11).
+ *    Counter = (v / 4, position j, request_id_base + r, purpose), key = (seed
+ *    low 32 bits, seed high 32 bits); vocabulary entry v uses output word v % 4,
+ *    mapped to the uniform (2 * (word >> 9) + 1) * 2^-24 in (0, 1).  Purposes:
+ *    0 draft Gumbel, 1 accept test (word 0 of block 0), 2 residual Gumbel,
+ *    3 bonus Gumbel.  Results depend only on (seed, global request id,
+ *    position), so a batch split into pieces with matching request_id_base
+ *    gives identical results.
+ *  - The library keeps no global state; calls are thread-safe.
+ */
+#ifndef SPEC_H
+#define SPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *spec_stream_t;
+
+enum spec_status_code {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* null pointer, bad size or enum value          */
+  SPEC_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement  */
+  SPEC_ERR_ALIGNMENT = 3,   /* a pointer is not aligned as documented        */
+  SPEC_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required    */
+  SPEC_ERR_CUDA = 5         /* a CUDA runtime call or launch failed          */
+};
+
+enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 };
+enum spec_verify_mode { SPEC_VERIFY_SAMPLE = 0, SPEC_VERIFY_GREEDY = 1 };
+enum spec_sched_mode { SPEC_SCHED_EARLY_STOP = 0, SPEC_SCHED_GLOBAL = 1 };
+enum spec_stage { SPEC_STAGE_DRAFT = 0, SPEC_STAGE_SCHEDULE = 1, SPEC_STAGE_VERIFY = 2 };
+
+/* Bits of the device status word. */
+#define SPEC_STATUS_BAD_TOKEN 0x1u    /* a token id was outside [0, V)          */
+#define SPEC_STATUS_BAD_ELL 0x2u      /* an l_r was outside [0, gamma]          */
+#define SPEC_STATUS_BAD_SURVIVAL 0x4u /* a survival was negative or not finite  */
+#define SPEC_STATUS_BAD_ROW 0x8u      /* a target row index was negative        */
+
+/* ------------------------------------------------------------------ draft -
+ * DSpark summary, "第二阶段：轻量顺序头" (sequential Markov head) and the
+ * history article, "杀招一": for k = 1..gamma, sequentially,
+ *     z_k = (U_k + B_k(x_{k-1})) / T_k,   B_k(x) = A_k[x, :] C_k,
+ *     P_k = softmax(z_k),  x_k ~ P_k  (Gumbel-max with the purpose-0 stream),
+ * x_0 = the anchor token x0[r].  DSpark summary, "2.1 置信度头": the
+ * confidence c_k = sigmoid((w . [h_k ; W1[x_{k-1}]]) / tau_k) with the
+ * per-position temperature tau_k of sequential temperature scaling, and the
+ * history article, "杀招二": survival a_{r,j} = prod_{i<=j} c_{r,i}.
+ *
+ * Layouts (dtype in brackets):
+ *   U      [R, gamma, V]   logit_dtype   parallel-backbone logits U_k
+ *   A      [gamma, V, r]   fac_dtype     left factor, row x = A_k[x, :]
+ *   Ct     [gamma, V, r]   fac_dtype     right factor C_k stored TRANSPOSED
+ *                                        (vocabulary-major): Ct[k][v][i] = C_k[i][v]
+ *   x0     [R] int32       anchor tokens
+ *   draft_temp [gamma] f32 T_k (> 0)
+ *   h      [R, gamma, d]   conf_dtype    backbone hidden states h_k
+ *   W1     [V, e]          conf_dtype    Markov embedding table
+ *   w      [d + e]         conf_dtype    confidence-head weights (no bias)
+ *   sts_temp [gamma] f32   tau_k (> 0)
+ * Outputs (f32 unless noted):
+ *   x [R, gamma] int32 sampled tokens; q_tok = P_k[x_k]; lse_q = log sum exp z_k;
+ *   c, a [R, gamma]; P_out [R, gamma, V] (nullable) the full draft distributions.
+ * Sizes: R >= 1, 1 <= gamma <= 64, 1 <= V < 2^30, 1 <= r <= 256, d >= 0, e >= 0,
+ * R * gamma * V < 2^40.  Alignment: every pointer aligned to its element size.
+ */
+typedef struct spec_draft_args {
+  int R, gamma, V, r, d, e;
+  int logit_dtype; /* spec_dtype of U                 */
+  int fac_dtype;   /* spec_dtype of A and Ct          */
+  int conf_dtype;  /* spec_dtype of h, W1 and w       */
+  uint32_t request_id_base;
+  const void *U;
+  const void *A;
+  const void *Ct;
+  const int32_t *x0;
+  const float *draft_temp;
+  const void *h;
+  const void *W1;
+  const void *w;
+  const float *sts_temp;
+  int32_t *x;
+  float *q_tok;
+  float *lse_q;
+  float *c;
+  float *a;
+  float *P_out;
+  void *workspace;
+  size_t workspace_bytes;
+  uint32_t *status; /* nullable device word */
+} spec_draft_args;
+
+int spec_draft_sample(const spec_draft_args *args, uint64_t seed, spec_stream_t stream);
+
+/* --------------------------------------------------------------- schedule -
+ * DSpark summary, "2.2 硬件感知前缀调度器": maximise Theta = tau * SPS(B),
+ * B = sum_r (1 + l_r), tau = sum_r sum_{j<=l_r} a_{r,j}, by sorting all
+ * R * gamma survivals in descending order and admitting them one at a time
+ * while Theta rises (early stop), cost O(gamma R log gamma R); the history
+ * article, "杀招三", walks through the same rule.  DSpark summary, "挑战2":
+ * the number admitted is capped by K (top-K from older confidences) and a
+ * global search over all sorted prefixes may replace the early stop.
+ *
+ *   a       [R, gamma] f32  survivals (>= 0; non-increasing in j for a
+ *                            prefix-closed result)
+ *   sps     [n_sps] f32     SPS(B) at B_i = b_lo + i * b_step (b_step > 0);
+ *                            linear interpolation inside, clamped outside
+ *   K       cap on sum_r l_r (>= 0)
+ *   mode    SPEC_SCHED_EARLY_STOP: admit while Theta_{n+1} > Theta_n (strict),
+ *           Theta_0 = 0;  SPEC_SCHED_GLOBAL: n = smallest argmax_n Theta_n
+ * Sort order: a descending, then request ascending, then position ascending.
+ * tau and Theta are computed in fp64.
+ * Outputs: ell [R] int32; row_off [R + 1] int32 with row_off[r + 1] = row_off[r]
+ * + 1 + l_r (the packed verify layout); stats [4] f64 = {n, B, tau, Theta};
+ * order [R * gamma] int32 (nullable) = candidate ids r * gamma + j - 1 in
+ * sorted order.  Sizes: R * gamma <= 8192 (one thread block).
+ */
+typedef struct spec_sched_args {
+  int R, gamma;
+  const float *a;
+  const float *sps;
+  int n_sps;
+  double b_lo, b_step;
+  int K;
+  int mode;
+  int32_t *ell;
+  int32_t *row_off;
+  double *stats;
+  int32_t *order;
+  void *workspace;
+  size_t workspace_bytes;
+  uint32_t *status;
+} spec_sched_args;
+
+int spec_schedule(const spec_sched_args *args, spec_stream_t stream);
+
+/* ----------------------------------------------------------------- verify -
+ * History article, "1.1运行机制" (rejection sampling): accept x_j with
+ * probability min(1, p(x_j) / q(x_j)) -- the test is u < p/q with u from the
+ * purpose-1 stream -- and discard the rest of the draft after the first
+ * rejection; DSpark summary, Figure 1: the rejected position j* is
+ * regenerated, here from norm(max(0, p - q)) (Gumbel-max over the residual,
+ * purpose 2; from p itself if the residual is zero everywhere), which makes
+ * the round lossless ("数学上的美感").  When all l_r admitted positions are
+ * accepted, one bonus token is sampled from target row l_r + 1 (purpose 3),
+ * the "1 +" of B in DSpark "2.2".  SPEC_VERIFY_GREEDY accepts while x_j is the
+ * target argmax (lowest index on ties) and emits the target argmax of the
+ * first mismatching row (or of row l_r + 1).
+ *
+ *   tgt      target logits rows [*, V] (tgt_dtype); the row of (r, j),
+ *            j = 1..l_r + 1, is tgt_row_off[r] + j - 1.  This fits a packed
+ *            [B, V] batch (tgt_row_off = row_off of spec_schedule) and a padded
+ *            [R, gamma + 1, V] layout (tgt_row_off[r] = r * (gamma + 1)).
+ *   ell [R], x [R, gamma] int32; q_tok, lse_q [R, gamma] f32 (from the draft)
+ *   p = softmax(L / target_temp)  (target_temp > 0; unused in greedy mode)
+ *   draft    the draft call's arguments (U, A, Ct, x0, draft_temp, r, dtypes):
+ *            the residual recomputes q at row j*.  May be NULL in greedy mode.
+ * Outputs: accept_len [R]; out_tok [R, gamma + 1] = accepted draft tokens, then
+ * the regenerated or bonus token, then -1; n_out [R] = accept_len + 1.
+ * Optional (nullable): p_tok [R, gamma] = p(x_j) for j <= l_r (others 0),
+ * lse_t [R, gamma + 1] = log sum exp(L_j / target_temp) of the rows read
+ * (sample mode; others 0).
+ */
+typedef struct spec_verify_args {
+  int mode;
+  int R, gamma, V;
+  int tgt_dtype;
+  uint32_t request_id_base;
+  const void *tgt;
+  const int32_t *tgt_row_off;
+  const int32_t *ell;
+  const int32_t *x;
+  const float *q_tok;
+  const float *lse_q;
+  float target_temp;
+  const spec_draft_args *draft;
+  int32_t *accept_len;
+  int32_t *out_tok;
+  int32_t *n_out;
+  float *p_tok;
+  float *lse_t;
+  void *workspace;
+  size_t workspace_bytes;
+  uint32_t *status;
+} spec_verify_args;
+
+int spec_verify(const spec_verify_args *args, uint64_t seed, spec_stream_t stream);
+
+/* ------------------------------------------------------------ stream ----
+ * The library's random stream, as the kernels draw it (see "Randomness" above):
+ * u_out[v] = uniform of vocabulary entry v at (position j, global request id
+ * rid, purpose) for v < V, and e_out[v] (nullable) = -ln(u_out[v]) as the
+ * sampling kernels compute it (an Exp(1) variate; Gumbel noise is -ln e).
+ * Lets a caller reproduce or audit any draw.  V >= 1; outputs are device f32.
+ */
+int spec_stream_uniforms(uint64_t seed, uint32_t j, uint32_t rid, uint32_t purpose, int V,
+                         float *u_out, float *e_out, spec_stream_t stream);
+
+/* Workspace bytes a stage needs for these sizes (0 if the sizes are invalid).
+ * `stage` is a spec_stage; r is ignored by SCHEDULE and VERIFY-greedy. */
+size_t spec_workspace_bytes(int stage, int R, int gamma, int V, int r);
+
+/* Static, NUL-terminated text for a status code. */
+const char *spec_error_string(int code);
+
+/* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
+int spec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_H */

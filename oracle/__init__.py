@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.orc_gumbel_argmax.restype = i32
         L.orc_sps_lookup.argtypes = [P, i32, f64, f64, f64]
         L.orc_sps_lookup.restype = f64
+        L.orc_accept_prob.argtypes = [i32, P, P]
+        L.orc_accept_prob.restype = f64
         L.orc_draft.argtypes = [i32, i32, i32, i32, P, i64, P, P, P, P, u64, u32, P, P, P, P, P, P]
         L.orc_draft.restype = i32
         L.orc_confidence.argtypes = [i32, i32, i32, i32, i32, P, i64, P, P, P, P, P, P, P]
@@ -111,6 +113,13 @@ def gumbel_argmax(logw, seed: int, j: int, rid: int, purpose: int):
 def sps_lookup(sps, b_lo: float, b_step: float, B: float) -> float:
     s = _f64(sps)
     return lib().orc_sps_lookup(_ptr(s), s.size, b_lo, b_step, B)
+
+
+def accept_prob(zt, zq) -> float:
+    """sum_v min(softmax(zt)_v, softmax(zq)_v): acceptance probability of one draft token."""
+    a, b = _f64(zt), _f64(zq)
+    assert a.size == b.size
+    return lib().orc_accept_prob(a.size, _ptr(a), _ptr(b))
 
 
 # ----------------------------------------------------------------- draft ----

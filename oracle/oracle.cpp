@@ -173,6 +173,17 @@ double orc_sps_lookup(const double* sps, int n_sps, double b_lo, double b_step, 
   return sps_lookup(sps, n_sps, b_lo, b_step, B);
 }
 
+// [DSpark] "2.1 置信度头": the acceptance probability of a token drawn from q
+// and verified against p is c* = 1 - (1/2) ||p - q||_1 = sum_v min(p_v, q_v),
+// with p = softmax(zt), q = softmax(zq).
+double orc_accept_prob(int V, const double* zt, const double* zq) {
+  std::vector<double> a(zt, zt + V), b(zq, zq + V);
+  const double la = log_sum_exp(a), lb = log_sum_exp(b);
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += std::min(std::exp(a[(size_t)v] - la), std::exp(b[(size_t)v] - lb));
+  return s;
+}
+
 // ------------------------------------------------------------------ draft ---
 // [DSpark] "第二阶段：轻量顺序头"; [History] "杀招一".  For every request r and
 // k = 1..gamma (sequential in k):

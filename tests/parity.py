@@ -1,0 +1,133 @@
+"""Comparison of the CUDA path with the oracle, stage by stage.
+
+Rules (from the method's statement of correctness):
+  * token ids, accept lengths, l_r: bit-exact, except decisions whose oracle
+    margin (Gumbel top-2 score gap, |u - p/q|, relative Theta gap) is below
+    NEAR_TIE; those are counted and the request is excluded downstream;
+  * probabilities and confidences: within PROB_TOL absolute (fp32 path; the
+    arithmetic is fp32 on exactly upcast bf16 inputs, so one tolerance serves
+    both input dtypes); log-sum-exp values within PROB_TOL relative.
+Stage isolation: every oracle stage is fed the CUDA path's outputs of the
+previous stage (draft tokens, survivals, l_r), so each stage is compared on its
+own decisions.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle
+
+NEAR_TIE = 1e-6
+PROB_TOL = 1e-5
+
+
+@dataclass
+class Report:
+    checked: int = 0
+    near_ties: int = 0
+    notes: list = field(default_factory=list)
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+def compare_draft(inp: dict, out: dict, seed: int, reqs, rid_base: int = 0, rep=None) -> Report:
+    rep = rep or Report()
+    A, Ct = to_np(inp["A"]), to_np(inp["Ct"])
+    x_gpu = to_np(out["x"])
+    for r in reqs:
+        od = oracle.draft(to_np(inp["U"][r:r + 1]), A, Ct, to_np(inp["x0"][r:r + 1]),
+                          to_np(inp["draft_temp"]), seed, rid_base=rid_base + r,
+                          x_cond=x_gpu[r:r + 1], want_P="P" in out)
+        same = od.x[0] == x_gpu[r]
+        tie = od.gap[0] < NEAR_TIE
+        assert np.all(same | tie), (r, od.x[0], x_gpu[r], od.gap[0])
+        rep.near_ties += int(np.sum(~same & tie))
+        rep.checked += len(same)
+        q = to_np(out["q_tok"][r])
+        lse = to_np(out["lse_q"][r])
+        ok = same  # values of a near-tie row refer to different tokens
+        assert np.all(np.abs(q - od.q_tok[0])[ok] < PROB_TOL), (r, q, od.q_tok[0])
+        assert np.all((np.abs(lse - od.lse[0]) / np.maximum(1, np.abs(od.lse[0])))[ok] < PROB_TOL)
+        if "P" in out:
+            assert np.abs(to_np(out["P"][r]) - od.P[0]).max() < PROB_TOL
+    return rep
+
+
+def compare_confidence(inp: dict, out: dict, reqs) -> None:
+    sl = list(reqs)
+    c, a = oracle.confidence(to_np(inp["h"][sl]), to_np(inp["W1"]), to_np(inp["w"]),
+                             to_np(inp["x0"][sl]), to_np(out["x"][sl]), to_np(inp["sts_temp"]))
+    assert np.abs(c - to_np(out["c"][sl])).max() < PROB_TOL
+    assert np.abs(a - to_np(out["a"][sl])).max() < PROB_TOL
+
+
+def compare_schedule(inp: dict, a_gpu: torch.Tensor, sched: dict, K: int, mode: int,
+                     rep=None) -> Report:
+    rep = rep or Report()
+    os_ = oracle.schedule(to_np(a_gpu).astype(np.float64), to_np(inp["sps"]).astype(np.float64),
+                          inp["b_lo"], inp["b_step"], K, mode)
+    stats = to_np(sched["stats"])
+    if os_.margin < NEAR_TIE:
+        rep.near_ties += 1
+        rep.notes.append(f"schedule near-tie margin {os_.margin:.3g}")
+        return rep
+    assert (to_np(sched["ell"]) == os_.ell).all()
+    assert (to_np(sched["row_off"]) == os_.row_off).all()
+    assert int(stats[0]) == os_.n and int(stats[1]) == os_.B
+    assert abs(stats[2] - os_.tau) <= 1e-9 * max(1.0, abs(os_.tau))
+    assert abs(stats[3] - os_.theta) <= 1e-9 * max(1.0, abs(os_.theta))
+    if "order" in sched:
+        assert (to_np(sched["order"]) == os_.order).all()
+    rep.checked += 1
+    return rep
+
+
+def compare_verify(inp: dict, d_out: dict, ell: torch.Tensor, v_out: dict, seed: int, mode: int,
+                   reqs, target_temp: float = 1.0, rid_base: int = 0, rep=None) -> Report:
+    rep = rep or Report()
+    tgt_all = inp["tgt"]
+    V = tgt_all.shape[-1]
+    G = (d_out["x"] if d_out is not None else inp["x"]).shape[1]
+    row_off = to_np(inp["tgt_row_off"])
+    ellv = to_np(ell)
+    if mode != oracle.MODE_GREEDY:
+        A, Ct, temps = to_np(inp["A"]), to_np(inp["Ct"]), to_np(inp["draft_temp"])
+    for r in reqs:
+        rows = to_np(tgt_all.reshape(-1, V)[row_off[r]: row_off[r] + ellv[r] + 1])
+        x = to_np((d_out["x"] if d_out is not None else inp["x"])[r:r + 1])
+        if mode == oracle.MODE_GREEDY:
+            ov = oracle.verify(mode, rows, np.array([0]), ellv[r:r + 1], x, np.ones((1, G)), 1.0,
+                               None, None, None, np.zeros(1, np.int32), np.ones(G), seed,
+                               rid_base=rid_base + r)
+        else:
+            ov = oracle.verify(mode, rows, np.array([0]), ellv[r:r + 1], x,
+                               to_np(d_out["q_tok"][r:r + 1]).astype(np.float64), target_temp,
+                               to_np(inp["U"][r:r + 1]), A, Ct,
+                               to_np(inp["x0"][r:r + 1]), temps, seed,
+                               rid_base=rid_base + r)
+        got = to_np(v_out["out_tok"][r])
+        if ov.margin[0] < NEAR_TIE and not (got == ov.out_tok[0]).all():
+            rep.near_ties += 1
+            rep.notes.append(f"verify near-tie r={r} margin={ov.margin[0]:.3g}")
+            continue
+        assert (got == ov.out_tok[0]).all(), (r, got, ov.out_tok[0], ov.margin[0])
+        assert int(v_out["accept_len"][r]) == ov.accept_len[0]
+        assert int(v_out["n_out"][r]) == ov.n_out[0]
+        rep.checked += 1
+        if "p_tok" in v_out and mode == oracle.MODE_SAMPLE:
+            z = rows.astype(np.float64) / target_temp
+            m = z.max(axis=1, keepdims=True)
+            lse = (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
+            lse_gpu = to_np(v_out["lse_t"][r])[: ellv[r] + 1]
+            assert np.all(np.abs(lse_gpu - lse) / np.maximum(1, np.abs(lse)) < PROB_TOL)
+            for j in range(1, ellv[r] + 1):
+                p = np.exp(z[j - 1, x[0, j - 1]] - lse[j - 1])
+                assert abs(float(v_out["p_tok"][r, j - 1]) - p) < PROB_TOL
+    return rep

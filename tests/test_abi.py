@@ -1,0 +1,127 @@
+"""The C ABI library loads and exports every symbol include/spec.h declares; the
+ctypes mirrors of the argument structs match the C layout; host-side argument
+checks reject bad calls before any CUDA work (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec.h")
+
+
+@pytest.fixture(scope="module")
+def spec():
+    import verify_sampling_gb300 as vs
+    if not os.path.exists(vs.LIB_PATH):
+        from verify_sampling_gb300 import build
+        build.build()
+    return vs
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(spec):
+    names = _declared_functions()
+    assert {"spec_draft_sample", "spec_schedule", "spec_verify", "spec_workspace_bytes",
+            "spec_error_string", "spec_stream_uniforms", "spec_version"} <= set(names)
+    lib = spec.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", spec.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (spec_\w+)", out))
+    assert set(names) == exported
+
+
+def test_struct_layout_matches_c(spec, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "spec.h"\n'
+        "#define P(T, f) printf(#T \".\" #f \" %zu\\n\", offsetof(T, f));\n"
+        "int main(void){\n"
+        'printf("spec_draft_args %zu\\n", sizeof(spec_draft_args));\n'
+        'printf("spec_sched_args %zu\\n", sizeof(spec_sched_args));\n'
+        'printf("spec_verify_args %zu\\n", sizeof(spec_verify_args));\n'
+        "P(spec_draft_args, status) P(spec_draft_args, workspace_bytes) P(spec_draft_args, U)\n"
+        "P(spec_sched_args, b_lo) P(spec_sched_args, stats) P(spec_sched_args, status)\n"
+        "P(spec_verify_args, target_temp) P(spec_verify_args, draft) P(spec_verify_args, status)\n"
+        "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True,
+                                                         text=True).stdout.splitlines())
+    assert int(got["spec_draft_args"]) == ctypes.sizeof(spec.DraftArgs)
+    assert int(got["spec_sched_args"]) == ctypes.sizeof(spec.SchedArgs)
+    assert int(got["spec_verify_args"]) == ctypes.sizeof(spec.VerifyArgs)
+    for key, (cls, field) in {"spec_draft_args.status": (spec.DraftArgs, "status"),
+                              "spec_draft_args.workspace_bytes": (spec.DraftArgs, "workspace_bytes"),
+                              "spec_draft_args.U": (spec.DraftArgs, "U"),
+                              "spec_sched_args.b_lo": (spec.SchedArgs, "b_lo"),
+                              "spec_sched_args.stats": (spec.SchedArgs, "stats"),
+                              "spec_sched_args.status": (spec.SchedArgs, "status"),
+                              "spec_verify_args.target_temp": (spec.VerifyArgs, "target_temp"),
+                              "spec_verify_args.draft": (spec.VerifyArgs, "draft"),
+                              "spec_verify_args.status": (spec.VerifyArgs, "status")}.items():
+        assert int(got[key]) == getattr(cls, field).offset, key
+
+
+def test_error_strings_and_version(spec):
+    lib = spec.lib()
+    assert lib.spec_version() >= 10000
+    for code in range(6):
+        assert lib.spec_error_string(code)
+    assert b"unknown" in lib.spec_error_string(99)
+
+
+def test_workspace_sizes(spec):
+    assert spec.workspace_bytes(spec.STAGE_SCHEDULE, 64, 8, 1000) == 0
+    d = spec.workspace_bytes(spec.STAGE_DRAFT, 512, 11, 129280, 128)
+    v = spec.workspace_bytes(spec.STAGE_VERIFY, 512, 11, 129280)
+    assert d > 0 and d % 256 == 0 and v > 0 and v % 256 == 0
+    assert spec.workspace_bytes(spec.STAGE_DRAFT, 0, 11, 129280, 128) == 0
+    assert spec.workspace_bytes(spec.STAGE_DRAFT, 4, 11, 100, 257) == 0   # rank > 256
+    assert spec.workspace_bytes(7, 4, 4, 100, 8) == 0
+
+
+def test_host_side_rejections_launch_nothing(spec):
+    lib = spec.lib()
+    assert lib.spec_draft_sample(None, 0, None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_schedule(None, None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify(None, 0, None) == spec.SPEC_ERR_INVALID_ARG
+    a = spec.DraftArgs()
+    a.R, a.gamma, a.V, a.r = 4, 4, 100, 8
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG  # nulls
+    a.gamma = 65
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    s = spec.SchedArgs()
+    s.R, s.gamma, s.n_sps, s.b_step, s.K = 100, 100, 1, 1.0, 5
+    s.a = s.sps = s.ell = s.row_off = s.stats = ctypes.c_void_p(256)
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_UNSUPPORTED  # 10^4 > 8192
+    s.gamma, s.b_step = 2, 0.0
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_INVALID_ARG
+    s.b_step = 1.0
+    s.stats = ctypes.c_void_p(260)  # not 8-byte aligned
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_ALIGNMENT
+    v = spec.VerifyArgs()
+    v.mode, v.R, v.gamma, v.V = 0, 2, 2, 10
+    v.tgt = v.tgt_row_off = v.ell = v.x = v.accept_len = v.out_tok = v.n_out = ctypes.c_void_p(256)
+    v.target_temp = 1.0
+    assert lib.spec_verify(ctypes.byref(v), 0, None) == spec.SPEC_ERR_INVALID_ARG  # no draft
+    v.mode = 7
+    assert lib.spec_verify(ctypes.byref(v), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_stream_uniforms(0, 1, 0, 0, 0, None, None, None) == spec.SPEC_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(spec, monkeypatch):
+    monkeypatch.setattr(spec, "_lib", None)
+    monkeypatch.setattr(spec, "LIB_PATH", "/nonexistent/libspec.so")
+    with pytest.raises(spec.SpecError):
+        spec.lib()

@@ -213,3 +213,27 @@ def test_figure1_round():
         assert v.accept_len[0] == exp["accept_len"] and v.n_out[0] == exp["n_out"]
         assert list(v.out_tok[0, :2]) == exp["emitted_prefix"]
         assert v.out_tok[0, 2] != exp["rejected_token"] and v.jstar[0] == 3
+
+
+def test_accept_prob_closed_form_matches_frequency():
+    """orc_accept_prob is 1 - TV(p, q); pinned by the acceptance frequency of the
+    oracle's own verifier over independent rounds and by the TV identity."""
+    rng = np.random.default_rng(21)
+    V = 9
+    U, D, A, Ct = _markov_draft_inputs(rng, V, 1)
+    t1 = rng.normal(0, 1.0, size=V).astype(np.float32)
+    zq = U[0].astype(np.float64) + D[0, 0].astype(np.float64)
+    cstar = oracle.accept_prob(t1.astype(np.float64), zq)
+    p, q = softmax(t1.astype(np.float64)), softmax(zq)
+    assert abs(cstar - (1 - 0.5 * np.abs(p - q).sum())) < 1e-14
+    R = 400_000
+    x0 = np.zeros(R, np.int32)
+
+    def tgt_fn(x):
+        tgt = np.zeros((x.shape[0], 2, V), np.float32)
+        tgt[:, 0] = t1
+        return tgt
+
+    _, v = _round(U, A, Ct, x0, tgt_fn, 1, seed=31, rid_base=0)
+    freq = (v.accept_len == 1).mean()
+    assert abs(freq - cstar) < 5 * np.sqrt(cstar * (1 - cstar) / R)

@@ -1,0 +1,311 @@
+"""verify_sampling_gb300 -- Python binding of libspec, the sm_103a CUDA library
+for the batched speculative-decoding round (draft / schedule / verify).
+
+The binding only marshals arguments: it checks tensor shapes and dtypes,
+allocates output and workspace tensors with torch (device memory and streams
+are all torch is used for), fills the C argument structs of ``include/spec.h``
+and calls the library.  Every step of the computation runs in the library's
+CUDA kernels.  There is no CPU fallback: if ``libspec.so`` is missing, every
+call raises.
+
+Entry points mirror the C ABI: :func:`draft_sample`, :func:`schedule`,
+:func:`verify`, plus :func:`run_round` that chains the three on one stream
+without a host synchronisation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspec.so")
+
+SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_ALIGNMENT, SPEC_ERR_WORKSPACE, \
+    SPEC_ERR_CUDA = range(6)
+SPEC_F32, SPEC_BF16 = 0, 1
+VERIFY_SAMPLE, VERIFY_GREEDY = 0, 1
+SCHED_EARLY_STOP, SCHED_GLOBAL = 0, 1
+STAGE_DRAFT, STAGE_SCHEDULE, STAGE_VERIFY = 0, 1, 2
+STATUS_BAD_TOKEN, STATUS_BAD_ELL, STATUS_BAD_SURVIVAL, STATUS_BAD_ROW = 0x1, 0x2, 0x4, 0x8
+
+_P = ctypes.c_void_p
+
+
+class DraftArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int), ("gamma", ctypes.c_int), ("V", ctypes.c_int), ("r", ctypes.c_int),
+                ("d", ctypes.c_int), ("e", ctypes.c_int), ("logit_dtype", ctypes.c_int),
+                ("fac_dtype", ctypes.c_int), ("conf_dtype", ctypes.c_int),
+                ("request_id_base", ctypes.c_uint32),
+                ("U", _P), ("A", _P), ("Ct", _P), ("x0", _P), ("draft_temp", _P), ("h", _P),
+                ("W1", _P), ("w", _P), ("sts_temp", _P), ("x", _P), ("q_tok", _P), ("lse_q", _P),
+                ("c", _P), ("a", _P), ("P_out", _P), ("workspace", _P),
+                ("workspace_bytes", ctypes.c_size_t), ("status", _P)]
+
+
+class SchedArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int), ("gamma", ctypes.c_int), ("a", _P), ("sps", _P),
+                ("n_sps", ctypes.c_int), ("b_lo", ctypes.c_double), ("b_step", ctypes.c_double),
+                ("K", ctypes.c_int), ("mode", ctypes.c_int), ("ell", _P), ("row_off", _P),
+                ("stats", _P), ("order", _P), ("workspace", _P),
+                ("workspace_bytes", ctypes.c_size_t), ("status", _P)]
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("R", ctypes.c_int), ("gamma", ctypes.c_int),
+                ("V", ctypes.c_int), ("tgt_dtype", ctypes.c_int),
+                ("request_id_base", ctypes.c_uint32), ("tgt", _P), ("tgt_row_off", _P),
+                ("ell", _P), ("x", _P), ("q_tok", _P), ("lse_q", _P),
+                ("target_temp", ctypes.c_float), ("draft", ctypes.POINTER(DraftArgs)),
+                ("accept_len", _P), ("out_tok", _P), ("n_out", _P), ("p_tok", _P), ("lse_t", _P),
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("status", _P)]
+
+
+class SpecError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libspec.so (built in-tree by ``build.py``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise SpecError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; "
+                            "g.build()'` (there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.spec_draft_sample.argtypes = [ctypes.POINTER(DraftArgs), ctypes.c_uint64, _P]
+        L.spec_schedule.argtypes = [ctypes.POINTER(SchedArgs), _P]
+        L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_uint64, _P]
+        for f in (L.spec_draft_sample, L.spec_schedule, L.spec_verify):
+            f.restype = ctypes.c_int
+        L.spec_workspace_bytes.argtypes = [ctypes.c_int] * 5
+        L.spec_workspace_bytes.restype = ctypes.c_size_t
+        L.spec_error_string.argtypes = [ctypes.c_int]
+        L.spec_error_string.restype = ctypes.c_char_p
+        L.spec_version.restype = ctypes.c_int
+        L.spec_stream_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                           ctypes.c_uint32, ctypes.c_int, _P, _P, _P]
+        L.spec_stream_uniforms.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != SPEC_OK:
+        raise SpecError(f"{what}: {lib().spec_error_string(rc).decode()} (code {rc})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_bytes(stage: int, R: int, gamma: int, V: int, r: int = 1) -> int:
+    return int(lib().spec_workspace_bytes(stage, R, gamma, V, r))
+
+
+def _workspace(nbytes: int, device, given: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    if given is not None:
+        if given.numel() * given.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return given
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def stream_uniforms(seed: int, j: int, rid: int, purpose: int, V: int, device="cuda",
+                    stream=None):
+    """spec_stream_uniforms: (u, -ln u) of vocabulary entries 0..V-1 for one draw site."""
+    u = torch.empty(V, dtype=torch.float32, device=device)
+    e = torch.empty(V, dtype=torch.float32, device=device)
+    _check(lib().spec_stream_uniforms(seed & 0xFFFFFFFFFFFFFFFF, j, rid, purpose, V, _ptr(u),
+                                      _ptr(e), _stream_handle(stream)), "spec_stream_uniforms")
+    return u, e
+
+
+# -------------------------------------------------------------------- draft --
+@dataclass
+class DraftInputs:
+    """Inputs of the draft stage (device tensors; see include/spec.h for layouts)."""
+    U: torch.Tensor            # [R, gamma, V]
+    A: torch.Tensor            # [gamma, V, r]
+    Ct: torch.Tensor           # [gamma, V, r]  C_k transposed (vocabulary-major)
+    x0: torch.Tensor           # [R] int32
+    draft_temp: torch.Tensor   # [gamma] f32
+    h: torch.Tensor            # [R, gamma, d]
+    W1: torch.Tensor           # [V, e]
+    w: torch.Tensor            # [d + e]
+    sts_temp: torch.Tensor     # [gamma] f32
+    request_id_base: int = 0
+
+
+def _draft_struct(inp: DraftInputs, outs: dict, ws: Optional[torch.Tensor], status) -> DraftArgs:
+    U, A, Ct = (_dev(inp.U, "U"), _dev(inp.A, "A"), _dev(inp.Ct, "Ct"))
+    R, gamma, V = U.shape
+    r = A.shape[2]
+    if A.shape != (gamma, V, r) or Ct.shape != (gamma, V, r) or A.dtype != Ct.dtype:
+        raise ValueError("A and Ct must both be [gamma, V, r] of one dtype")
+    h, W1, w = _dev(inp.h, "h"), _dev(inp.W1, "W1"), _dev(inp.w, "w")
+    d, e = h.shape[2], W1.shape[1]
+    if h.shape[:2] != (R, gamma) or W1.shape[0] != V or w.numel() != d + e:
+        raise ValueError("confidence-head shapes do not match")
+    if not (h.dtype == W1.dtype == w.dtype):
+        raise ValueError("h, W1 and w must share one dtype")
+    for name, t, dt in (("x0", inp.x0, torch.int32), ("draft_temp", inp.draft_temp, torch.float32),
+                        ("sts_temp", inp.sts_temp, torch.float32)):
+        if _dev(t, name).dtype != dt:
+            raise TypeError(f"{name} must be {dt}")
+    a = DraftArgs()
+    a.R, a.gamma, a.V, a.r, a.d, a.e = R, gamma, V, r, d, e
+    a.logit_dtype, a.fac_dtype, a.conf_dtype = _dtype_code(U), _dtype_code(A), _dtype_code(h)
+    a.request_id_base = inp.request_id_base
+    a.U, a.A, a.Ct, a.x0, a.draft_temp = _ptr(U), _ptr(A), _ptr(Ct), _ptr(inp.x0), _ptr(inp.draft_temp)
+    a.h, a.W1, a.w, a.sts_temp = _ptr(h), _ptr(W1), _ptr(w), _ptr(inp.sts_temp)
+    if outs:
+        a.x, a.q_tok, a.lse_q = _ptr(outs["x"]), _ptr(outs["q_tok"]), _ptr(outs["lse_q"])
+        a.c, a.a, a.P_out = _ptr(outs["c"]), _ptr(outs["a"]), _ptr(outs.get("P"))
+    a.workspace = _ptr(ws)
+    a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    a.status = _ptr(status)
+    return a
+
+
+def draft_outputs(R: int, gamma: int, V: int, device, want_P: bool = False) -> dict:
+    f = dict(dtype=torch.float32, device=device)
+    outs = {"x": torch.empty(R, gamma, dtype=torch.int32, device=device),
+            "q_tok": torch.empty(R, gamma, **f), "lse_q": torch.empty(R, gamma, **f),
+            "c": torch.empty(R, gamma, **f), "a": torch.empty(R, gamma, **f)}
+    if want_P:
+        outs["P"] = torch.empty(R, gamma, V, **f)
+    return outs
+
+
+def draft_sample(inp: DraftInputs, seed: int, *, want_P: bool = False, out: Optional[dict] = None,
+                 workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                 stream=None) -> dict:
+    """spec_draft_sample: sample x_1..x_gamma, q(x_k), lse_k, confidences and survivals."""
+    R, gamma, V = inp.U.shape
+    r = inp.A.shape[2]
+    outs = out if out is not None else draft_outputs(R, gamma, V, inp.U.device, want_P)
+    ws = _workspace(workspace_bytes(STAGE_DRAFT, R, gamma, V, r), inp.U.device, workspace)
+    a = _draft_struct(inp, outs, ws, status)
+    _check(lib().spec_draft_sample(ctypes.byref(a), seed & 0xFFFFFFFFFFFFFFFF, _stream_handle(stream)),
+           "spec_draft_sample")
+    return outs
+
+
+# ----------------------------------------------------------------- schedule --
+def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: int,
+             mode: int = SCHED_EARLY_STOP, *, want_order: bool = False, out: Optional[dict] = None,
+             status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """spec_schedule: l_r, packed row offsets and {n, B, tau, Theta} on the device."""
+    a = _dev(a, "a")
+    sps = _dev(sps, "sps")
+    if a.dtype != torch.float32 or sps.dtype != torch.float32:
+        raise TypeError("a and sps must be float32")
+    R, gamma = a.shape
+    dev = a.device
+    outs = out if out is not None else {
+        "ell": torch.empty(R, dtype=torch.int32, device=dev),
+        "row_off": torch.empty(R + 1, dtype=torch.int32, device=dev),
+        "stats": torch.empty(4, dtype=torch.float64, device=dev)}
+    if want_order and "order" not in outs:
+        outs["order"] = torch.empty(R * gamma, dtype=torch.int32, device=dev)
+    s = SchedArgs()
+    s.R, s.gamma = R, gamma
+    s.a, s.sps, s.n_sps = _ptr(a), _ptr(sps), sps.numel()
+    s.b_lo, s.b_step, s.K, s.mode = float(b_lo), float(b_step), int(K), int(mode)
+    s.ell, s.row_off, s.stats = _ptr(outs["ell"]), _ptr(outs["row_off"]), _ptr(outs["stats"])
+    s.order = _ptr(outs.get("order"))
+    s.status = _ptr(status)
+    _check(lib().spec_schedule(ctypes.byref(s), _stream_handle(stream)), "spec_schedule")
+    return outs
+
+
+# ------------------------------------------------------------------- verify --
+def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.Tensor,
+           x: torch.Tensor, seed: int, *, q_tok: Optional[torch.Tensor] = None,
+           lse_q: Optional[torch.Tensor] = None, target_temp: float = 1.0,
+           draft: Optional[DraftInputs] = None, request_id_base: int = 0, want_p: bool = False,
+           out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+           status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """spec_verify: accept lengths and emitted tokens (sample or greedy mode)."""
+    tgt = _dev(tgt, "tgt")
+    x = _dev(x, "x")
+    R, gamma = x.shape
+    V = tgt.shape[-1]
+    dev = tgt.device
+    outs = out if out is not None else {
+        "accept_len": torch.empty(R, dtype=torch.int32, device=dev),
+        "out_tok": torch.empty(R, gamma + 1, dtype=torch.int32, device=dev),
+        "n_out": torch.empty(R, dtype=torch.int32, device=dev)}
+    if want_p and "p_tok" not in outs:
+        outs["p_tok"] = torch.empty(R, gamma, dtype=torch.float32, device=dev)
+        outs["lse_t"] = torch.empty(R, gamma + 1, dtype=torch.float32, device=dev)
+    ws = _workspace(workspace_bytes(STAGE_VERIFY, R, gamma, V), dev, workspace)
+    v = VerifyArgs()
+    v.mode, v.R, v.gamma, v.V, v.tgt_dtype = int(mode), R, gamma, V, _dtype_code(tgt)
+    v.request_id_base = request_id_base
+    v.tgt, v.tgt_row_off, v.ell, v.x = _ptr(tgt), _ptr(_dev(tgt_row_off, "tgt_row_off")), \
+        _ptr(_dev(ell, "ell")), _ptr(x)
+    v.q_tok, v.lse_q = _ptr(q_tok), _ptr(lse_q)
+    v.target_temp = float(target_temp)
+    keep = None
+    if draft is not None:
+        keep = _draft_struct(draft, {}, None, None)
+        v.draft = ctypes.pointer(keep)
+    v.accept_len, v.out_tok, v.n_out = _ptr(outs["accept_len"]), _ptr(outs["out_tok"]), \
+        _ptr(outs["n_out"])
+    v.p_tok, v.lse_t = _ptr(outs.get("p_tok")), _ptr(outs.get("lse_t"))
+    v.workspace = _ptr(ws)
+    v.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    v.status = _ptr(status)
+    _check(lib().spec_verify(ctypes.byref(v), seed & 0xFFFFFFFFFFFFFFFF, _stream_handle(stream)),
+           "spec_verify")
+    del keep
+    return outs
+
+
+# -------------------------------------------------------------------- round --
+def run_round(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.Tensor,
+              sps: torch.Tensor, b_lo: float, b_step: float, K: int, seed: int, *,
+              sched_mode: int = SCHED_EARLY_STOP, target_temp: float = 1.0,
+              bufs: Optional[dict] = None, stream=None) -> dict:
+    """One full round -- draft, schedule, verify -- on one stream, no host sync."""
+    bufs = {} if bufs is None else bufs
+    d = draft_sample(draft_in, seed, out=bufs.get("draft"), workspace=bufs.get("ws_draft"),
+                     status=bufs.get("status"), stream=stream)
+    s = schedule(d["a"], sps, b_lo, b_step, K, sched_mode, out=bufs.get("sched"),
+                 status=bufs.get("status"), stream=stream)
+    v = verify(VERIFY_SAMPLE, tgt, tgt_row_off, s["ell"], d["x"], seed, q_tok=d["q_tok"],
+               lse_q=d["lse_q"], target_temp=target_temp, draft=draft_in,
+               request_id_base=draft_in.request_id_base, out=bufs.get("verify"),
+               workspace=bufs.get("ws_verify"), status=bufs.get("status"), stream=stream)
+    return {"draft": d, "sched": s, "verify": v}

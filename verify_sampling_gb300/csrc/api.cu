@@ -1,0 +1,262 @@
+// C-ABI entry points of libspec: argument validation, workspace carving and
+// kernel launches.  Every check happens on the host before anything is
+// launched; no call synchronises the host or allocates device memory.
+#include <cstdint>
+
+#include "draft.cuh"
+#include "schedule.cuh"
+#include "verify.cuh"
+
+namespace {
+
+using namespace spec;
+
+constexpr int kMaxGridY = 65535;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool valid_dtype(int d) { return d == SPEC_F32 || d == SPEC_BF16; }
+size_t dtype_size(int d) { return d == SPEC_F32 ? 4 : 2; }
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t draft_scratch_bytes(int R, int V) {
+  const size_t ns = (size_t)draft_nsplit(R, V);
+  return align256((size_t)R * ns * sizeof(Partial)) + align256((size_t)R * sizeof(unsigned));
+}
+
+bool draft_sizes_ok(int R, int gamma, int V, int r) {
+  return R >= 1 && R <= kMaxGridY && gamma >= 1 && gamma <= kMaxGamma && V >= 1 &&
+         V < (1 << 30) && r >= 1 && r <= kMaxRank &&
+         (double)R * gamma * V < 1099511627776.0;  // 2^40
+}
+
+bool verify_sizes_ok(int R, int gamma, int V) {
+  return R >= 1 && R <= kMaxGridY && gamma >= 1 && gamma + 1 <= kMaxGridY && V >= 1 &&
+         V < (1 << 30) && (double)R * (gamma + 1) * V < 1099511627776.0;
+}
+
+int check_draft_args(const spec_draft_args* a) {
+  if (!a) return SPEC_ERR_INVALID_ARG;
+  if (!draft_sizes_ok(a->R, a->gamma, a->V, a->r) || a->d < 0 || a->e < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (!valid_dtype(a->logit_dtype) || !valid_dtype(a->fac_dtype) || !valid_dtype(a->conf_dtype))
+    return SPEC_ERR_INVALID_ARG;
+  if (!a->U || !a->A || !a->Ct || !a->x0 || !a->draft_temp || !a->x || !a->q_tok || !a->lse_q)
+    return SPEC_ERR_INVALID_ARG;
+  if (!a->sts_temp || !a->c || !a->a) return SPEC_ERR_INVALID_ARG;
+  if ((a->d > 0 && !a->h) || (a->e > 0 && !a->W1) || (a->d + a->e > 0 && !a->w))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t ls = dtype_size(a->logit_dtype), fs = dtype_size(a->fac_dtype),
+               cs = dtype_size(a->conf_dtype);
+  if (!aligned(a->U, ls) || !aligned(a->A, fs) || !aligned(a->Ct, fs) || !aligned(a->x0, 4) ||
+      !aligned(a->draft_temp, 4) || !aligned(a->x, 4) || !aligned(a->q_tok, 4) ||
+      !aligned(a->lse_q, 4) || !aligned(a->sts_temp, 4) || !aligned(a->c, 4) ||
+      !aligned(a->a, 4) || !aligned(a->P_out, 4) || !aligned(a->h, cs) || !aligned(a->W1, cs) ||
+      !aligned(a->w, cs) || !aligned(a->status, 4))
+    return SPEC_ERR_ALIGNMENT;
+  return SPEC_OK;
+}
+
+int check_workspace(void* ws, size_t have, size_t need) {
+  if (need == 0) return SPEC_OK;
+  if (!ws || have < need) return SPEC_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return SPEC_ERR_ALIGNMENT;
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* spec_error_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "success";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument (null pointer, size or enum value)";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case SPEC_ERR_ALIGNMENT: return "pointer not aligned as required";
+    case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status code";
+  }
+}
+
+size_t spec_workspace_bytes(int stage, int R, int gamma, int V, int r) {
+  switch (stage) {
+    case SPEC_STAGE_DRAFT:
+      return draft_sizes_ok(R, gamma, V, r) ? draft_scratch_bytes(R, V) : 0;
+    case SPEC_STAGE_SCHEDULE:
+      return 0;
+    case SPEC_STAGE_VERIFY:
+      return verify_sizes_ok(R, gamma, V) ? verify_scratch_bytes(R, gamma, V) : 0;
+    default:
+      return 0;
+  }
+}
+
+int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t stream) {
+  int rc = check_draft_args(args);
+  if (rc != SPEC_OK) return rc;
+  const spec_draft_args& a = *args;
+  const size_t need = draft_scratch_bytes(a.R, a.V);
+  rc = check_workspace(a.workspace, a.workspace_bytes, need);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const int nsplit = draft_nsplit(a.R, a.V);
+  char* ws = static_cast<char*>(a.workspace);
+  DraftStepParams p{};
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.V = a.V;
+  p.rank = a.r;
+  p.nsplit = nsplit;
+  p.rid_base = a.request_id_base;
+  p.key = philox_key(seed);
+  p.U = a.U;
+  p.A = a.A;
+  p.Ct = a.Ct;
+  p.x0 = a.x0;
+  p.draft_temp = a.draft_temp;
+  p.x = a.x;
+  p.q_tok = a.q_tok;
+  p.lse_q = a.lse_q;
+  p.P_out = a.P_out;
+  p.partials = reinterpret_cast<Partial*>(ws);
+  const size_t cnt_off = align256((size_t)a.R * nsplit * sizeof(Partial));
+  p.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
+  p.status = a.status;
+  if (cudaMemsetAsync(p.counters, 0, (size_t)a.R * sizeof(unsigned), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (launch_draft_steps(p, a.logit_dtype, a.fac_dtype, a.P_out != nullptr, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+
+  ConfParams c{};
+  c.R = a.R;
+  c.gamma = a.gamma;
+  c.V = a.V;
+  c.d = a.d;
+  c.e = a.e;
+  c.x0 = a.x0;
+  c.x = a.x;
+  c.h = a.h;
+  c.W1 = a.W1;
+  c.w = a.w;
+  c.sts_temp = a.sts_temp;
+  c.c = a.c;
+  c.a = a.a;
+  c.status = a.status;
+  if (launch_confidence(c, a.conf_dtype, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+int spec_schedule(const spec_sched_args* args, spec_stream_t stream) {
+  if (!args) return SPEC_ERR_INVALID_ARG;
+  const spec_sched_args& a = *args;
+  if (a.R < 1 || a.gamma < 1 || a.n_sps < 1 || a.K < 0 ||
+      (a.mode != SPEC_SCHED_EARLY_STOP && a.mode != SPEC_SCHED_GLOBAL) || !(a.b_step > 0.0) ||
+      !(a.b_step < 1e300) || !(a.b_lo > -1e300 && a.b_lo < 1e300))
+    return SPEC_ERR_INVALID_ARG;
+  if (!a.a || !a.sps || !a.ell || !a.row_off || !a.stats) return SPEC_ERR_INVALID_ARG;
+  if ((long)a.R * a.gamma > kSchedMaxCandidates) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned(a.a, 4) || !aligned(a.sps, 4) || !aligned(a.ell, 4) || !aligned(a.row_off, 4) ||
+      !aligned(a.stats, 8) || !aligned(a.order, 4) || !aligned(a.status, 4))
+    return SPEC_ERR_ALIGNMENT;
+  SchedParams p{};
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.n_sps = a.n_sps;
+  p.K = a.K;
+  p.mode = a.mode;
+  p.b_lo = a.b_lo;
+  p.b_step = a.b_step;
+  p.a = a.a;
+  p.sps = a.sps;
+  p.ell = a.ell;
+  p.row_off = a.row_off;
+  p.stats = a.stats;
+  p.order = a.order;
+  p.status = a.status;
+  return launch_schedule(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK
+                                                                                    : SPEC_ERR_CUDA;
+}
+
+int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t stream) {
+  if (!args) return SPEC_ERR_INVALID_ARG;
+  const spec_verify_args& a = *args;
+  if (a.mode != SPEC_VERIFY_SAMPLE && a.mode != SPEC_VERIFY_GREEDY) return SPEC_ERR_INVALID_ARG;
+  if (!verify_sizes_ok(a.R, a.gamma, a.V) || !valid_dtype(a.tgt_dtype)) return SPEC_ERR_INVALID_ARG;
+  if (!a.tgt || !a.tgt_row_off || !a.ell || !a.x || !a.accept_len || !a.out_tok || !a.n_out)
+    return SPEC_ERR_INVALID_ARG;
+  const bool sample = a.mode == SPEC_VERIFY_SAMPLE;
+  int fac_dtype = SPEC_BF16, logit_dtype = SPEC_BF16, rank = 1;
+  if (sample) {
+    if (!a.q_tok || !a.lse_q || !a.draft || !(a.target_temp > 0.f) || !(a.target_temp < 1e30f))
+      return SPEC_ERR_INVALID_ARG;
+    const spec_draft_args& d = *a.draft;
+    if (d.R != a.R || d.gamma != a.gamma || d.V != a.V || d.r < 1 || d.r > kMaxRank ||
+        !valid_dtype(d.logit_dtype) || !valid_dtype(d.fac_dtype) || !d.U || !d.A || !d.Ct ||
+        !d.x0 || !d.draft_temp)
+      return SPEC_ERR_INVALID_ARG;
+    if (d.request_id_base != a.request_id_base) return SPEC_ERR_INVALID_ARG;
+    fac_dtype = d.fac_dtype;
+    logit_dtype = d.logit_dtype;
+    rank = d.r;
+    if (!aligned(d.U, dtype_size(logit_dtype)) || !aligned(d.A, dtype_size(fac_dtype)) ||
+        !aligned(d.Ct, dtype_size(fac_dtype)) || !aligned(d.x0, 4) || !aligned(d.draft_temp, 4) ||
+        !aligned(a.q_tok, 4) || !aligned(a.lse_q, 4))
+      return SPEC_ERR_ALIGNMENT;
+  }
+  if (!aligned(a.tgt, dtype_size(a.tgt_dtype)) || !aligned(a.tgt_row_off, 4) || !aligned(a.ell, 4) ||
+      !aligned(a.x, 4) || !aligned(a.accept_len, 4) || !aligned(a.out_tok, 4) ||
+      !aligned(a.n_out, 4) || !aligned(a.p_tok, 4) || !aligned(a.lse_t, 4) || !aligned(a.status, 4))
+    return SPEC_ERR_ALIGNMENT;
+  const size_t need = verify_scratch_bytes(a.R, a.gamma, a.V);
+  int rc = check_workspace(a.workspace, a.workspace_bytes, need);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  VerifyParams p{};
+  p.mode = a.mode;
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.V = a.V;
+  p.nsplit = verify_nsplit(a.R, a.gamma, a.V);
+  p.rank = rank;
+  p.rid_base = a.request_id_base;
+  p.key = philox_key(seed);
+  p.inv_target_temp = sample ? 1.0f / a.target_temp : 1.0f;
+  p.tgt = a.tgt;
+  p.tgt_row_off = a.tgt_row_off;
+  p.ell = a.ell;
+  p.x = a.x;
+  p.q_tok = a.q_tok;
+  p.lse_q = a.lse_q;
+  if (sample) {
+    p.U = a.draft->U;
+    p.A = a.draft->A;
+    p.Ct = a.draft->Ct;
+    p.x0 = a.draft->x0;
+    p.draft_temp = a.draft->draft_temp;
+  }
+  p.accept_len = a.accept_len;
+  p.out_tok = a.out_tok;
+  p.n_out = a.n_out;
+  p.p_tok = a.p_tok;
+  p.lse_t = a.lse_t;
+  p.status = a.status;
+  size_t cnt_off = 0, cnt_bytes = 0;
+  p.ws = verify_scratch_carve(a.workspace, a.R, a.gamma, a.V, &cnt_off, &cnt_bytes);
+  if (cudaMemsetAsync(static_cast<char*>(a.workspace) + cnt_off, 0, cnt_bytes, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (a.p_tok && cudaMemsetAsync(a.p_tok, 0, (size_t)a.R * a.gamma * sizeof(float), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (a.lse_t &&
+      cudaMemsetAsync(a.lse_t, 0, (size_t)a.R * (a.gamma + 1) * sizeof(float), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (launch_verify(p, a.tgt_dtype, logit_dtype, fac_dtype, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+}  // extern "C"

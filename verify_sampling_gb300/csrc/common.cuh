@@ -1,0 +1,271 @@
+// Device building blocks shared by the sm_103a kernels of libspec.
+//
+//  * Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+//    32x32->64 multiplies of words 0 and 2, with a Weyl key schedule.
+//  * Gumbel-max in "exponential race" form: argmax_v (z_v + G_v) with
+//    G_v = -ln(E_v), E_v = -ln(u_v), equals argmax_v exp(z_v - m) / E_v for any
+//    shift m.  The kernels keep exp(z - m) (already needed for the softmax sum)
+//    and compare candidates by cross-multiplication, so no second logarithm and
+//    no division appear in the streaming loop.
+//  * Online softmax state (running max m, sum s of exp(z - m)).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "spec.h"
+
+namespace spec {
+
+constexpr uint32_t kPurposeDraft = 0;
+constexpr uint32_t kPurposeAccept = 1;
+constexpr uint32_t kPurposeResidual = 2;
+constexpr uint32_t kPurposeBonus = 3;
+
+// ----------------------------------------------------------------- Philox --
+struct PhiloxKey {
+  uint32_t lo, hi;
+};
+
+__host__ __device__ inline PhiloxKey philox_key(uint64_t seed) {
+  return PhiloxKey{(uint32_t)(seed & 0xffffffffull), (uint32_t)(seed >> 32)};
+}
+
+// One Philox-4x32-10 block for counter (w0, w1, w2, w3).
+__device__ __forceinline__ uint4 philox(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                        PhiloxKey key) {
+  uint32_t k0 = key.lo, k1 = key.hi;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t p0_lo = 0xD2511F53u * w0;
+    const uint32_t p0_hi = __umulhi(0xD2511F53u, w0);
+    const uint32_t p1_lo = 0xCD9E8D57u * w2;
+    const uint32_t p1_hi = __umulhi(0xCD9E8D57u, w2);
+    w0 = p1_hi ^ w1 ^ k0;
+    w1 = p1_lo;
+    w2 = p0_hi ^ w3 ^ k1;
+    w3 = p0_lo;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint4(w0, w1, w2, w3);
+}
+
+__device__ __forceinline__ uint32_t word_of(uint4 b, int lane) {
+  return lane == 0 ? b.x : lane == 1 ? b.y : lane == 2 ? b.z : b.w;
+}
+
+// Uniform (2*(x>>9)+1) * 2^-24 in (0,1): the bit pattern 1.m (m = x>>9) is
+// 1 + m*2^-23; subtracting 1 - 2^-24 leaves (2m+1)*2^-24, which is representable,
+// so the subtraction is exact.
+__device__ __forceinline__ float uniform_from_word(uint32_t x) {
+  return __uint_as_float(0x3f800000u | (x >> 9)) - 0.99999994f;
+}
+
+// E = -ln(u) > 0, an Exp(1) variate.  logf is accurate to about one ulp of its
+// result, which keeps E accurate relative to itself even for u near 1 (u - 1
+// is exact there).
+__device__ __forceinline__ float neg_log_uniform(uint32_t x) { return -logf(uniform_from_word(x)); }
+
+// ------------------------------------------------------------ races/state --
+// Gumbel race + online softmax over a stream of logits z.
+struct Race {
+  float m;   // running max of z
+  float s;   // sum of exp(z - m)
+  float be;  // exp(z_best - m)
+  float bE;  // E of the best candidate
+  int idx;   // best candidate (-1: none yet)
+};
+
+__device__ __forceinline__ Race race_empty() { return Race{-CUDART_INF_F, 0.f, 0.f, 1.f, -1}; }
+
+// Does candidate (e1/E1, i1) beat (e2/E2, i2)?  Lower index wins exact ties.
+__device__ __forceinline__ bool race_beats(float e1, float E1, int i1, float e2, float E2, int i2) {
+  if (i1 < 0) return false;
+  if (i2 < 0) return true;
+  const float l = e1 * E2, r = e2 * E1;
+  return l > r || (l == r && i1 < i2);
+}
+
+__device__ __forceinline__ void race_push(Race& st, float z, float E, int v) {
+  if (!(z > -CUDART_INF_F)) return;  // -inf (masked) or NaN never wins
+  if (z > st.m) {
+    const float sc = expf(st.m - z);
+    st.s *= sc;
+    st.be *= sc;
+    st.m = z;
+  }
+  const float e = expf(z - st.m);
+  st.s += e;
+  if (race_beats(e, E, v, st.be, st.bE, st.idx)) {
+    st.be = e;
+    st.bE = E;
+    st.idx = v;
+  }
+}
+
+__device__ __forceinline__ Race race_merge(const Race& a, const Race& b) {
+  if (b.idx < 0) return a;
+  if (a.idx < 0) return b;
+  const float m = fmaxf(a.m, b.m);
+  const float sa = expf(a.m - m), sb = expf(b.m - m);
+  Race o;
+  o.m = m;
+  o.s = a.s * sa + b.s * sb;
+  const float ea = a.be * sa, eb = b.be * sb;
+  if (race_beats(ea, a.bE, a.idx, eb, b.bE, b.idx)) {
+    o.be = ea;
+    o.bE = a.bE;
+    o.idx = a.idx;
+  } else {
+    o.be = eb;
+    o.bE = b.bE;
+    o.idx = b.idx;
+  }
+  return o;
+}
+
+__device__ __forceinline__ Race race_shfl_down(const Race& st, int off) {
+  Race o;
+  o.m = __shfl_down_sync(0xffffffffu, st.m, off);
+  o.s = __shfl_down_sync(0xffffffffu, st.s, off);
+  o.be = __shfl_down_sync(0xffffffffu, st.be, off);
+  o.bE = __shfl_down_sync(0xffffffffu, st.bE, off);
+  o.idx = __shfl_down_sync(0xffffffffu, st.idx, off);
+  return o;
+}
+
+// Online softmax only (m, s).
+struct Soft {
+  float m, s;
+};
+__device__ __forceinline__ Soft soft_empty() { return Soft{-CUDART_INF_F, 0.f}; }
+__device__ __forceinline__ void soft_push(Soft& st, float z) {
+  if (!(z > -CUDART_INF_F)) return;
+  if (z > st.m) {
+    st.s *= expf(st.m - z);
+    st.m = z;
+  }
+  st.s += expf(z - st.m);
+}
+__device__ __forceinline__ Soft soft_merge(const Soft& a, const Soft& b) {
+  if (!(b.m > -CUDART_INF_F)) return a;
+  if (!(a.m > -CUDART_INF_F)) return b;
+  const float m = fmaxf(a.m, b.m);
+  return Soft{m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+}
+
+// Weighted race without a softmax: argmax_v w_v / E_v over w_v > 0.
+struct WRace {
+  float bw, bE;
+  int idx;
+};
+__device__ __forceinline__ WRace wrace_empty() { return WRace{0.f, 1.f, -1}; }
+__device__ __forceinline__ void wrace_push(WRace& st, float w, float E, int v) {
+  if (!(w > 0.f)) return;
+  if (race_beats(w, E, v, st.bw, st.bE, st.idx)) {
+    st.bw = w;
+    st.bE = E;
+    st.idx = v;
+  }
+}
+__device__ __forceinline__ WRace wrace_merge(const WRace& a, const WRace& b) {
+  return race_beats(b.bw, b.bE, b.idx, a.bw, a.bE, a.idx) ? b : a;
+}
+
+// Argmax with lowest index on ties.
+struct ArgMax {
+  float val;
+  int idx;
+};
+__device__ __forceinline__ ArgMax argmax_empty() { return ArgMax{-CUDART_INF_F, -1}; }
+__device__ __forceinline__ void argmax_push(ArgMax& st, float v, int i) {
+  if (st.idx < 0 || v > st.val || (v == st.val && i < st.idx)) {
+    st.val = v;
+    st.idx = i;
+  }
+}
+__device__ __forceinline__ ArgMax argmax_merge(const ArgMax& a, const ArgMax& b) {
+  if (b.idx < 0) return a;
+  if (a.idx < 0) return b;
+  if (b.val > a.val || (b.val == a.val && b.idx < a.idx)) return b;
+  return a;
+}
+
+// Workspace record for one partial result (32 bytes).
+struct alignas(32) Partial {
+  float f0, f1, f2, f3;
+  int i0;
+  float f4, f5;
+  int i1;
+};
+
+// Read a partial published by another CTA (L2, bypassing L1).
+__device__ __forceinline__ Partial load_partial(const Partial* p) {
+  const int4* q = reinterpret_cast<const int4*>(p);
+  int4 a = __ldcg(q), b = __ldcg(q + 1);
+  Partial o;
+  o.f0 = __int_as_float(a.x);
+  o.f1 = __int_as_float(a.y);
+  o.f2 = __int_as_float(a.z);
+  o.f3 = __int_as_float(a.w);
+  o.i0 = b.x;
+  o.f4 = __int_as_float(b.y);
+  o.f5 = __int_as_float(b.z);
+  o.i1 = b.w;
+  return o;
+}
+
+// ----------------------------------------------------------------- loads ---
+__device__ __forceinline__ float ld_f(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16* p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+
+// ---------------------------------------------------------- block helpers --
+// Block-wide merge of per-thread states; the result is valid in thread 0.
+template <typename S, typename ShflFn, typename MergeFn>
+__device__ __forceinline__ S block_reduce(S st, S* smem, ShflFn shfl, MergeFn merge) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) st = merge(st, shfl(st, off));
+  if (lane == 0) smem[warp] = st;
+  __syncthreads();
+  if (warp == 0) {
+    st = smem[lane < nwarps ? lane : 0];
+    if (lane >= nwarps) st = smem[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      S o = shfl(st, off);
+      if (lane + off < nwarps) st = merge(st, o);
+    }
+  }
+  return st;
+}
+
+// Last-block-done protocol: returns true in exactly one CTA of the group that
+// shares `counter`, after all of the group's CTAs have published their
+// partials (each CTA calls this once, after writing its partial).  The winning
+// CTA resets the counter for the next use.
+__device__ __forceinline__ bool last_block_arrives(unsigned* counter, unsigned expected) {
+  __shared__ bool is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(counter, 1u);
+    is_last = (prev == expected - 1);
+    if (is_last) *counter = 0u;
+  }
+  __syncthreads();
+  if (is_last) __threadfence();
+  return is_last;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+}  // namespace spec

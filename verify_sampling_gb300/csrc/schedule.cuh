@@ -1,0 +1,25 @@
+// Parameters and launcher of the single-block prefix scheduler (internal header).
+#pragma once
+
+#include "common.cuh"
+
+namespace spec {
+
+constexpr int kSchedMaxCandidates = 8192;  // R * gamma, one thread block
+
+struct SchedParams {
+  int R, gamma, n_sps, K, mode, npow2;
+  double b_lo, b_step;
+  const float* a;
+  const float* sps;
+  int32_t* ell;
+  int32_t* row_off;
+  double* stats;
+  int32_t* order;
+  uint32_t* status;
+};
+
+size_t schedule_smem_bytes(int R, int gamma);
+cudaError_t launch_schedule(SchedParams p, cudaStream_t stream);
+
+}  // namespace spec
