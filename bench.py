@@ -40,7 +40,7 @@ def _args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", default="c5", choices=["c2", "c3", "c5", "greedy"])
+    p.add_argument("--config", default="c5", choices=["c2", "c3", "c5", "c5p", "greedy"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     return p.parse_args()

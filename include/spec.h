@@ -75,6 +75,9 @@ enum spec_stage { SPEC_STAGE_DRAFT = 0, SPEC_STAGE_SCHEDULE = 1, SPEC_STAGE_VERI
 #define SPEC_STATUS_BAD_ELL 0x2u      /* an l_r was outside [0, gamma]          */
 #define SPEC_STATUS_BAD_SURVIVAL 0x4u /* a survival was negative or not finite  */
 #define SPEC_STATUS_BAD_ROW 0x8u      /* a target row index was negative        */
+#define SPEC_STATUS_TIMEOUT 0x10u     /* an internal pipeline wait gave up after
+                                         2 s (never expected): the call's
+                                         outputs are invalid                     */
 
 /* ------------------------------------------------------------------ draft -
  * DSpark summary, "第二阶段：轻量顺序头" (sequential Markov head) and the

@@ -80,6 +80,9 @@ WORKLOADS = {
     "c5": Workload("c5", 512, 11, 129280, 128, 2048, 128, torch.float32, torch.bfloat16,
                    torch.bfloat16, "sample", 2048, 0, "zipf", "sawtooth", 4.0, 0.0, 5),
 }
+# Profiling case: the c5 per-launch shape (R=512, V=129280, r=128, fp32) with two
+# draft positions, small enough for a multi-pass profiler capture (~1.3 GB).
+WORKLOADS["c5p"] = WORKLOADS["c5"].scaled(name="c5p", gamma=2)
 
 
 def _calibration() -> dict:

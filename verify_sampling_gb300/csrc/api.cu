@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include "draft.cuh"
+#include "draft_tc.cuh"
 #include "schedule.cuh"
 #include "verify.cuh"
 
@@ -19,9 +20,26 @@ bool valid_dtype(int d) { return d == SPEC_F32 || d == SPEC_BF16; }
 size_t dtype_size(int d) { return d == SPEC_F32 ? 4 : 2; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// Partials: the larger of the generic kernel's [R, nsplit] and the fused
+// kernel's [R, splits <= kMaxDeviceSms]; counters: one per request (generic)
+// or per 128-request tile (fused).
 size_t draft_scratch_bytes(int R, int V) {
-  const size_t ns = (size_t)draft_nsplit(R, V);
+  const size_t ns = (size_t)std::max(draft_nsplit(R, V), kMaxDeviceSms);
   return align256((size_t)R * ns * sizeof(Partial)) + align256((size_t)R * sizeof(unsigned));
+}
+
+// The fused tensor-core path needs bf16 factors with r a multiple of 64, 16-byte
+// aligned rows of U (V * element size a multiple of 16) and an sm_100-family GPU.
+bool draft_tc_ok(const spec_draft_args& a, int* sms) {
+  if (a.fac_dtype != SPEC_BF16 || a.r % 64 != 0 || a.r > 256) return false;
+  if (((size_t)a.V * dtype_size(a.logit_dtype)) % 16 != 0) return false;
+  if (!aligned(a.U, 16) || !aligned(a.A, 16) || !aligned(a.Ct, 16)) return false;
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return major == 10 && *sms >= 1 && *sms <= kMaxDeviceSms;
 }
 
 bool draft_sizes_ok(int R, int gamma, int V, int r) {
@@ -124,13 +142,41 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
   p.lse_q = a.lse_q;
   p.P_out = a.P_out;
   p.partials = reinterpret_cast<Partial*>(ws);
-  const size_t cnt_off = align256((size_t)a.R * nsplit * sizeof(Partial));
+  const size_t cnt_off =
+      align256((size_t)a.R * std::max(nsplit, kMaxDeviceSms) * sizeof(Partial));
   p.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
   p.status = a.status;
   if (cudaMemsetAsync(p.counters, 0, (size_t)a.R * sizeof(unsigned), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  if (launch_draft_steps(p, a.logit_dtype, a.fac_dtype, a.P_out != nullptr, s) != cudaSuccess)
+  int sms = 0;
+  if (draft_tc_ok(a, &sms)) {
+    DraftTCParams t{};
+    t.R = a.R;
+    t.gamma = a.gamma;
+    t.V = a.V;
+    t.rank = a.r;
+    t.mtiles = (a.R + 127) / 128;
+    t.ntiles = (a.V + 63) / 64;
+    t.nsplit = draft_tc_nsplit(a.R, a.V, sms);
+    t.rid_base = a.request_id_base;
+    t.key = p.key;
+    t.x0 = a.x0;
+    t.draft_temp = a.draft_temp;
+    t.A = a.A;
+    t.x = a.x;
+    t.q_tok = a.q_tok;
+    t.lse_q = a.lse_q;
+    t.partials = p.partials;
+    t.counters = p.counters;
+    t.status = a.status;
+    if (launch_draft_tc(t, a.logit_dtype, a.U, a.Ct, sms, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (a.P_out && launch_draft_steps(p, a.logit_dtype, a.fac_dtype, true, s, /*probs_only=*/true) !=
+                       cudaSuccess)
+      return SPEC_ERR_CUDA;
+  } else if (launch_draft_steps(p, a.logit_dtype, a.fac_dtype, a.P_out != nullptr, s) !=
+             cudaSuccess) {
     return SPEC_ERR_CUDA;
+  }
 
   ConfParams c{};
   c.R = a.R;

@@ -149,10 +149,10 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(ConfParams p) 
 // ------------------------------------------------------------- launchers --
 template <typename TL, typename TF>
 static cudaError_t launch_draft_typed(const DraftStepParams& base, bool want_probs,
-                                      cudaStream_t stream) {
+                                      bool probs_only, cudaStream_t stream) {
   DraftStepParams p = base;
   const dim3 grid((unsigned)p.nsplit, (unsigned)p.R);
-  for (int k = 1; k <= p.gamma; ++k) {
+  for (int k = 1; k <= p.gamma && !probs_only; ++k) {
     p.k = k;
     draft_step_kernel<TL, TF><<<grid, kDraftThreads, 0, stream>>>(p);
     cudaError_t err = cudaGetLastError();
@@ -168,14 +168,14 @@ static cudaError_t launch_draft_typed(const DraftStepParams& base, bool want_pro
 }
 
 cudaError_t launch_draft_steps(const DraftStepParams& p, int logit_dtype, int fac_dtype,
-                               bool want_probs, cudaStream_t stream) {
+                               bool want_probs, cudaStream_t stream, bool probs_only) {
   if (logit_dtype == SPEC_F32 && fac_dtype == SPEC_F32)
-    return launch_draft_typed<float, float>(p, want_probs, stream);
+    return launch_draft_typed<float, float>(p, want_probs, probs_only, stream);
   if (logit_dtype == SPEC_F32 && fac_dtype == SPEC_BF16)
-    return launch_draft_typed<float, __nv_bfloat16>(p, want_probs, stream);
+    return launch_draft_typed<float, __nv_bfloat16>(p, want_probs, probs_only, stream);
   if (logit_dtype == SPEC_BF16 && fac_dtype == SPEC_F32)
-    return launch_draft_typed<__nv_bfloat16, float>(p, want_probs, stream);
-  return launch_draft_typed<__nv_bfloat16, __nv_bfloat16>(p, want_probs, stream);
+    return launch_draft_typed<__nv_bfloat16, float>(p, want_probs, probs_only, stream);
+  return launch_draft_typed<__nv_bfloat16, __nv_bfloat16>(p, want_probs, probs_only, stream);
 }
 
 cudaError_t launch_confidence(const ConfParams& p, int conf_dtype, cudaStream_t stream) {

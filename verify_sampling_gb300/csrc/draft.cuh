@@ -51,8 +51,10 @@ inline int draft_nsplit(int R, int V) {
   return std::max(1, std::min(max_split, (target_ctas + R - 1) / R));
 }
 
+// gamma generic sampling steps, then (want_probs) the P_out pass; probs_only
+// skips the sampling steps (their outputs came from the fused kernel).
 cudaError_t launch_draft_steps(const DraftStepParams& p, int logit_dtype, int fac_dtype,
-                               bool want_probs, cudaStream_t stream);
+                               bool want_probs, cudaStream_t stream, bool probs_only = false);
 cudaError_t launch_confidence(const ConfParams& p, int conf_dtype, cudaStream_t stream);
 
 }  // namespace spec

@@ -1,0 +1,467 @@
+// Fused draft step on the 5th-generation tensor cores (sm_100 family).
+//
+// One launch per draft position k computes, for a tile of 128 requests and a
+// range of the vocabulary,
+//     bias[m, v] = A_k[x_{m,k-1}, :] . C_k[:, v]          (tcgen05.mma, bf16 -> f32 in TMEM)
+//     z[m, v]    = (U[m, k, v] + bias[m, v]) / T_k
+// and folds every z into a per-request online softmax (max, sum) and a Gumbel
+// race with the purpose-0 Philox stream, as the generic kernel does; no z is
+// ever written to memory.  DSpark summary, "第二阶段：轻量顺序头" and the history
+// article, "杀招一": P_k = softmax(U_k + B_k(x_{k-1})), B_k low-rank.
+//
+// CTA layout (576 threads, one CTA per SM):
+//   warps 0-15  epilogue: warp w reads TMEM lane quadrant w % 4 (32 requests)
+//               and column group w / 4 (16 of the 64 columns of a tile)
+//   warp 16     TMA producer: C_k tile [64 x r] and U tile [128 x 64] per stage
+//   warp 17     tensor-memory owner and single-thread MMA issuer
+// Pipelines: a ring of `stages` shared-memory stages (full/empty mbarriers) and
+// four 64-column TMEM accumulators (full/empty mbarriers).  The gathered A rows
+// (128 x r bf16) are written once per launch in the 128-byte swizzle layout.
+// Every wait is bounded; on a timeout the CTA sets SPEC_STATUS_TIMEOUT, drains
+// what it issued and returns.
+//
+// Gumbel race filter: a candidate can beat the current best only if
+// exp(z - m) / E > best, and E = -ln u >= 1 - u for u in (0,1), so elements
+// with exp(z - m) / (1 - u) below the best are skipped without computing the
+// logarithm.  1 - u is exact (it is the uniform of the complemented word).
+#include "draft.cuh"
+#include "draft_tc.cuh"
+#include "tc.cuh"
+
+namespace spec {
+
+namespace {
+
+constexpr int kNT = 64;             // vocabulary columns per tile (MMA N)
+constexpr int kEpiWarps = 16;       // 4 lane quadrants x 4 column groups
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kThreadsTC = (kEpiWarps + 2) * 32;
+constexpr int kTmemBufs = 4;
+constexpr uint32_t kTmemCols = kTmemBufs * kNT;
+constexpr int kMaxStages = 8;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kFilterSlack = 1.0f - 1.0f / 4194304.0f;  // 1 - 2^-22
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ Race race_shfl_xor(const Race& st, int mask) {
+  Race o;
+  o.m = __shfl_xor_sync(0xffffffffu, st.m, mask);
+  o.s = __shfl_xor_sync(0xffffffffu, st.s, mask);
+  o.be = __shfl_xor_sync(0xffffffffu, st.be, mask);
+  o.bE = __shfl_xor_sync(0xffffffffu, st.bE, mask);
+  o.idx = __shfl_xor_sync(0xffffffffu, st.idx, mask);
+  return o;
+}
+
+template <typename TL>
+struct UTile {
+  static constexpr int kBoxCols = 128 / (int)sizeof(TL);  // 128-byte rows
+  static constexpr int kBoxes = kNT / kBoxCols;
+  static constexpr uint32_t kBytes = 128u * kNT * sizeof(TL);
+};
+
+// 16 consecutive logits of `row` starting at column 16*grp of the tile.
+__device__ __forceinline__ void load_u16(const unsigned char* tile, int row, int grp, float (&u)[16],
+                                         float) {
+  const int box = grp >> 1, c0 = (grp & 1) * 4;
+  const unsigned char* base = tile + box * 16384 + row * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 f = *reinterpret_cast<const float4*>(base + (((c0 + j) ^ (row & 7)) << 4));
+    u[4 * j] = f.x;
+    u[4 * j + 1] = f.y;
+    u[4 * j + 2] = f.z;
+    u[4 * j + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void load_u16(const unsigned char* tile, int row, int grp, float (&u)[16],
+                                         __nv_bfloat16) {
+  const unsigned char* base = tile + row * 128;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 q = *reinterpret_cast<const uint4*>(base + (((grp * 2 + j) ^ (row & 7)) << 4));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      u[8 * j + 2 * h] = __uint_as_float(w[h] << 16);
+      u[8 * j + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+    }
+  }
+}
+
+}  // namespace
+
+template <typename TL, int KC>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    draft_tc_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_c,
+                    DraftTCParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kCBytes = KC * kNT * 128;
+  constexpr uint32_t kUBytes = UTile<TL>::kBytes;
+  constexpr uint32_t kStageBytes = kCBytes + kUBytes;
+  unsigned char* sA = smem;
+  unsigned char* sStage = smem + KC * 16384;
+
+  __shared__ __align__(8) uint64_t full_c[kMaxStages], full_u[kMaxStages], empty_s[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull[kTmemBufs], tempty[kTmemBufs];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ Race grp_state[3][128];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mtile = blockIdx.x % p.mtiles, split = blockIdx.x / p.mtiles;
+  const int m0 = mtile * 128;
+  const int t_begin = (int)((long)split * p.ntiles / p.nsplit);
+  const int t_end = (int)((long)(split + 1) * p.ntiles / p.nsplit);
+  const int T = t_end - t_begin;
+  const int S = p.stages;
+  const int k = p.k;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full_c[s], 1);
+      tc::mbar_init(&full_u[s], 1);
+      tc::mbar_init(&empty_s[s], 1 + kEpiWarps);
+    }
+    for (int b = 0; b < kTmemBufs; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], kEpiWarps);
+    }
+    abort_flag = 0;
+    tc::fence_barrier_init();
+    tc::fence_proxy_async();
+  }
+  if (warp == kMmaWarp) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  if (warp == kProducerWarp && lane == 0) {
+    tc::tma_prefetch_desc(&tm_u);
+    tc::tma_prefetch_desc(&tm_c);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  // The next position's grid may start its prologue and its U / C loads on SMs
+  // that this grid frees; it waits (griddepcontrol.wait) before reading x.
+  tc::grid_dep_launch();
+
+  auto fail = [&]() {
+    abort_flag = 1;
+    set_status(p.status, SPEC_STATUS_TIMEOUT);
+  };
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int t = 0; t < T && !abort_flag; ++t) {
+        const int s = t % S;
+        const uint32_t ph = (uint32_t)(t / S) & 1u;
+        if (!tc::mbar_wait(&empty_s[s], ph ^ 1u, kWaitNs)) {
+          fail();
+          break;
+        }
+        unsigned char* st = sStage + s * kStageBytes;
+        const int n0 = (t_begin + t) * kNT;
+        tc::mbar_expect_tx(&full_c[s], kCBytes);
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) tc::tma_load_3d(st + kc * 8192, &tm_c, &full_c[s], kc * 64, n0, k - 1);
+        tc::mbar_expect_tx(&full_u[s], kUBytes);
+#pragma unroll
+        for (int bx = 0; bx < UTile<TL>::kBoxes; ++bx)
+          tc::tma_load_3d(st + kCBytes + bx * 16384, &tm_u, &full_u[s], n0 + bx * UTile<TL>::kBoxCols,
+                          k - 1, m0);
+        issued = t + 1;
+      }
+      if (abort_flag) {
+        // drain: the last load issued into each stage must land before exit
+        for (int t = (issued > S ? issued - S : 0); t < issued; ++t) {
+          const uint32_t ph = (uint32_t)(t / S) & 1u;
+          tc::mbar_wait(&full_c[t % S], ph, kWaitNs);
+          tc::mbar_wait(&full_u[t % S], ph, kWaitNs);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    named_bar_sync(1, (kEpiWarps + 1) * 32);  // gathered A rows are in shared memory
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::bf16_idesc(128, kNT);
+      int last = -1;
+      for (int t = 0; t < T && !abort_flag; ++t) {
+        const int s = t % S, b = t % kTmemBufs;
+        if (!tc::mbar_wait(&full_c[s], (uint32_t)(t / S) & 1u, kWaitNs) ||
+            !tc::mbar_wait(&tempty[b], ((uint32_t)(t / kTmemBufs) & 1u) ^ 1u, kWaitNs)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const unsigned char* st = sStage + s * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < KC * 4; ++kk) {
+          const int kc = kk >> 2, ko = (kk & 3) * 32;
+          const uint64_t ad = tc::sw128_desc(tc::smem_u32(sA + kc * 16384 + ko));
+          const uint64_t bd = tc::sw128_desc(tc::smem_u32(st + kc * 8192 + ko));
+          tc::mma_bf16(tmem + (uint32_t)(b * kNT), ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&tfull[b]);
+        tc::mma_commit(&empty_s[s]);
+        last = t;
+      }
+      if (abort_flag && last >= 0)  // in-flight MMAs must finish before TMEM is freed
+        tc::mbar_wait(&tfull[last % kTmemBufs], (uint32_t)(last / kTmemBufs) & 1u, kWaitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int quad = warp & 3, grp = warp >> 2;
+    const int row = quad * 32 + lane, m = m0 + row;
+    const bool valid = m < p.R;
+    const int V = p.V, rank = p.rank, gamma = p.gamma;
+
+    tc::grid_dep_wait();  // x_{k-1} written by the previous position's grid
+    const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
+    for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
+      const int i = idx / (KC * 8), c = idx % (KC * 8);
+      uint4 val = make_uint4(0, 0, 0, 0);
+      const int mm = m0 + i;
+      if (mm < p.R) {
+        int xp = (k == 1) ? p.x0[mm] : p.x[(size_t)mm * gamma + (k - 2)];
+        if (xp < 0 || xp >= V) {
+          if (c == 0) set_status(p.status, SPEC_STATUS_BAD_TOKEN);
+          xp = 0;
+        }
+        val = *reinterpret_cast<const uint4*>(Ak + (size_t)xp * rank + c * 8);
+      }
+      const int kc = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(sA + kc * 16384 + i * 128 + ((cc ^ (i & 7)) << 4)) = val;
+    }
+    tc::fence_proxy_async();
+    named_bar_sync(1, (kEpiWarps + 1) * 32);
+
+    Race st = race_empty();
+    float be_slack = 0.f;  // st.be * (1 - 2^-22)
+    const float inv_t = 1.0f / p.draft_temp[k - 1];
+    const uint32_t rid = p.rid_base + (uint32_t)m;
+    const PhiloxKey key = p.key;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % S, b = t % kTmemBufs;
+      if (abort_flag) break;
+      if (!tc::mbar_wait(&tfull[b], (uint32_t)(t / kTmemBufs) & 1u, kWaitNs) ||
+          !tc::mbar_wait(&full_u[s], (uint32_t)(t / S) & 1u, kWaitNs)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t braw[16];
+      tc::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kNT + grp * 16), braw);
+      float u[16];
+      load_u16(sStage + s * kStageBytes + kCBytes, row, grp, u, TL());
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&tempty[b]);
+        tc::mbar_arrive(&empty_s[s]);
+      }
+      if (!valid) continue;
+      const int colbase = (t_begin + t) * kNT + grp * 16;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int v0 = colbase + 4 * q;
+        if (v0 >= V) break;
+        const uint4 bits = philox((uint32_t)(v0 >> 2), (uint32_t)k, rid, kPurposeDraft, key);
+        float z[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          z[i] = (v0 + i < V) ? (u[4 * q + i] + __uint_as_float(braw[4 * q + i])) * inv_t : -CUDART_INF_F;
+        const float mz = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+        if (mz > st.m) {
+          const float sc = tc::ex2((st.m - mz) * kLog2e);
+          st.s *= sc;
+          st.be *= sc;
+          be_slack = st.be * kFilterSlack;
+          st.m = mz;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float e = tc::ex2((z[i] - st.m) * kLog2e);
+          st.s += e;
+          const uint32_t word = word_of(bits, i);
+          const float w = uniform_from_word(~word);  // 1 - u, exact
+          if (e > 0.f && e * st.bE >= be_slack * w) {
+            const float E = -logf(uniform_from_word(word));
+            if (race_beats(e, E, v0 + i, st.be, st.bE, st.idx)) {
+              st.be = e;
+              st.bE = E;
+              st.idx = v0 + i;
+              be_slack = e * kFilterSlack;
+            }
+          }
+        }
+      }
+    }
+    // merge the four column groups of each row inside the CTA
+    if (grp > 0) grp_state[grp - 1][row] = st;
+    named_bar_sync(2, kEpiWarps * 32);
+    if (grp == 0 && valid) {
+#pragma unroll
+      for (int g = 0; g < 3; ++g) st = race_merge(st, grp_state[g][row]);
+      Partial w{};
+      w.f0 = st.m;
+      w.f1 = st.s;
+      w.f2 = st.be;
+      w.f3 = st.bE;
+      w.i0 = st.idx;
+      p.partials[(size_t)m * p.nsplit + split] = w;
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (!last_block_arrives(p.counters + mtile, (unsigned)p.nsplit)) return;
+
+  // Last CTA of this request tile: merge the partials of every split, four
+  // threads per request.
+  if (threadIdx.x < kEpiWarps * 32) {
+    const int row = threadIdx.x >> 2, part = threadIdx.x & 3, m = m0 + row;
+    Race acc = race_empty();
+    if (m < p.R)
+      for (int s = part; s < p.nsplit; s += 4) {
+        const Partial w = load_partial(p.partials + (size_t)m * p.nsplit + s);
+        acc = race_merge(acc, Race{w.f0, w.f1, w.f2, w.f3, w.i0});
+      }
+    acc = race_merge(acc, race_shfl_xor(acc, 1));
+    acc = race_merge(acc, race_shfl_xor(acc, 2));
+    if (part == 0 && m < p.R) {
+      const size_t o = (size_t)m * p.gamma + (k - 1);
+      p.x[o] = acc.idx;
+      p.q_tok[o] = acc.be / acc.s;
+      p.lse_q[o] = acc.m + logf(acc.s);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host --
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t es, const void* base, uint64_t d0,
+               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename TL, int KC>
+size_t smem_bytes(int stages) {
+  return 1024 + (size_t)KC * 16384 + (size_t)stages * (KC * kNT * 128 + UTile<TL>::kBytes);
+}
+
+template <typename TL, int KC>
+int pick_stages() {
+  const size_t budget = 227 * 1024 - 8 * 1024;  // static shared memory and slack
+  int s = kMaxStages;
+  while (s > 2 && smem_bytes<TL, KC>(s) > budget) --s;
+  return s;
+}
+
+template <typename TL, int KC>
+cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* Ct, int device_sms,
+                         cudaStream_t stream) {
+  DraftTCParams p = base;
+  CUtensorMap tm_u, tm_c;
+  const CUtensorMapDataType udt =
+      sizeof(TL) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_3d(&tm_u, udt, sizeof(TL), U, (uint64_t)p.V, (uint64_t)p.gamma, (uint64_t)p.R,
+                 UTile<TL>::kBoxCols, 1, 128) ||
+      !encode_3d(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ct, (uint64_t)p.rank, (uint64_t)p.V,
+                 (uint64_t)p.gamma, 64, kNT, 1))
+    return cudaErrorInvalidValue;
+  p.stages = pick_stages<TL, KC>();
+  const size_t smem = smem_bytes<TL, KC>(p.stages);
+  auto kern = draft_tc_kernel<TL, KC>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  (void)device_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.mtiles * p.nsplit));
+  cfg.blockDim = dim3(kThreadsTC);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  for (int k = 1; k <= p.gamma; ++k) {
+    p.k = k;
+    err = cudaLaunchKernelEx(&cfg, kern, tm_u, tm_c, p);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int draft_tc_nsplit(int R, int V, int device_sms) {
+  const int mtiles = (R + 127) / 128;
+  const int ntiles = (V + kNT - 1) / kNT;
+  int ns = std::max(1, device_sms / mtiles);
+  return std::max(1, std::min(ns, ntiles));
+}
+
+cudaError_t launch_draft_tc(const DraftTCParams& p, int logit_dtype, const void* U, const void* Ct,
+                            int device_sms, cudaStream_t stream) {
+  const int KC = p.rank / 64;
+  if (logit_dtype == SPEC_F32) {
+    switch (KC) {
+      case 1: return launch_typed<float, 1>(p, U, Ct, device_sms, stream);
+      case 2: return launch_typed<float, 2>(p, U, Ct, device_sms, stream);
+      case 3: return launch_typed<float, 3>(p, U, Ct, device_sms, stream);
+      case 4: return launch_typed<float, 4>(p, U, Ct, device_sms, stream);
+    }
+  } else {
+    switch (KC) {
+      case 1: return launch_typed<__nv_bfloat16, 1>(p, U, Ct, device_sms, stream);
+      case 2: return launch_typed<__nv_bfloat16, 2>(p, U, Ct, device_sms, stream);
+      case 3: return launch_typed<__nv_bfloat16, 3>(p, U, Ct, device_sms, stream);
+      case 4: return launch_typed<__nv_bfloat16, 4>(p, U, Ct, device_sms, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace spec

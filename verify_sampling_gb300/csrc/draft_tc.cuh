@@ -1,0 +1,33 @@
+// Fused tensor-core draft step (internal header).
+#pragma once
+
+#include "common.cuh"
+
+namespace spec {
+
+// Upper bound on the SM count the workspace is sized for.
+constexpr int kMaxDeviceSms = 256;
+
+struct DraftTCParams {
+  int R, gamma, V, rank, k, nsplit, mtiles, ntiles, stages;
+  uint32_t rid_base;
+  PhiloxKey key;
+  const int32_t* x0;
+  const float* draft_temp;
+  const void* A;  // bf16 [gamma, V, rank]
+  int32_t* x;
+  float* q_tok;
+  float* lse_q;
+  Partial* partials;   // [R, nsplit]
+  unsigned* counters;  // [mtiles], zero on entry
+  uint32_t* status;
+};
+
+// Vocabulary splits per 128-request tile for a device with `device_sms` SMs.
+int draft_tc_nsplit(int R, int V, int device_sms);
+
+// gamma dependent launches (one per position) of the fused kernel.
+cudaError_t launch_draft_tc(const DraftTCParams& p, int logit_dtype, const void* U, const void* Ct,
+                            int device_sms, cudaStream_t stream);
+
+}  // namespace spec
