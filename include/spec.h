@@ -36,7 +36,7 @@
  *  - Randomness: one counter-based Philox-4x32-10 stream (Salmon et al., SC'11).
  *    Counter = (v / 4, position j, request_id_base + r, purpose), key = (seed
  *    low 32 bits, seed high 32 bits); vocabulary entry v uses output word v % 4,
- *    mapped to the uniform (2 * (word >> 9) + 1) * 2^-24 in (0, 1).  Purposes:
+ *    mapped to the uniform (2 * (word & 0x7FFFFF) + 1) * 2^-24 in (0, 1).  Purposes:
  *    0 draft Gumbel, 1 accept test (word 0 of block 0), 2 residual Gumbel,
  *    3 bonus Gumbel.  Results depend only on (seed, global request id,
  *    position), so a batch split into pieces with matching request_id_base

@@ -61,11 +61,12 @@ void philox_block(const uint32_t counter[4], const uint32_t key[2], uint32_t out
 
 // The random stream of this library: counter = (v / 4, position j, global
 // request id, purpose), key = (seed low word, seed high word); vocabulary entry v
-// takes word v % 4.  Word x maps to the open-interval uniform (2*(x>>9)+1)*2^-24,
+// takes word v % 4.  Word x maps to the open-interval uniform
+// (2*(x & 0x7FFFFF)+1)*2^-24 (its low 23 bits),
 // which is exact in fp32 and fp64 alike.
 enum Purpose : uint32_t { kDraftGumbel = 0, kAcceptU = 1, kResidualGumbel = 2, kBonusGumbel = 3 };
 
-double uniform_from_word(uint32_t x) { return (2.0 * (double)(x >> 9) + 1.0) * 0x1p-24; }
+double uniform_from_word(uint32_t x) { return (2.0 * (double)(x & 0x7fffffu) + 1.0) * 0x1p-24; }
 
 struct Stream {
   uint32_t key[2];

@@ -27,7 +27,14 @@ SMALL = {
     "v1": synth.WORKLOADS["tiny"].scaled(R=2, gamma=1, V=1, r=1, d=3, e=1),
     "r1_gamma1": synth.WORKLOADS["c2"].scaled(R=1, gamma=1, V=4097, d=64, e=16, r=16),
     "no_cap_room": synth.WORKLOADS["c5"].scaled(R=5, gamma=4, V=999, d=16, e=8, r=8, K=0),
+    # fused tensor-core path: bf16/fp32 rows of 16-byte multiples, r in {64, 128},
+    # vocabulary ragged against the 64-column tile, R spanning two 128-request tiles
+    "tc_c2_small": synth.WORKLOADS["c2"].scaled(R=6, gamma=5, V=20000, d=256),
+    "tc_c3_small_R130": synth.WORKLOADS["c3"].scaled(R=130, gamma=3, V=4136, d=64),
+    "tc_c5_small": synth.WORKLOADS["c5"].scaled(R=8, gamma=6, V=12004, d=200),
+    "tc_c5_temp": synth.WORKLOADS["c5"].scaled(R=3, gamma=2, V=3000, d=16, r=64),
 }
+SAMPLED = {"tc_c3_small_R130": [0, 1, 2, 64, 127, 128, 129]}
 
 
 def _to_dev(inp):
@@ -52,8 +59,10 @@ def test_round_parity_small(name):
     inp = synth.make_inputs(wl, "cpu")
     g = _to_dev(inp)
     seed = 1000 + len(name)
-    d, s, v = _run(g, wl, seed, want_P=(wl.V <= 20001))
-    reqs = range(wl.R)
+    if name == "tc_c5_temp":  # non-unit draft temperatures on the fused path
+        g["draft_temp"] = torch.tensor([0.7, 1.6], device=DEV)
+    d, s, v = _run(g, wl, seed, want_P=(wl.V <= 20001 and wl.R <= 16))
+    reqs = SAMPLED.get(name, range(wl.R))
     rep = compare_draft(g, d, seed, reqs)
     compare_confidence(g, d, reqs)
     compare_schedule(g, d["a"], s, wl.K, wl.sched_mode, rep)

@@ -71,8 +71,8 @@ def test_uniform_is_open_interval_odd_multiple():
             scaled = u * 2.0 ** 24
             assert 0.0 < u < 1.0
             assert scaled == int(scaled) and int(scaled) % 2 == 1
-            # the 23 high bits of the word select the odd multiple
-            assert (int(scaled) - 1) // 2 == word >> 9
+            # the 23 low bits of the word select the odd multiple
+            assert (int(scaled) - 1) // 2 == word & 0x7FFFFF
 
 
 def test_uniform_streams_differ_by_purpose_position_request():

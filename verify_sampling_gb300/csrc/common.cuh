@@ -33,35 +33,57 @@ __host__ __device__ inline PhiloxKey philox_key(uint64_t seed) {
   return PhiloxKey{(uint32_t)(seed & 0xffffffffull), (uint32_t)(seed >> 32)};
 }
 
-// One Philox-4x32-10 block for counter (w0, w1, w2, w3).
+// Round keys of the Weyl schedule: round i uses (key.lo + i*W0, key.hi + i*W1).
+struct PhiloxRoundKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__host__ __device__ inline PhiloxRoundKeys philox_round_keys(PhiloxKey key) {
+  PhiloxRoundKeys rk;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    rk.k0[i] = key.lo + (uint32_t)i * 0x9E3779B9u;
+    rk.k1[i] = key.hi + (uint32_t)i * 0xBB67AE85u;
+  }
+  return rk;
+}
+
+// One Philox-4x32-10 block for counter (w0, w1, w2, w3).  Each round takes the
+// two 32x32 -> 64-bit products of words 0 and 2 (one wide multiply each).
 __device__ __forceinline__ uint4 philox(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                        PhiloxKey key) {
-  uint32_t k0 = key.lo, k1 = key.hi;
+                                        const PhiloxRoundKeys& rk) {
 #pragma unroll
   for (int round = 0; round < 10; ++round) {
-    const uint32_t p0_lo = 0xD2511F53u * w0;
-    const uint32_t p0_hi = __umulhi(0xD2511F53u, w0);
-    const uint32_t p1_lo = 0xCD9E8D57u * w2;
-    const uint32_t p1_hi = __umulhi(0xCD9E8D57u, w2);
-    w0 = p1_hi ^ w1 ^ k0;
-    w1 = p1_lo;
-    w2 = p0_hi ^ w3 ^ k1;
-    w3 = p0_lo;
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    const uint64_t p0 = (uint64_t)0xD2511F53u * w0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * w2;
+    w0 = (uint32_t)(p1 >> 32) ^ w1 ^ rk.k0[round];
+    w1 = (uint32_t)p1;
+    w2 = (uint32_t)(p0 >> 32) ^ w3 ^ rk.k1[round];
+    w3 = (uint32_t)p0;
   }
   return make_uint4(w0, w1, w2, w3);
+}
+
+__device__ __forceinline__ uint4 philox(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                        PhiloxKey key) {
+  return philox(w0, w1, w2, w3, philox_round_keys(key));
 }
 
 __device__ __forceinline__ uint32_t word_of(uint4 b, int lane) {
   return lane == 0 ? b.x : lane == 1 ? b.y : lane == 2 ? b.z : b.w;
 }
 
-// Uniform (2*(x>>9)+1) * 2^-24 in (0,1): the bit pattern 1.m (m = x>>9) is
-// 1 + m*2^-23; subtracting 1 - 2^-24 leaves (2m+1)*2^-24, which is representable,
-// so the subtraction is exact.
+// Uniform (2*m+1) * 2^-24 in (0,1) with m = the low 23 bits of the word: the bit
+// pattern 1.m is 1 + m*2^-23; subtracting 1 - 2^-24 leaves (2m+1)*2^-24, which
+// is representable, so the subtraction is exact.
 __device__ __forceinline__ float uniform_from_word(uint32_t x) {
-  return __uint_as_float(0x3f800000u | (x >> 9)) - 0.99999994f;
+  return __uint_as_float(0x3f800000u | (x & 0x7fffffu)) - 0.99999994f;
+}
+
+// 1 + (1 - u) - 2^-24 as a float (exact): the pattern 1.m' of the complemented
+// low bits m' = 2^23 - 1 - m.  One logic operation.
+__device__ __forceinline__ float one_plus_w(uint32_t x) {
+  return __uint_as_float(0x3f800000u | (~x & 0x7fffffu));
 }
 
 // E = -ln(u) > 0, an Exp(1) variate.  logf is accurate to about one ulp of its

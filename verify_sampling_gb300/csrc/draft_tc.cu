@@ -4,10 +4,10 @@
 // range of the vocabulary,
 //     bias[m, v] = A_k[x_{m,k-1}, :] . C_k[:, v]          (tcgen05.mma, bf16 -> f32 in TMEM)
 //     z[m, v]    = (U[m, k, v] + bias[m, v]) / T_k
-// and folds every z into a per-request online softmax (max, sum) and a Gumbel
-// race with the purpose-0 Philox stream, as the generic kernel does; no z is
-// ever written to memory.  DSpark summary, "第二阶段：轻量顺序头" and the history
-// article, "杀招一": P_k = softmax(U_k + B_k(x_{k-1})), B_k low-rank.
+// and folds every z into a per-request online softmax (sum of exp) and a
+// Gumbel race with the purpose-0 Philox stream; no z is ever written to
+// memory.  DSpark summary, "第二阶段：轻量顺序头" and the history article,
+// "杀招一": P_k = softmax(U_k + B_k(x_{k-1})), B_k low-rank.
 //
 // CTA layout (576 threads, one CTA per SM):
 //   warps 0-15  epilogue: warp w reads TMEM lane quadrant w % 4 (32 requests)
@@ -20,10 +20,15 @@
 // Every wait is bounded; on a timeout the CTA sets SPEC_STATUS_TIMEOUT, drains
 // what it issued and returns.
 //
-// Gumbel race filter: a candidate can beat the current best only if
-// exp(z - m) / E > best, and E = -ln u >= 1 - u for u in (0,1), so elements
-// with exp(z - m) / (1 - u) below the best are skipped without computing the
-// logarithm.  1 - u is exact (it is the uniform of the complemented word).
+// Gumbel race (see common.cuh): the winner maximises z_v - ln E_v with
+// E_v = -ln u_v.  Each thread keeps e = 2^(z log2e / T - ref) and the best
+// (e, E); the logarithm E is computed only for candidates, selected by an exact
+// filter: since E >= 1 - u, an element can reach a score g only if
+// 1 - u <= e * 2^(ref - g).  The bound g is the larger of the thread's own best
+// and the best score any thread of the same request has published so far (a
+// per-request word in the workspace, raised with atomicMax).  Published scores
+// are real scores lowered by a margin, so the request's winner always passes;
+// the filter only decides which elements need the exact comparison.
 #include "draft.cuh"
 #include "draft_tc.cuh"
 #include "tc.cuh"
@@ -42,10 +47,48 @@ constexpr uint32_t kTmemCols = kTmemBufs * kNT;
 constexpr int kMaxStages = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFilterSlack = 1.0f - 1.0f / 4194304.0f;  // 1 - 2^-22
+constexpr float kFilterUp = 1.0f + 1.0f / 262144.0f;  // 1 + 2^-18
+constexpr float kPublishMargin = 1.0f / 4096.0f;      // log2 units
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Order-preserving map float -> uint32 (0 sorts below every float).
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {  // NaN for key 0
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Merge of two race states whose reference `m` is in log2 units.
+__device__ __forceinline__ Race race_merge2(const Race& a, const Race& b) {
+  if (b.idx < 0) return a;
+  if (a.idx < 0) return b;
+  const float m = fmaxf(a.m, b.m);
+  const float sa = tc::ex2(a.m - m), sb = tc::ex2(b.m - m);
+  Race o;
+  o.m = m;
+  o.s = a.s * sa + b.s * sb;
+  const float ea = a.be * sa, eb = b.be * sb;
+  if (race_beats(ea, a.bE, a.idx, eb, b.bE, b.idx)) {
+    o.be = ea;
+    o.bE = a.bE;
+    o.idx = a.idx;
+  } else {
+    o.be = eb;
+    o.bE = b.bE;
+    o.idx = b.idx;
+  }
+  return o;
 }
 
 __device__ __forceinline__ Race race_shfl_xor(const Race& st, int mask) {
@@ -58,6 +101,22 @@ __device__ __forceinline__ Race race_shfl_xor(const Race& st, int mask) {
   return o;
 }
 
+// Cold path: exact race test of one filtered element; on a new best, publish
+// the request's score and return true.
+__device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word, int v,
+                                               unsigned* row_best) {
+  const float E = -logf(uniform_from_word(word));
+  if (!race_beats(e, E, v, st.be, st.bE, st.idx)) return false;
+  st.be = e;
+  st.bE = E;
+  st.idx = v;
+  // score in log2 units: ref + log2(e) - log2(E), lowered by a margin that
+  // covers the approximate logarithms
+  const float score = st.m + lg2(e) - lg2(E) - kPublishMargin;
+  atomicMax(row_best, ordered_key(score));
+  return true;
+}
+
 template <typename TL>
 struct UTile {
   static constexpr int kBoxCols = 128 / (int)sizeof(TL);  // 128-byte rows
@@ -65,26 +124,35 @@ struct UTile {
   static constexpr uint32_t kBytes = 128u * kNT * sizeof(TL);
 };
 
-// 16 consecutive logits of `row` starting at column 16*grp of the tile.
-__device__ __forceinline__ void load_u16(const unsigned char* tile, int row, int grp, float (&u)[16],
-                                         float) {
+// Byte offsets, inside a U tile, of the four 16-byte chunks holding the 16
+// logits of `row` from column 16*grp (fp32: two 32-column boxes; bf16: one
+// 64-column box), in the 128-byte swizzle layout the TMA writes.
+__device__ __forceinline__ void u_offsets(int row, int grp, uint32_t (&off)[4], float) {
   const int box = grp >> 1, c0 = (grp & 1) * 4;
-  const unsigned char* base = tile + box * 16384 + row * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) off[j] = box * 16384 + row * 128 + (((c0 + j) ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ void u_offsets(int row, int grp, uint32_t (&off)[4], __nv_bfloat16) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) off[j] = row * 128 + (((grp * 2 + j) ^ (row & 7)) << 4);
+  off[2] = off[3] = 0;
+}
+__device__ __forceinline__ void load_u16(const unsigned char* tile, const uint32_t (&off)[4],
+                                         float (&u)[16], float) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float4 f = *reinterpret_cast<const float4*>(base + (((c0 + j) ^ (row & 7)) << 4));
+    const float4 f = *reinterpret_cast<const float4*>(tile + off[j]);
     u[4 * j] = f.x;
     u[4 * j + 1] = f.y;
     u[4 * j + 2] = f.z;
     u[4 * j + 3] = f.w;
   }
 }
-__device__ __forceinline__ void load_u16(const unsigned char* tile, int row, int grp, float (&u)[16],
-                                         __nv_bfloat16) {
-  const unsigned char* base = tile + row * 128;
+__device__ __forceinline__ void load_u16(const unsigned char* tile, const uint32_t (&off)[4],
+                                         float (&u)[16], __nv_bfloat16) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const uint4 q = *reinterpret_cast<const uint4*>(base + (((grp * 2 + j) ^ (row & 7)) << 4));
+    const uint4 q = *reinterpret_cast<const uint4*>(tile + off[j]);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -94,9 +162,22 @@ __device__ __forceinline__ void load_u16(const unsigned char* tile, int row, int
   }
 }
 
+// Ring position with incremental phase (no division by the runtime depth).
+struct Ring {
+  int idx;
+  uint32_t phase;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 }  // namespace
 
 template <typename TL, int KC>
+// 576 threads per CTA leave at most 96 registers per thread.
 __global__ void __launch_bounds__(kThreadsTC, 1)
     draft_tc_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_c,
                     DraftTCParams p) {
@@ -113,7 +194,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   __shared__ __align__(8) uint64_t tfull[kTmemBufs], tempty[kTmemBufs];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ Race grp_state[3][128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mtile = blockIdx.x % p.mtiles, split = blockIdx.x / p.mtiles;
@@ -159,23 +239,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (warp == kProducerWarp) {
     if (lane == 0) {
       int issued = 0;
-      for (int t = 0; t < T && !abort_flag; ++t) {
-        const int s = t % S;
-        const uint32_t ph = (uint32_t)(t / S) & 1u;
-        if (!tc::mbar_wait(&empty_s[s], ph ^ 1u, kWaitNs)) {
+      Ring r{0, 0u};
+      for (int t = 0; t < T && !abort_flag; ++t, r.next(S)) {
+        if (!tc::mbar_wait(&empty_s[r.idx], r.phase ^ 1u, kWaitNs)) {
           fail();
           break;
         }
-        unsigned char* st = sStage + s * kStageBytes;
+        unsigned char* st = sStage + r.idx * kStageBytes;
         const int n0 = (t_begin + t) * kNT;
-        tc::mbar_expect_tx(&full_c[s], kCBytes);
+        tc::mbar_expect_tx(&full_c[r.idx], kCBytes);
 #pragma unroll
-        for (int kc = 0; kc < KC; ++kc) tc::tma_load_3d(st + kc * 8192, &tm_c, &full_c[s], kc * 64, n0, k - 1);
-        tc::mbar_expect_tx(&full_u[s], kUBytes);
+        for (int kc = 0; kc < KC; ++kc)
+          tc::tma_load_3d(st + kc * 8192, &tm_c, &full_c[r.idx], kc * 64, n0, k - 1);
+        tc::mbar_expect_tx(&full_u[r.idx], kUBytes);
 #pragma unroll
         for (int bx = 0; bx < UTile<TL>::kBoxes; ++bx)
-          tc::tma_load_3d(st + kCBytes + bx * 16384, &tm_u, &full_u[s], n0 + bx * UTile<TL>::kBoxCols,
-                          k - 1, m0);
+          tc::tma_load_3d(st + kCBytes + bx * 16384, &tm_u, &full_u[r.idx],
+                          n0 + bx * UTile<TL>::kBoxCols, k - 1, m0);
         issued = t + 1;
       }
       if (abort_flag) {
@@ -192,24 +272,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = tc::bf16_idesc(128, kNT);
       int last = -1;
-      for (int t = 0; t < T && !abort_flag; ++t) {
-        const int s = t % S, b = t % kTmemBufs;
-        if (!tc::mbar_wait(&full_c[s], (uint32_t)(t / S) & 1u, kWaitNs) ||
-            !tc::mbar_wait(&tempty[b], ((uint32_t)(t / kTmemBufs) & 1u) ^ 1u, kWaitNs)) {
+      Ring r{0, 0u}, rb{0, 0u};
+      const uint32_t a_base = tc::smem_u32(sA);
+      for (int t = 0; t < T && !abort_flag; ++t, r.next(S), rb.next(kTmemBufs)) {
+        if (!tc::mbar_wait(&full_c[r.idx], r.phase, kWaitNs) ||
+            !tc::mbar_wait(&tempty[rb.idx], rb.phase ^ 1u, kWaitNs)) {
           fail();
           break;
         }
         tc::fence_after_sync();
-        const unsigned char* st = sStage + s * kStageBytes;
+        const uint32_t b_base = tc::smem_u32(sStage + r.idx * kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < KC * 4; ++kk) {
           const int kc = kk >> 2, ko = (kk & 3) * 32;
-          const uint64_t ad = tc::sw128_desc(tc::smem_u32(sA + kc * 16384 + ko));
-          const uint64_t bd = tc::sw128_desc(tc::smem_u32(st + kc * 8192 + ko));
-          tc::mma_bf16(tmem + (uint32_t)(b * kNT), ad, bd, idesc, kk > 0 ? 1u : 0u);
+          tc::mma_bf16(tmem + (uint32_t)(rb.idx * kNT), tc::sw128_desc(a_base + kc * 16384 + ko),
+                       tc::sw128_desc(b_base + kc * 8192 + ko), idesc, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&tfull[b]);
-        tc::mma_commit(&empty_s[s]);
+        tc::mma_commit(&tfull[rb.idx]);
+        tc::mma_commit(&empty_s[r.idx]);
         last = t;
       }
       if (abort_flag && last >= 0)  // in-flight MMAs must finish before TMEM is freed
@@ -243,74 +323,148 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     tc::fence_proxy_async();
     named_bar_sync(1, (kEpiWarps + 1) * 32);
 
+    // Race state in log2 units: e = 2^(z log2e / T - st.m).  The reference
+    // st.m is fixed at the first tile of the row (its maximum) and moves only
+    // when a tile's sum overflows, or by exact powers of two when the running
+    // sum grows large -- no per-element maximum is needed.
     Race st = race_empty();
-    float be_slack = 0.f;  // st.be * (1 - 2^-22)
-    const float inv_t = 1.0f / p.draft_temp[k - 1];
+    // c_own = (bE / be) * (1 + 2^-18): the filter factor of the thread's own
+    // best; the shared best adds c_shared = 2^(ref - g).  The test
+    // f <= e*c + 1 with f = 1 + (1 - u) - 2^-24 is 1 - u <= e*c with a safe
+    // margin (e*c + 1 rounds by at most 2^-24, covered by the 2^-24 in f and
+    // the slack in c).
+    float c_own = CUDART_INF_F;
+    const float kscale = kLog2e / p.draft_temp[k - 1];
+    float nref = 0.f;  // -st.m once the reference is set
     const uint32_t rid = p.rid_base + (uint32_t)m;
-    const PhiloxKey key = p.key;
-    for (int t = 0; t < T; ++t) {
-      const int s = t % S, b = t % kTmemBufs;
+    const PhiloxRoundKeys rk = philox_round_keys(p.key);
+    unsigned* row_best = p.row_best + (size_t)(k - 1) * p.R + (valid ? m : 0);
+    uint32_t shared_key = 0;
+    uint32_t uoff[4];
+    u_offsets(row, grp, uoff, TL());
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
+    Ring r{0, 0u}, rb{0, 0u};
+    for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
       if (abort_flag) break;
-      if (!tc::mbar_wait(&tfull[b], (uint32_t)(t / kTmemBufs) & 1u, kWaitNs) ||
-          !tc::mbar_wait(&full_u[s], (uint32_t)(t / S) & 1u, kWaitNs)) {
+      const uint32_t shared_now = shared_key;
+      if (valid) shared_key = __ldcg(row_best);  // used by the next tile
+      if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
+          !tc::mbar_wait(&full_u[r.idx], r.phase, kWaitNs)) {
         fail();
         break;
       }
       tc::fence_after_sync();
       uint32_t braw[16];
-      tc::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kNT + grp * 16), braw);
+      tc::tmem_ld16(t_lane + (uint32_t)(rb.idx * kNT), braw);
       float u[16];
-      load_u16(sStage + s * kStageBytes + kCBytes, row, grp, u, TL());
+      load_u16(sStage + r.idx * kStageBytes + kCBytes, uoff, u, TL());
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        tc::mbar_arrive(&tempty[b]);
-        tc::mbar_arrive(&empty_s[s]);
+        tc::mbar_arrive(&tempty[rb.idx]);
+        tc::mbar_arrive(&empty_s[r.idx]);
       }
       if (!valid) continue;
       const int colbase = (t_begin + t) * kNT + grp * 16;
+      float z[16];  // U + bias (the temperature is folded into kscale)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v0 = colbase + 4 * q;
-        if (v0 >= V) break;
-        const uint4 bits = philox((uint32_t)(v0 >> 2), (uint32_t)k, rid, kPurposeDraft, key);
-        float z[4];
+      for (int i = 0; i < 16; ++i) z[i] = u[i] + __uint_as_float(braw[i]);
+      if (colbase + 16 > V) {  // vocabulary tail (last tile only)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          z[i] = (v0 + i < V) ? (u[4 * q + i] + __uint_as_float(braw[4 * q + i])) * inv_t : -CUDART_INF_F;
-        const float mz = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-        if (mz > st.m) {
-          const float sc = tc::ex2((st.m - mz) * kLog2e);
+        for (int i = 0; i < 16; ++i)
+          if (colbase + i >= V) z[i] = -CUDART_INF_F;
+      }
+      if (!(st.m > -CUDART_INF_F)) {  // first tile of the row: fix the reference
+        float mz = z[0];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) mz = fmaxf(mz, z[i]);
+        if (!(mz > -CUDART_INF_F)) continue;
+        st.m = mz * kscale;
+        nref = -st.m;
+      }
+      // Two halves of eight columns, each one straight-line block: two
+      // independent Philox blocks, eight exponentials, split partial sums and
+      // the race filter as one predicate; the cold path is the only branch.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int cb = colbase + 8 * h;
+        uint32_t words[8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint4 bits = philox((uint32_t)((cb >> 2) + q), (uint32_t)k, rid, kPurposeDraft, rk);
+          words[4 * q] = bits.x;
+          words[4 * q + 1] = bits.y;
+          words[4 * q + 2] = bits.z;
+          words[4 * q + 3] = bits.w;
+        }
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = tc::ex2(fmaf(z[8 * h + i], kscale, nref));
+        float ts = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+        if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
+          float mz = z[8 * h];
+#pragma unroll
+          for (int i = 1; i < 8; ++i) mz = fmaxf(mz, z[8 * h + i]);
+          const float mnew = fmaxf(mz * kscale, st.m);
+          const float sc = tc::ex2(st.m - mnew);
           st.s *= sc;
           st.be *= sc;
-          be_slack = st.be * kFilterSlack;
-          st.m = mz;
-        }
+          st.m = mnew;
+          nref = -mnew;
+          c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+          ts = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float e = tc::ex2((z[i] - st.m) * kLog2e);
-          st.s += e;
-          const uint32_t word = word_of(bits, i);
-          const float w = uniform_from_word(~word);  // 1 - u, exact
-          if (e > 0.f && e * st.bE >= be_slack * w) {
-            const float E = -logf(uniform_from_word(word));
-            if (race_beats(e, E, v0 + i, st.be, st.bE, st.idx)) {
-              st.be = e;
-              st.bE = E;
-              st.idx = v0 + i;
-              be_slack = e * kFilterSlack;
+          for (int i = 0; i < 8; ++i) {
+            e[i] = tc::ex2(fmaf(z[8 * h + i], kscale, nref));
+            ts += e[i];
+          }
+        }
+        st.s += ts;
+        if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
+          st.s *= 0x1p-64f;
+          st.be *= 0x1p-64f;
+          st.m += 64.f;
+          nref -= 64.f;
+          c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+        }
+        // filter factor: the tighter of the own best and the request's shared best
+        const float c_filt = fminf(c_own, tc::ex2(st.m - key_value(shared_now)) * kFilterUp);
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) any |= one_plus_w(words[i]) <= fmaf(e[i], c_filt, 1.0f);
+        if (any) {  // rare: elements that could beat the best, in index order
+          uint32_t mask = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mask |= (one_plus_w(words[i]) <= fmaf(e[i], c_filt, 1.0f) ? 1u : 0u) << i;
+          if (cb + 8 > V) mask &= (V > cb) ? (1u << (V - cb)) - 1u : 0u;
+          while (mask) {
+            const int i = __ffs(mask) - 1;
+            mask &= mask - 1u;
+            float ei = e[0];
+            uint32_t wi = words[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) {
+              ei = (i == j) ? e[j] : ei;
+              wi = (i == j) ? words[j] : wi;
             }
+            if (race_candidate(st, ei, wi, cb + i, row_best))
+              c_own = __fdividef(st.bE, st.be) * kFilterUp;
           }
         }
       }
     }
-    // merge the four column groups of each row inside the CTA
-    if (grp > 0) grp_state[grp - 1][row] = st;
+    // Merge the four column groups of each row inside the CTA, through the
+    // stage buffers (every issued load has been consumed once all epilogue
+    // warps reach the barrier).
+    Race* grp_state = reinterpret_cast<Race*>(sStage);  // [3][128]
+    named_bar_sync(2, kEpiWarps * 32);
+    if (grp > 0) grp_state[(grp - 1) * 128 + row] = st;
     named_bar_sync(2, kEpiWarps * 32);
     if (grp == 0 && valid) {
 #pragma unroll
-      for (int g = 0; g < 3; ++g) st = race_merge(st, grp_state[g][row]);
+      for (int g = 0; g < 3; ++g) st = race_merge2(st, grp_state[g * 128 + row]);
       Partial w{};
       w.f0 = st.m;
       w.f1 = st.s;
@@ -338,15 +492,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (m < p.R)
       for (int s = part; s < p.nsplit; s += 4) {
         const Partial w = load_partial(p.partials + (size_t)m * p.nsplit + s);
-        acc = race_merge(acc, Race{w.f0, w.f1, w.f2, w.f3, w.i0});
+        acc = race_merge2(acc, Race{w.f0, w.f1, w.f2, w.f3, w.i0});
       }
-    acc = race_merge(acc, race_shfl_xor(acc, 1));
-    acc = race_merge(acc, race_shfl_xor(acc, 2));
+    acc = race_merge2(acc, race_shfl_xor(acc, 1));
+    acc = race_merge2(acc, race_shfl_xor(acc, 2));
     if (part == 0 && m < p.R) {
       const size_t o = (size_t)m * p.gamma + (k - 1);
       p.x[o] = acc.idx;
       p.q_tok[o] = acc.be / acc.s;
-      p.lse_q[o] = acc.m + logf(acc.s);
+      // lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s, with m in log2 units
+      p.lse_q[o] = (float)((double)acc.m * 0.6931471805599453 + log((double)acc.s));
     }
   }
 }
@@ -392,14 +547,14 @@ size_t smem_bytes(int stages) {
 
 template <typename TL, int KC>
 int pick_stages() {
-  const size_t budget = 227 * 1024 - 8 * 1024;  // static shared memory and slack
+  const size_t budget = 227 * 1024 - 1024;  // static shared memory (< 0.5 KB) and slack
   int s = kMaxStages;
   while (s > 2 && smem_bytes<TL, KC>(s) > budget) --s;
   return s;
 }
 
 template <typename TL, int KC>
-cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* Ct, int device_sms,
+cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* Ct,
                          cudaStream_t stream) {
   DraftTCParams p = base;
   CUtensorMap tm_u, tm_c;
@@ -415,7 +570,6 @@ cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* C
   auto kern = draft_tc_kernel<TL, KC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  (void)device_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.mtiles * p.nsplit));
   cfg.blockDim = dim3(kThreadsTC);
@@ -444,21 +598,21 @@ int draft_tc_nsplit(int R, int V, int device_sms) {
 }
 
 cudaError_t launch_draft_tc(const DraftTCParams& p, int logit_dtype, const void* U, const void* Ct,
-                            int device_sms, cudaStream_t stream) {
+                            cudaStream_t stream) {
   const int KC = p.rank / 64;
   if (logit_dtype == SPEC_F32) {
     switch (KC) {
-      case 1: return launch_typed<float, 1>(p, U, Ct, device_sms, stream);
-      case 2: return launch_typed<float, 2>(p, U, Ct, device_sms, stream);
-      case 3: return launch_typed<float, 3>(p, U, Ct, device_sms, stream);
-      case 4: return launch_typed<float, 4>(p, U, Ct, device_sms, stream);
+      case 1: return launch_typed<float, 1>(p, U, Ct, stream);
+      case 2: return launch_typed<float, 2>(p, U, Ct, stream);
+      case 3: return launch_typed<float, 3>(p, U, Ct, stream);
+      case 4: return launch_typed<float, 4>(p, U, Ct, stream);
     }
   } else {
     switch (KC) {
-      case 1: return launch_typed<__nv_bfloat16, 1>(p, U, Ct, device_sms, stream);
-      case 2: return launch_typed<__nv_bfloat16, 2>(p, U, Ct, device_sms, stream);
-      case 3: return launch_typed<__nv_bfloat16, 3>(p, U, Ct, device_sms, stream);
-      case 4: return launch_typed<__nv_bfloat16, 4>(p, U, Ct, device_sms, stream);
+      case 1: return launch_typed<__nv_bfloat16, 1>(p, U, Ct, stream);
+      case 2: return launch_typed<__nv_bfloat16, 2>(p, U, Ct, stream);
+      case 3: return launch_typed<__nv_bfloat16, 3>(p, U, Ct, stream);
+      case 4: return launch_typed<__nv_bfloat16, 4>(p, U, Ct, stream);
     }
   }
   return cudaErrorInvalidValue;

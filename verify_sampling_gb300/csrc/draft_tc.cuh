@@ -20,6 +20,7 @@ struct DraftTCParams {
   float* lse_q;
   Partial* partials;   // [R, nsplit]
   unsigned* counters;  // [mtiles], zero on entry
+  unsigned* row_best;  // [gamma, R] shared race bounds (order-preserving keys), zero on entry
   uint32_t* status;
 };
 
@@ -28,6 +29,6 @@ int draft_tc_nsplit(int R, int V, int device_sms);
 
 // gamma dependent launches (one per position) of the fused kernel.
 cudaError_t launch_draft_tc(const DraftTCParams& p, int logit_dtype, const void* U, const void* Ct,
-                            int device_sms, cudaStream_t stream);
+                            cudaStream_t stream);
 
 }  // namespace spec
