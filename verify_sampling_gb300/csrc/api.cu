@@ -6,6 +6,7 @@
 #include "draft.cuh"
 #include "draft_tc.cuh"
 #include "schedule.cuh"
+#include "residual_tc.cuh"
 #include "verify.cuh"
 
 namespace {
@@ -295,6 +296,16 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   p.p_tok = a.p_tok;
   p.lse_t = a.lse_t;
   p.status = a.status;
+  if (sample) {
+    int dev = 0, major = 0, sms = 0;
+    p.tc_residual =
+        cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        major == 10 && sms >= 1 && sms <= kMaxDeviceSms &&
+        resid_tc_supported(a.tgt_dtype, logit_dtype, fac_dtype, rank, a.V, a.tgt, p.U, p.A, p.Ct);
+    p.device_sms = sms;
+  }
   size_t cnt_off = 0, cnt_bytes = 0;
   p.ws = verify_scratch_carve(a.workspace, a.R, a.gamma, a.V, &cnt_off, &cnt_bytes);
   if (cudaMemsetAsync(static_cast<char*>(a.workspace) + cnt_off, 0, cnt_bytes, s) != cudaSuccess)

@@ -31,75 +31,14 @@
 // the filter only decides which elements need the exact comparison.
 #include "draft.cuh"
 #include "draft_tc.cuh"
+#include "fused_tc.cuh"
 #include "tc.cuh"
 
 namespace spec {
 
 namespace {
 
-constexpr int kNT = 64;             // vocabulary columns per tile (MMA N)
-constexpr int kEpiWarps = 16;       // 4 lane quadrants x 4 column groups
-constexpr int kProducerWarp = kEpiWarps;
-constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr int kThreadsTC = (kEpiWarps + 2) * 32;
-constexpr int kTmemBufs = 4;
-constexpr uint32_t kTmemCols = kTmemBufs * kNT;
-constexpr int kMaxStages = 8;
-constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFilterUp = 1.0f + 1.0f / 262144.0f;  // 1 + 2^-18
-constexpr float kPublishMargin = 1.0f / 4096.0f;      // log2 units
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Order-preserving map float -> uint32 (0 sorts below every float).
-__device__ __forceinline__ uint32_t ordered_key(float f) {
-  const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {  // NaN for key 0
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Merge of two race states whose reference `m` is in log2 units.
-__device__ __forceinline__ Race race_merge2(const Race& a, const Race& b) {
-  if (b.idx < 0) return a;
-  if (a.idx < 0) return b;
-  const float m = fmaxf(a.m, b.m);
-  const float sa = tc::ex2(a.m - m), sb = tc::ex2(b.m - m);
-  Race o;
-  o.m = m;
-  o.s = a.s * sa + b.s * sb;
-  const float ea = a.be * sa, eb = b.be * sb;
-  if (race_beats(ea, a.bE, a.idx, eb, b.bE, b.idx)) {
-    o.be = ea;
-    o.bE = a.bE;
-    o.idx = a.idx;
-  } else {
-    o.be = eb;
-    o.bE = b.bE;
-    o.idx = b.idx;
-  }
-  return o;
-}
-
-__device__ __forceinline__ Race race_shfl_xor(const Race& st, int mask) {
-  Race o;
-  o.m = __shfl_xor_sync(0xffffffffu, st.m, mask);
-  o.s = __shfl_xor_sync(0xffffffffu, st.s, mask);
-  o.be = __shfl_xor_sync(0xffffffffu, st.be, mask);
-  o.bE = __shfl_xor_sync(0xffffffffu, st.bE, mask);
-  o.idx = __shfl_xor_sync(0xffffffffu, st.idx, mask);
-  return o;
-}
+using namespace fused;
 
 // Cold path: exact race test of one filtered element; on a new best, publish
 // the request's score and return true.
@@ -117,68 +56,13 @@ __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word,
   return true;
 }
 
-template <typename TL>
-struct UTile {
-  static constexpr int kBoxCols = 128 / (int)sizeof(TL);  // 128-byte rows
-  static constexpr int kBoxes = kNT / kBoxCols;
-  static constexpr uint32_t kBytes = 128u * kNT * sizeof(TL);
-};
-
-// Byte offsets, inside a U tile, of the four 16-byte chunks holding the 16
-// logits of `row` from column 16*grp (fp32: two 32-column boxes; bf16: one
-// 64-column box), in the 128-byte swizzle layout the TMA writes.
-__device__ __forceinline__ void u_offsets(int row, int grp, uint32_t (&off)[4], float) {
-  const int box = grp >> 1, c0 = (grp & 1) * 4;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) off[j] = box * 16384 + row * 128 + (((c0 + j) ^ (row & 7)) << 4);
-}
-__device__ __forceinline__ void u_offsets(int row, int grp, uint32_t (&off)[4], __nv_bfloat16) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) off[j] = row * 128 + (((grp * 2 + j) ^ (row & 7)) << 4);
-  off[2] = off[3] = 0;
-}
-__device__ __forceinline__ void load_u16(const unsigned char* tile, const uint32_t (&off)[4],
-                                         float (&u)[16], float) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float4 f = *reinterpret_cast<const float4*>(tile + off[j]);
-    u[4 * j] = f.x;
-    u[4 * j + 1] = f.y;
-    u[4 * j + 2] = f.z;
-    u[4 * j + 3] = f.w;
-  }
-}
-__device__ __forceinline__ void load_u16(const unsigned char* tile, const uint32_t (&off)[4],
-                                         float (&u)[16], __nv_bfloat16) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint4 q = *reinterpret_cast<const uint4*>(tile + off[j]);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      u[8 * j + 2 * h] = __uint_as_float(w[h] << 16);
-      u[8 * j + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-    }
-  }
-}
-
-// Ring position with incremental phase (no division by the runtime depth).
-struct Ring {
-  int idx;
-  uint32_t phase;
-  __device__ __forceinline__ void next(int n) {
-    if (++idx == n) {
-      idx = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 }  // namespace
+
+using namespace fused;
 
 template <typename TL, int KC>
 // 576 threads per CTA leave at most 96 registers per thread.
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     draft_tc_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_c,
                     DraftTCParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -509,37 +393,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 // ------------------------------------------------------------------ host --
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = []() -> EncodeTiledFn {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(ptr);
-  }();
-  return fn;
-}
-
-bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t es, const void* base, uint64_t d0,
-               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
-  const cuuint32_t box[3] = {b0, b1, b2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename TL, int KC>
 size_t smem_bytes(int stages) {
   return 1024 + (size_t)KC * 16384 + (size_t)stages * (KC * kNT * 128 + UTile<TL>::kBytes);
@@ -547,7 +400,7 @@ size_t smem_bytes(int stages) {
 
 template <typename TL, int KC>
 int pick_stages() {
-  const size_t budget = 227 * 1024 - 1024;  // static shared memory (< 0.5 KB) and slack
+  const size_t budget = kSmemBudget;
   int s = kMaxStages;
   while (s > 2 && smem_bytes<TL, KC>(s) > budget) --s;
   return s;
@@ -560,10 +413,12 @@ cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* C
   CUtensorMap tm_u, tm_c;
   const CUtensorMapDataType udt =
       sizeof(TL) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!encode_3d(&tm_u, udt, sizeof(TL), U, (uint64_t)p.V, (uint64_t)p.gamma, (uint64_t)p.R,
-                 UTile<TL>::kBoxCols, 1, 128) ||
-      !encode_3d(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ct, (uint64_t)p.rank, (uint64_t)p.V,
-                 (uint64_t)p.gamma, 64, kNT, 1))
+  const uint64_t udims[3] = {(uint64_t)p.V, (uint64_t)p.gamma, (uint64_t)p.R};
+  const uint32_t ubox[3] = {(uint32_t)UTile<TL>::kBoxCols, 1, 128};
+  const uint64_t cdims[3] = {(uint64_t)p.rank, (uint64_t)p.V, (uint64_t)p.gamma};
+  const uint32_t cbox[3] = {64, (uint32_t)kNT, 1};
+  if (!encode_tiled(&tm_u, udt, sizeof(TL), U, 3, udims, ubox) ||
+      !encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ct, 3, cdims, cbox))
     return cudaErrorInvalidValue;
   p.stages = pick_stages<TL, KC>();
   const size_t smem = smem_bytes<TL, KC>(p.stages);
@@ -572,7 +427,7 @@ cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* C
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.mtiles * p.nsplit));
-  cfg.blockDim = dim3(kThreadsTC);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -1,0 +1,465 @@
+// Fused residual resample on the tensor cores (sm_100 family).
+//
+// For every request whose first rejection is at position j* = k the target
+// token is regenerated from norm(max(0, p - q)) at row k (history article,
+// "1.1运行机制"; DSpark summary, Figure 1): Gumbel-max over
+// log(max(0, p_v - q_v)) + G_v with the purpose-2 stream, i.e. argmax of
+// res_v / E_v in race form; if no residual is positive, the same race over
+// p_v.  q_v = exp(z_v - lse_q) with z the draft logits of row k:
+//     z[m, v] = (U[m, k, v] + A_k[x_{m,k-1}, :] . C_k[:, v]) / T_k,
+// so the bias is again a rank-r GEMM: the requests of one position form the
+// M dimension (gathered, up to 128 per tile), the vocabulary the N dimension.
+// p_v = exp(L_v / T_t - m_t) / s_t uses the softmax max/sum of the target row
+// that the verify row pass stored.
+//
+// Layout and pipelines follow the fused draft kernel (fused_tc.cuh): one CTA
+// per SM, 16 epilogue warps, a TMA producer warp and an MMA warp.  Rows are
+// gathered: the producer loads one 128-byte row box per request and operand
+// (U row and target row), which lands in the same 128-byte swizzle layout as
+// a 128-row box.  Work split: the request tiles of all positions are counted
+// on the device; CTA b takes tile b % M and vocabulary split b / M.
+#include "fused_tc.cuh"
+#include "draft_tc.cuh"
+#include "residual_tc.cuh"
+#include "tc.cuh"
+
+namespace spec {
+
+namespace {
+
+using namespace fused;
+
+__device__ __forceinline__ WRace wrace_merge_(const WRace& a, const WRace& b) {
+  return race_beats(b.bw, b.bE, b.idx, a.bw, a.bE, a.idx) ? b : a;
+}
+
+// Gathered rows are copied linearly, one 64-column segment per request, with a
+// 16-byte pad per row so that eight consecutive rows reading the same 16-byte
+// chunk hit eight different bank groups.
+template <typename T>
+struct RowTile {
+  static constexpr uint32_t kPitch = kNT * sizeof(T) + 16;
+  static constexpr uint32_t kBytes = 128 * kPitch;
+};
+
+// 16 consecutive values of `row` from column 16*grp.
+__device__ __forceinline__ void load_row16(const unsigned char* tile, int row, int grp,
+                                           float (&v)[16], float) {
+  const unsigned char* base = tile + row * RowTile<float>::kPitch + grp * 64;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 f = *reinterpret_cast<const float4*>(base + 16 * j);
+    v[4 * j] = f.x;
+    v[4 * j + 1] = f.y;
+    v[4 * j + 2] = f.z;
+    v[4 * j + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void load_row16(const unsigned char* tile, int row, int grp,
+                                           float (&v)[16], __nv_bfloat16) {
+  const unsigned char* base = tile + row * RowTile<__nv_bfloat16>::kPitch + grp * 32;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 q = *reinterpret_cast<const uint4*>(base + 16 * j);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * j + 2 * h] = __uint_as_float(w[h] << 16);
+      v[8 * j + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+    }
+  }
+}
+
+constexpr uint32_t round1024(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+}  // namespace
+
+using namespace fused;
+
+// 576 threads per CTA leave at most 96 registers per thread.
+template <typename TT, typename TL, int KC>
+__global__ void __launch_bounds__(kThreads, 1)
+    resid_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const TL* __restrict__ U,
+                    const TT* __restrict__ tgt, ResidTCParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kCBytes = KC * kNT * 128;
+  constexpr uint32_t kUBytes = RowTile<TL>::kBytes;
+  constexpr uint32_t kTBytes = RowTile<TT>::kBytes;
+  constexpr uint32_t kStageBytes = round1024(kCBytes + kUBytes + kTBytes);
+  unsigned char* sA = smem;
+  unsigned char* sStage = smem + KC * 16384;
+
+  __shared__ __align__(8) uint64_t full_c[kMaxStages], full_r[kMaxStages], empty_s[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull[kTmemBufs], tempty[kTmemBufs];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ int s_tile[5];  // M, k, first list index, rows, splits
+  __shared__ int s_req[128];
+  __shared__ int s_trow[128];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.gamma;
+
+  // ---- work assignment (identical in every CTA) -------------------------
+  if (threadIdx.x == 0) {
+    int M = 0;
+    for (int kk = 0; kk < G; ++kk) M += (p.res_cnt[kk] + 127) / 128;
+    int nsplit = M > 0 ? max(1, (int)gridDim.x / M) : 1;
+    nsplit = min(min(nsplit, p.ntiles), kMaxDeviceSms);
+    int mt = M > 0 ? (int)blockIdx.x % M : 0, split = M > 0 ? (int)blockIdx.x / M : 0;
+    int k = 0, i0 = 0, rows = 0;
+    if (M > 0 && split < nsplit) {
+      int acc = 0;
+      for (int kk = 0; kk < G; ++kk) {
+        const int n = (p.res_cnt[kk] + 127) / 128;
+        if (mt < acc + n) {
+          k = kk + 1;
+          i0 = (mt - acc) * 128;
+          rows = min(128, p.res_cnt[kk] - i0);
+          break;
+        }
+        acc += n;
+      }
+    }
+    s_tile[0] = (rows > 0) ? M : 0;
+    s_tile[1] = k;
+    s_tile[2] = i0;
+    s_tile[3] = rows;
+    s_tile[4] = nsplit;
+  }
+  __syncthreads();
+  const int M = s_tile[0];
+  if (M == 0) return;  // nothing to do (uniform across the CTA)
+  const int nsplit = s_tile[4];
+  const int k = s_tile[1], i0 = s_tile[2], nrows = s_tile[3];
+  const int mt = (int)blockIdx.x % M, split = (int)blockIdx.x / M;
+  const int t_begin = (int)((long)split * p.ntiles / nsplit);
+  const int t_end = (int)((long)(split + 1) * p.ntiles / nsplit);
+  const int T = t_end - t_begin;
+  const int S = p.stages;
+  const int G1 = G + 1;
+
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+    int r = -1, trow = 0;
+    if (i < nrows) {
+      r = p.res_list[(size_t)(k - 1) * p.R + i0 + i];
+      trow = p.tgt_row_off[r] + (k - 1);
+    }
+    s_req[i] = r;
+    s_trow[i] = trow;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full_c[s], 1);
+      tc::mbar_init(&full_r[s], 1);
+      tc::mbar_init(&empty_s[s], 1 + kEpiWarps);
+    }
+    for (int b = 0; b < kTmemBufs; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], kEpiWarps);
+    }
+    abort_flag = 0;
+    tc::fence_barrier_init();
+    tc::fence_proxy_async();
+  }
+  if (warp == kMmaWarp) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  if (warp == kProducerWarp && lane == 0) tc::tma_prefetch_desc(&tm_c);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  auto fail = [&]() {
+    abort_flag = 1;
+    set_status(p.status, SPEC_STATUS_TIMEOUT);
+  };
+
+  if (warp == kProducerWarp) {
+    // All 32 lanes issue row loads; lane 0 also the C tile and the byte counts.
+    int issued = 0;
+    Ring r{0, 0u};
+    for (int t = 0; t < T && !abort_flag; ++t, r.next(S)) {
+      bool ok = true;
+      if (lane == 0) ok = tc::mbar_wait(&empty_s[r.idx], r.phase ^ 1u, kWaitNs);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      unsigned char* st = sStage + r.idx * kStageBytes;
+      const int n0 = (t_begin + t) * kNT;
+      // columns of this tile inside the vocabulary (a multiple of 16 bytes in
+      // both dtypes, because V times the element size is)
+      const int seg = min(kNT, p.V - n0);
+      const uint32_t ub = (uint32_t)seg * sizeof(TL), tb = (uint32_t)seg * sizeof(TT);
+      if (lane == 0) {
+        tc::mbar_expect_tx(&full_c[r.idx], kCBytes);
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc)
+          tc::tma_load_3d(st + kc * 8192, &tm_c, &full_c[r.idx], kc * 64, n0, k - 1);
+        tc::mbar_expect_tx(&full_r[r.idx], (uint32_t)nrows * (ub + tb));
+      }
+      __syncwarp();
+      for (int i = lane; i < nrows; i += 32) {
+        const size_t urow = (size_t)s_req[i] * p.gamma + (k - 1);
+        tc::bulk_load(st + kCBytes + i * RowTile<TL>::kPitch, U + urow * p.V + n0, ub, &full_r[r.idx]);
+        tc::bulk_load(st + kCBytes + kUBytes + i * RowTile<TT>::kPitch,
+                      tgt + (size_t)s_trow[i] * p.V + n0, tb, &full_r[r.idx]);
+      }
+      issued = t + 1;
+    }
+    if (abort_flag && lane == 0) {
+      for (int t = (issued > S ? issued - S : 0); t < issued; ++t) {
+        const uint32_t ph = (uint32_t)(t / S) & 1u;
+        tc::mbar_wait(&full_c[t % S], ph, kWaitNs);
+        tc::mbar_wait(&full_r[t % S], ph, kWaitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    named_bar_sync(1, (kEpiWarps + 1) * 32);
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::bf16_idesc(128, kNT);
+      int last = -1;
+      Ring r{0, 0u}, rb{0, 0u};
+      const uint32_t a_base = tc::smem_u32(sA);
+      for (int t = 0; t < T && !abort_flag; ++t, r.next(S), rb.next(kTmemBufs)) {
+        if (!tc::mbar_wait(&full_c[r.idx], r.phase, kWaitNs) ||
+            !tc::mbar_wait(&tempty[rb.idx], rb.phase ^ 1u, kWaitNs)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t b_base = tc::smem_u32(sStage + r.idx * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < KC * 4; ++kk) {
+          const int kc = kk >> 2, ko = (kk & 3) * 32;
+          tc::mma_bf16(tmem + (uint32_t)(rb.idx * kNT), tc::sw128_desc(a_base + kc * 16384 + ko),
+                       tc::sw128_desc(b_base + kc * 8192 + ko), idesc, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&tfull[rb.idx]);
+        tc::mma_commit(&empty_s[r.idx]);
+        last = t;
+      }
+      if (abort_flag && last >= 0)
+        tc::mbar_wait(&tfull[last % kTmemBufs], (uint32_t)(last / kTmemBufs) & 1u, kWaitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int quad = warp & 3, grp = warp >> 2;
+    const int row = quad * 32 + lane;
+    const bool valid = row < nrows;
+    const int V = p.V, rank = p.rank;
+    const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
+    for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
+      const int i = idx / (KC * 8), c = idx % (KC * 8);
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (i < nrows) {
+        const int req = s_req[i];
+        int xp = (k == 1) ? p.x0[req] : p.x[(size_t)req * G + (k - 2)];
+        if (xp < 0 || xp >= V) xp = 0;
+        val = *reinterpret_cast<const uint4*>(Ak + (size_t)xp * rank + c * 8);
+      }
+      const int kc = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(sA + kc * 16384 + i * 128 + ((cc ^ (i & 7)) << 4)) = val;
+    }
+    tc::fence_proxy_async();
+    named_bar_sync(1, (kEpiWarps + 1) * 32);
+
+    // Per-request constants (log2 units): q = 2^(z kq + nq), p = 2^(L kt + nt) / s_t.
+    const int req = valid ? s_req[row] : 0;
+    const uint32_t rid = p.rid_base + (uint32_t)req;
+    const size_t rk1 = (size_t)req * G + (k - 1);
+    const size_t rj = (size_t)req * G1 + (k - 1);
+    const float kq = kLog2e / p.draft_temp[k - 1];
+    const float nq = valid ? -p.lse_q[rk1] * kLog2e : 0.f;
+    const float kt = kLog2e * p.inv_target_temp;
+    const float nt = valid ? -p.row_m[rj] * kLog2e : 0.f;
+    const float inv_s = valid ? 1.0f / p.row_s[rj] : 0.f;
+    unsigned* row_best = p.row_best + req;
+    const PhiloxRoundKeys rk = philox_round_keys(p.key);
+    // Race on the residual: an element can beat a best (bw, bE) only if
+    // 1 - u <= res * bE / bw (filter as in the draft kernel, with the shared
+    // per-request bound).  Requests with no positive residual anywhere are
+    // flagged by the final combine and served by the fallback kernel.
+    WRace rres = wrace_empty();
+    float c_res = CUDART_INF_F;
+    uint32_t shared_key = 0;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
+    Ring r{0, 0u}, rb{0, 0u};
+    for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
+      if (abort_flag) break;
+      const uint32_t shared_now = shared_key;
+      if (valid) shared_key = __ldcg(row_best);
+      if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
+          !tc::mbar_wait(&full_r[r.idx], r.phase, kWaitNs)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      // q first (frees the bias and U registers), then the target row.
+      float qv[16], L[16];
+      {
+        uint32_t braw[16];
+        float u[16];
+        tc::tmem_ld16(t_lane + (uint32_t)(rb.idx * kNT), braw);
+        load_row16(sStage + r.idx * kStageBytes + kCBytes, row, grp, u, TL());
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) qv[c] = tc::ex2(fmaf(u[c] + __uint_as_float(braw[c]), kq, nq));
+      }
+      load_row16(sStage + r.idx * kStageBytes + kCBytes + kUBytes, row, grp, L, TT());
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&tempty[rb.idx]);
+        tc::mbar_arrive(&empty_s[r.idx]);
+      }
+      if (!valid) continue;
+      const int colbase = (t_begin + t) * kNT + grp * 16;
+      const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int cb = colbase + 8 * h;
+        uint32_t words[8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint4 bits = philox((uint32_t)((cb >> 2) + q), (uint32_t)k, rid, kPurposeResidual, rk);
+          words[4 * q] = bits.x;
+          words[4 * q + 1] = bits.y;
+          words[4 * q + 2] = bits.z;
+          words[4 * q + 3] = bits.w;
+        }
+        float res[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) res[i] = tc::ex2(fmaf(L[8 * h + i], kt, nt)) * inv_s - qv[8 * h + i];
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) any |= one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f);
+        if (any) {  // rare: exact race tests, in index order
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f) && res[i] > 0.f && cb + i < V) {
+              const float E = -logf(uniform_from_word(words[i]));
+              if (race_beats(res[i], E, cb + i, rres.bw, rres.bE, rres.idx)) {
+                rres = WRace{res[i], E, cb + i};
+                c_res = __fdividef(E, res[i]) * kFilterUp;
+                atomicMax(row_best, ordered_key(lg2(res[i]) - lg2(E) - kPublishMargin));
+              }
+            }
+          }
+        }
+      }
+    }
+    // merge the four column groups through the stage buffers
+    WRace* grp_state = reinterpret_cast<WRace*>(sStage);  // [3][128]
+    named_bar_sync(2, kEpiWarps * 32);
+    if (grp > 0) grp_state[(grp - 1) * 128 + row] = rres;
+    named_bar_sync(2, kEpiWarps * 32);
+    if (grp == 0 && valid) {
+#pragma unroll
+      for (int g = 0; g < 3; ++g) rres = wrace_merge_(rres, grp_state[g * 128 + row]);
+      Partial w{};
+      w.f0 = rres.bw;
+      w.f1 = rres.bE;
+      w.i0 = rres.idx;
+      p.partials[((size_t)mt * 128 + row) * nsplit + split] = w;
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (!last_block_arrives(p.counters + mt, (unsigned)nsplit)) return;
+
+  // Last CTA of this request tile: merge the splits, four threads per request.
+  if (threadIdx.x < kEpiWarps * 32) {
+    const int row = threadIdx.x >> 2, part = threadIdx.x & 3;
+    WRace a = wrace_empty();
+    if (row < nrows)
+      for (int s = part; s < nsplit; s += 4) {
+        const Partial w = load_partial(p.partials + ((size_t)mt * 128 + row) * nsplit + s);
+        a = wrace_merge_(a, WRace{w.f0, w.f1, w.i0});
+      }
+    a = wrace_merge_(a, wrace_shfl_xor(a, 1));
+    a = wrace_merge_(a, wrace_shfl_xor(a, 2));
+    if (part == 0 && row < nrows) {
+      const int req = s_req[row];
+      if (a.idx >= 0)
+        p.out_tok[(size_t)req * G1 + (k - 1)] = a.idx;
+      else
+        p.fallback[req] = k;  // no positive residual: sample from p instead
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host --
+namespace {
+
+template <typename TT, typename TL, int KC>
+size_t smem_bytes(int stages) {
+  return 1024 + (size_t)KC * 16384 +
+         (size_t)stages * round1024(KC * kNT * 128 + RowTile<TL>::kBytes + RowTile<TT>::kBytes);
+}
+
+template <typename TT, typename TL, int KC>
+cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void* U, const void* Ct,
+                         int grid, cudaStream_t stream) {
+  ResidTCParams p = base;
+  CUtensorMap tm_c;
+  const uint64_t cdims[3] = {(uint64_t)p.rank, (uint64_t)p.V, (uint64_t)p.gamma};
+  const uint32_t cbox[3] = {64, (uint32_t)kNT, 1};
+  if (!encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ct, 3, cdims, cbox))
+    return cudaErrorInvalidValue;
+  int s = kMaxStages;
+  while (s > 2 && smem_bytes<TT, TL, KC>(s) > kSmemBudget) --s;
+  p.stages = s;
+  const size_t smem = smem_bytes<TT, TL, KC>(s);
+  auto kern = resid_tc_kernel<TT, TL, KC>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kThreads, smem, stream>>>(tm_c, static_cast<const TL*>(U), static_cast<const TT*>(tgt), p);
+  return cudaGetLastError();
+}
+
+template <typename TT, typename TL>
+cudaError_t launch_kc(const ResidTCParams& p, const void* tgt, const void* U, const void* Ct,
+                      int grid, cudaStream_t stream) {
+  switch (p.rank / 64) {
+    case 1: return launch_typed<TT, TL, 1>(p, tgt, U, Ct, grid, stream);
+    case 2: return launch_typed<TT, TL, 2>(p, tgt, U, Ct, grid, stream);
+    case 3: return launch_typed<TT, TL, 3>(p, tgt, U, Ct, grid, stream);
+    case 4: return launch_typed<TT, TL, 4>(p, tgt, U, Ct, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool resid_tc_supported(int tgt_dtype, int logit_dtype, int fac_dtype, int rank, int V,
+                        const void* tgt, const void* U, const void* A, const void* Ct) {
+  auto es = [](int d) { return d == SPEC_F32 ? (size_t)4 : (size_t)2; };
+  auto al16 = [](const void* q) { return ((uintptr_t)q & 15) == 0; };
+  return fac_dtype == SPEC_BF16 && rank % 64 == 0 && rank <= 256 &&
+         ((size_t)V * es(logit_dtype)) % 16 == 0 && ((size_t)V * es(tgt_dtype)) % 16 == 0 &&
+         al16(tgt) && al16(U) && al16(A) && al16(Ct);
+}
+
+cudaError_t launch_resid_tc(const ResidTCParams& p, int tgt_dtype, int logit_dtype, const void* tgt,
+                            const void* U, const void* Ct, int grid, cudaStream_t stream) {
+  if (tgt_dtype == SPEC_F32) {
+    if (logit_dtype == SPEC_F32) return launch_kc<float, float>(p, tgt, U, Ct, grid, stream);
+    return launch_kc<float, __nv_bfloat16>(p, tgt, U, Ct, grid, stream);
+  }
+  if (logit_dtype == SPEC_F32) return launch_kc<__nv_bfloat16, float>(p, tgt, U, Ct, grid, stream);
+  return launch_kc<__nv_bfloat16, __nv_bfloat16>(p, tgt, U, Ct, grid, stream);
+}
+
+}  // namespace spec

@@ -1,0 +1,40 @@
+// Fused tensor-core residual resample (internal header).
+#pragma once
+
+#include "common.cuh"
+
+namespace spec {
+
+struct ResidTCParams {
+  int R, gamma, V, rank, stages, ntiles, max_mtiles;
+  uint32_t rid_base;
+  PhiloxKey key;
+  float inv_target_temp;
+  const int32_t* x0;
+  const int32_t* x;
+  const float* draft_temp;
+  const void* A;  // bf16 [gamma, V, rank]
+  const float* lse_q;
+  const int32_t* tgt_row_off;
+  const float* row_m;       // [R, gamma + 1] target-row softmax max (natural units)
+  const float* row_s;       // [R, gamma + 1] target-row softmax sum
+  const int* res_cnt;       // [gamma] requests whose first rejection is at j = k
+  const int* res_list;      // [gamma, R] those requests
+  Partial* partials;        // [max_mtiles, 128, nsplit]
+  unsigned* counters;       // [max_mtiles], zero on entry
+  unsigned* row_best;       // [R] shared race bounds, zero on entry
+  int32_t* out_tok;         // [R, gamma + 1]
+  int* fallback;            // [R] position whose residual was zero everywhere (0: none)
+  uint32_t* status;
+};
+
+// Request tiles the residual kernel may need: sum_k ceil(cnt_k / 128).
+inline int resid_tc_max_mtiles(int R, int gamma) { return (R + 127) / 128 + gamma; }
+
+bool resid_tc_supported(int tgt_dtype, int logit_dtype, int fac_dtype, int rank, int V,
+                        const void* tgt, const void* U, const void* A, const void* Ct);
+
+cudaError_t launch_resid_tc(const ResidTCParams& p, int tgt_dtype, int logit_dtype, const void* tgt,
+                            const void* U, const void* Ct, int grid, cudaStream_t stream);
+
+}  // namespace spec

@@ -16,6 +16,9 @@
 // they recompute q at j* and draw the residual Gumbel-max.
 #include "verify.cuh"
 
+#include "draft_tc.cuh"
+#include "residual_tc.cuh"
+
 namespace spec {
 
 namespace {
@@ -64,6 +67,10 @@ __device__ void resolve_request(const VerifyParams& p, int r, int l) {
   p.accept_len[r] = acc;
   p.n_out[r] = acc + 1;
   ws.req_jstar[r] = (p.mode == SPEC_VERIFY_SAMPLE) ? jstar : 0;
+  if (p.tc_residual && p.mode == SPEC_VERIFY_SAMPLE && jstar > 0) {
+    const int pos = atomicAdd(ws.res_num + (jstar - 1), 1);
+    ws.res_list[(size_t)(jstar - 1) * p.R + pos] = r;
+  }
 }
 
 }  // namespace
@@ -214,12 +221,15 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_rows_kernel(VerifyParam
   }
 }
 
+// Generic residual (any dtype, FFMA bias).  `gate[r]` is the rejected position
+// of request r (0: nothing to do): every rejected request when the fused
+// kernel is not used, else only those whose fused residual was zero everywhere.
 template <typename TT, typename TL, typename TF>
-__global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p, const int* gate) {
   __shared__ float arow[256];
   __shared__ WRace red[kVerifyThreads / 32];
   const int r = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
-  const int jstar = p.ws.req_jstar[r];
+  const int jstar = gate[r];
   if (jstar == 0) return;
   const int V = p.V, G1 = p.gamma + 1, rank = p.rank;
   const uint32_t rid = p.rid_base + (uint32_t)r;
@@ -296,73 +306,126 @@ __global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p
 // ------------------------------------------------------------- scratch ----
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-static size_t layout(int R, int gamma, int V, size_t off[9]) {
+// Scratch layout: arrays that need no initialisation first, then the
+// counters and flags that every call zeroes in one memset.
+enum { kRowPart, kResPart, kRowM, kRowS, kRowRes, kReqJstar, kResList, kRtPart,
+       kRowCnt, kReqCnt, kResCnt, kResNum, kRtCnt, kRtBest, kFallback, kLayoutN };
+
+static size_t layout(int R, int gamma, int V, size_t off[kLayoutN]) {
   const size_t rows = (size_t)R * (gamma + 1);
   const size_t ns = (size_t)verify_nsplit(R, gamma, V), nr = (size_t)residual_nsplit(R, V);
+  const size_t mt = (size_t)resid_tc_max_mtiles(R, gamma);
+  const size_t sizes[kLayoutN] = {rows * ns * sizeof(Partial), (size_t)R * nr * sizeof(Partial),
+                                  rows * sizeof(float), rows * sizeof(float), rows * sizeof(int),
+                                  (size_t)R * sizeof(int), (size_t)gamma * R * sizeof(int),
+                                  mt * 128 * kMaxDeviceSms * sizeof(Partial),
+                                  rows * sizeof(unsigned), (size_t)R * sizeof(unsigned),
+                                  (size_t)R * sizeof(unsigned), (size_t)gamma * sizeof(int),
+                                  mt * sizeof(unsigned), (size_t)R * sizeof(unsigned),
+                                  (size_t)R * sizeof(int)};
   size_t o = 0;
-  off[0] = o; o = align_up(o + rows * ns * sizeof(Partial));
-  off[1] = o; o = align_up(o + (size_t)R * nr * sizeof(Partial));
-  off[2] = o; o = align_up(o + rows * sizeof(float));
-  off[3] = o; o = align_up(o + rows * sizeof(float));
-  off[4] = o; o = align_up(o + rows * sizeof(int));
-  off[5] = o; o = align_up(o + (size_t)R * sizeof(int));
-  off[6] = o;  // counters: row_cnt, req_cnt, res_cnt contiguous
-  o = o + rows * sizeof(unsigned);
-  off[7] = o; o += (size_t)R * sizeof(unsigned);
-  off[8] = o; o += (size_t)R * sizeof(unsigned);
+  for (int i = 0; i < kLayoutN; ++i) {
+    off[i] = o;
+    o = (i < kRowCnt) ? align_up(o + sizes[i]) : o + sizes[i];
+  }
   return align_up(o);
 }
 
 size_t verify_scratch_bytes(int R, int gamma, int V) {
-  size_t off[9];
+  size_t off[kLayoutN];
   return layout(R, gamma, V, off);
 }
 
 VerifyScratch verify_scratch_carve(void* base, int R, int gamma, int V, size_t* counters_offset,
                                    size_t* counters_bytes) {
-  size_t off[9];
+  size_t off[kLayoutN];
   const size_t total = layout(R, gamma, V, off);
   char* b = static_cast<char*>(base);
   VerifyScratch s;
-  s.row_part = reinterpret_cast<Partial*>(b + off[0]);
-  s.res_part = reinterpret_cast<Partial*>(b + off[1]);
-  s.row_m = reinterpret_cast<float*>(b + off[2]);
-  s.row_s = reinterpret_cast<float*>(b + off[3]);
-  s.row_res = reinterpret_cast<int*>(b + off[4]);
-  s.req_jstar = reinterpret_cast<int*>(b + off[5]);
-  s.row_cnt = reinterpret_cast<unsigned*>(b + off[6]);
-  s.req_cnt = reinterpret_cast<unsigned*>(b + off[7]);
-  s.res_cnt = reinterpret_cast<unsigned*>(b + off[8]);
-  *counters_offset = off[6];
-  *counters_bytes = total - off[6];
+  s.row_part = reinterpret_cast<Partial*>(b + off[kRowPart]);
+  s.res_part = reinterpret_cast<Partial*>(b + off[kResPart]);
+  s.row_m = reinterpret_cast<float*>(b + off[kRowM]);
+  s.row_s = reinterpret_cast<float*>(b + off[kRowS]);
+  s.row_res = reinterpret_cast<int*>(b + off[kRowRes]);
+  s.req_jstar = reinterpret_cast<int*>(b + off[kReqJstar]);
+  s.res_list = reinterpret_cast<int*>(b + off[kResList]);
+  s.rt_part = reinterpret_cast<Partial*>(b + off[kRtPart]);
+  s.row_cnt = reinterpret_cast<unsigned*>(b + off[kRowCnt]);
+  s.req_cnt = reinterpret_cast<unsigned*>(b + off[kReqCnt]);
+  s.res_cnt = reinterpret_cast<unsigned*>(b + off[kResCnt]);
+  s.res_num = reinterpret_cast<int*>(b + off[kResNum]);
+  s.rt_cnt = reinterpret_cast<unsigned*>(b + off[kRtCnt]);
+  s.rt_best = reinterpret_cast<unsigned*>(b + off[kRtBest]);
+  s.fallback = reinterpret_cast<int*>(b + off[kFallback]);
+  *counters_offset = off[kRowCnt];
+  *counters_bytes = total - off[kRowCnt];
   return s;
 }
 
 // ------------------------------------------------------------ launchers ---
 template <typename TT, typename TL, typename TF>
-static cudaError_t launch_typed(const VerifyParams& p, cudaStream_t stream) {
+static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_dtype,
+                                cudaStream_t stream) {
   const dim3 g1((unsigned)p.nsplit, (unsigned)(p.gamma + 1), (unsigned)p.R);
   verify_rows_kernel<TT><<<g1, kVerifyThreads, 0, stream>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || p.mode == SPEC_VERIFY_GREEDY) return err;
   const dim3 g2((unsigned)residual_nsplit(p.R, p.V), (unsigned)p.R);
-  residual_kernel<TT, TL, TF><<<g2, kVerifyThreads, 0, stream>>>(p);
+  if (!p.tc_residual) {
+    residual_kernel<TT, TL, TF><<<g2, kVerifyThreads, 0, stream>>>(p, p.ws.req_jstar);
+    return cudaGetLastError();
+  }
+  ResidTCParams t{};
+  t.R = p.R;
+  t.gamma = p.gamma;
+  t.V = p.V;
+  t.rank = p.rank;
+  t.ntiles = (p.V + 63) / 64;
+  t.max_mtiles = resid_tc_max_mtiles(p.R, p.gamma);
+  t.rid_base = p.rid_base;
+  t.key = p.key;
+  t.inv_target_temp = p.inv_target_temp;
+  t.x0 = p.x0;
+  t.x = p.x;
+  t.draft_temp = p.draft_temp;
+  t.A = p.A;
+  t.lse_q = p.lse_q;
+  t.tgt_row_off = p.tgt_row_off;
+  t.row_m = p.ws.row_m;
+  t.row_s = p.ws.row_s;
+  t.res_cnt = p.ws.res_num;
+  t.res_list = p.ws.res_list;
+  t.partials = p.ws.rt_part;
+  t.counters = p.ws.rt_cnt;
+  t.row_best = p.ws.rt_best;
+  t.out_tok = p.out_tok;
+  t.fallback = p.ws.fallback;
+  t.status = p.status;
+  const int grid = std::max(p.device_sms, t.max_mtiles);
+  err = launch_resid_tc(t, tgt_dtype, logit_dtype, p.tgt, p.U, p.Ct, grid, stream);
+  if (err != cudaSuccess) return err;
+  // requests whose residual was zero everywhere (fp32 rounding only): the
+  // generic kernel redoes them, sampling from p if its residual is zero too
+  residual_kernel<TT, TL, TF><<<g2, kVerifyThreads, 0, stream>>>(p, p.ws.fallback);
   return cudaGetLastError();
 }
 
 template <typename TT>
-static cudaError_t launch_tgt(const VerifyParams& p, int logit_dtype, int fac_dtype,
+static cudaError_t launch_tgt(const VerifyParams& p, int tgt_dtype, int logit_dtype, int fac_dtype,
                               cudaStream_t stream) {
-  if (logit_dtype == SPEC_F32 && fac_dtype == SPEC_F32) return launch_typed<TT, float, float>(p, stream);
-  if (logit_dtype == SPEC_F32) return launch_typed<TT, float, __nv_bfloat16>(p, stream);
-  if (fac_dtype == SPEC_F32) return launch_typed<TT, __nv_bfloat16, float>(p, stream);
-  return launch_typed<TT, __nv_bfloat16, __nv_bfloat16>(p, stream);
+  if (logit_dtype == SPEC_F32 && fac_dtype == SPEC_F32)
+    return launch_typed<TT, float, float>(p, tgt_dtype, logit_dtype, stream);
+  if (logit_dtype == SPEC_F32)
+    return launch_typed<TT, float, __nv_bfloat16>(p, tgt_dtype, logit_dtype, stream);
+  if (fac_dtype == SPEC_F32)
+    return launch_typed<TT, __nv_bfloat16, float>(p, tgt_dtype, logit_dtype, stream);
+  return launch_typed<TT, __nv_bfloat16, __nv_bfloat16>(p, tgt_dtype, logit_dtype, stream);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, int tgt_dtype, int logit_dtype, int fac_dtype,
                           cudaStream_t stream) {
-  if (tgt_dtype == SPEC_F32) return launch_tgt<float>(p, logit_dtype, fac_dtype, stream);
-  return launch_tgt<__nv_bfloat16>(p, logit_dtype, fac_dtype, stream);
+  if (tgt_dtype == SPEC_F32) return launch_tgt<float>(p, tgt_dtype, logit_dtype, fac_dtype, stream);
+  return launch_tgt<__nv_bfloat16>(p, tgt_dtype, logit_dtype, fac_dtype, stream);
 }
 
 }  // namespace spec

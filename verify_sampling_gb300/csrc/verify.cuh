@@ -17,9 +17,15 @@ struct VerifyScratch {
   float* row_s;       // [R, gamma + 1] softmax sum
   int* row_res;       // [R, gamma + 1] accept bit (sample) / argmax (greedy) / bonus token
   int* req_jstar;     // [R] residual position (0: none)
+  int* res_list;      // [gamma, R] requests per rejected position (fused residual)
+  Partial* rt_part;   // [max_mtiles, 128, kMaxDeviceSms] fused-residual partials
   unsigned* row_cnt;  // [R, gamma + 1]   } zeroed together
   unsigned* req_cnt;  // [R]              } at the start
   unsigned* res_cnt;  // [R]              } of every call
+  int* res_num;       // [gamma]          }
+  unsigned* rt_cnt;   // [max_mtiles]     }
+  unsigned* rt_best;  // [R]              }
+  int* fallback;      // [R]              }
 };
 
 struct VerifyParams {
@@ -45,6 +51,8 @@ struct VerifyParams {
   float* p_tok;
   float* lse_t;
   uint32_t* status;
+  bool tc_residual;      // residual on the fused tensor-core kernel
+  int device_sms;
   VerifyScratch ws;
 };
 
