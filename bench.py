@@ -193,6 +193,28 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ replicas ----
+def replica_layout(rank: int, wl) -> tuple[int, int]:
+    """Rank `rank` runs its own batch of wl.R requests: input seed and global
+    request id of its first request (Philox is keyed by global request ids, so
+    the ranks' random streams never overlap)."""
+    return wl.seed + rank, rank * wl.R
+
+
+def combine_over_ranks(ms: float, positions: float, device, world: int) -> tuple[float, float]:
+    """Whole-job figures of a replica run: the slowest rank's time and the
+    positions of all ranks (all_reduce MAX and SUM; no-op for one rank)."""
+    if world == 1:
+        return ms, positions
+    import torch
+    import torch.distributed as dist
+    tm = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    tp = torch.tensor([positions], dtype=torch.float64, device=device)
+    dist.all_reduce(tp, op=dist.ReduceOp.SUM)
+    return float(tm.item()), float(tp.item())
+
+
 # ------------------------------------------------------------------ ours ----
 def main():
     args = _args()
@@ -213,8 +235,8 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    g = synth.make_inputs(wl, dev, seed=wl.seed + rank)
-    rid_base = rank * wl.R
+    seed_in, rid_base = replica_layout(rank, wl)
+    g = synth.make_inputs(wl, dev, seed=seed_in)
     greedy = wl.mode == "greedy"
     din = None if greedy else synth.draft_inputs(g, request_id_base=rid_base)
     R, G, V = wl.R, wl.gamma, wl.V
@@ -288,15 +310,7 @@ def main():
     else:
         B_sum = float(stats_hist[:, 1].sum())
         positions = args.steps * R * G + B_sum
-    t = torch.tensor([ms, positions], dtype=torch.float64, device=dev)
-    if world > 1:
-        tm = t[:1].clone()
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        tp = t[1:].clone()
-        dist.all_reduce(tp, op=dist.ReduceOp.SUM)
-        ms_max, pos_all = float(tm), float(tp)
-    else:
-        ms_max, pos_all = ms, positions
+    ms_max, pos_all = combine_over_ranks(ms, positions, dev, world)
     value = pos_all / (ms_max / 1000.0)
 
     # ------------------------------------------------ roofline (rank 0) ----
@@ -314,7 +328,9 @@ def main():
         per_launch = R * V * es_u + V * wl.r * es_f
         dur_ms = stage_ms["draft"] / (args.steps * G)
         kernel = "draft_step (one launch per position k)"
-        launches = G + 1 + 1 + 2
+        # per round: gamma draft steps, confidence, schedule, verify rows,
+        # fused residual, residual fallback (gated, exits at once when unused)
+        launches = G + 5
     achieved = per_launch / (dur_ms / 1000.0) / 1e9
     traffic = None if greedy else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
