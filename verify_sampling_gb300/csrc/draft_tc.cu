@@ -25,10 +25,12 @@
 // (e, E); the logarithm E is computed only for candidates, selected by an exact
 // filter: since E >= 1 - u, an element can reach a score g only if
 // 1 - u <= e * 2^(ref - g).  The bound g is the larger of the thread's own best
-// and the best score any thread of the same request has published so far (a
-// per-request word in the workspace, raised with atomicMax).  Published scores
-// are real scores lowered by a margin, so the request's winner always passes;
-// the filter only decides which elements need the exact comparison.
+// and the best score any thread of the same row in the CTA has published so
+// far (a shared-memory word per row, raised with atomicMax).  Published scores
+// are real scores lowered by a margin, so the row's winner always passes; the
+// filter only decides which elements need the exact comparison.  The race
+// starts from the first tile's largest element, so the first tile does not
+// send every element through the exact test.
 #include "draft.cuh"
 #include "draft_tc.cuh"
 #include "fused_tc.cuh"
@@ -41,9 +43,9 @@ namespace {
 using namespace fused;
 
 // Cold path: exact race test of one filtered element; on a new best, publish
-// the request's score and return true.
+// the row's score to the CTA and return true.
 __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word, int v,
-                                               unsigned* row_best) {
+                                               uint32_t* row_best, uint32_t shared_seen) {
   const float E = -logf(uniform_from_word(word));
   if (!race_beats(e, E, v, st.be, st.bE, st.idx)) return false;
   st.be = e;
@@ -52,7 +54,8 @@ __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word,
   // score in log2 units: ref + log2(e) - log2(E), lowered by a margin that
   // covers the approximate logarithms
   const float score = st.m + lg2(e) - lg2(E) - kPublishMargin;
-  atomicMax(row_best, ordered_key(score));
+  const uint32_t key = ordered_key(score);
+  if (key > shared_seen) atomicMax(row_best, key);  // shared memory
   return true;
 }
 
@@ -77,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t full_c[kMaxStages], full_u[kMaxStages], empty_s[kMaxStages];
   __shared__ __align__(8) uint64_t tfull[kTmemBufs], tempty[kTmemBufs];
   __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t s_best[128];  // per tile row: best race score so far (ordered key, 0 = none)
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -188,22 +192,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int V = p.V, rank = p.rank, gamma = p.gamma;
 
     tc::grid_dep_wait();  // x_{k-1} written by the previous position's grid
+    // Gather A_k[x_{k-1}] for the tile's 128 requests: 128 x r bf16 in 16-byte
+    // chunks, 2*KC per thread, all loads in flight before the stores.
     const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
-    for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
-      const int i = idx / (KC * 8), c = idx % (KC * 8);
-      uint4 val = make_uint4(0, 0, 0, 0);
-      const int mm = m0 + i;
-      if (mm < p.R) {
-        int xp = (k == 1) ? p.x0[mm] : p.x[(size_t)mm * gamma + (k - 2)];
-        if (xp < 0 || xp >= V) {
-          if (c == 0) set_status(p.status, SPEC_STATUS_BAD_TOKEN);
-          xp = 0;
-        }
-        val = *reinterpret_cast<const uint4*>(Ak + (size_t)xp * rank + c * 8);
+    {
+      constexpr int kPer = 128 * KC * 8 / (kEpiWarps * 32);
+      int xp[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = threadIdx.x + j * kEpiWarps * 32, mm = m0 + idx / (KC * 8);
+        xp[j] = mm < p.R ? ((k == 1) ? p.x0[mm] : p.x[(size_t)mm * gamma + (k - 2)]) : -1;
       }
-      const int kc = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(sA + kc * 16384 + i * 128 + ((cc ^ (i & 7)) << 4)) = val;
+      uint4 val[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = threadIdx.x + j * kEpiWarps * 32, c = idx % (KC * 8), mm = m0 + idx / (KC * 8);
+        val[j] = make_uint4(0, 0, 0, 0);
+        if (mm < p.R) {
+          int x = xp[j];
+          if (x < 0 || x >= V) {
+            if (c == 0) set_status(p.status, SPEC_STATUS_BAD_TOKEN);
+            x = 0;
+          }
+          val[j] = *reinterpret_cast<const uint4*>(Ak + (size_t)x * rank + c * 8);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = threadIdx.x + j * kEpiWarps * 32, i = idx / (KC * 8), c = idx % (KC * 8);
+        const int kc = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(sA + kc * 16384 + i * 128 + ((cc ^ (i & 7)) << 4)) = val[j];
+      }
     }
+    if (threadIdx.x < 128) s_best[threadIdx.x] = 0;
     tc::fence_proxy_async();
     named_bar_sync(1, (kEpiWarps + 1) * 32);
 
@@ -219,19 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the slack in c).
     float c_own = CUDART_INF_F;
     const float kscale = kLog2e / p.draft_temp[k - 1];
+    const float2 kscale2 = make_float2(kscale, kscale);
     float nref = 0.f;  // -st.m once the reference is set
-    const uint32_t rid = p.rid_base + (uint32_t)m;
-    const PhiloxRoundKeys rk = philox_round_keys(p.key);
-    unsigned* row_best = p.row_best + (size_t)(k - 1) * p.R + (valid ? m : 0);
-    uint32_t shared_key = 0;
+    const PhiloxRow prow = philox_row((uint32_t)k, p.rid_base + (uint32_t)m, kPurposeDraft, p.rk);
+    uint32_t* row_best = &s_best[row];
     uint32_t uoff[4];
     u_offsets(row, grp, uoff, TL());
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
     Ring r{0, 0u}, rb{0, 0u};
     for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
       if (abort_flag) break;
-      const uint32_t shared_now = shared_key;
-      if (valid) shared_key = __ldcg(row_best);  // used by the next tile
       if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
           !tc::mbar_wait(&full_u[r.idx], r.phase, kWaitNs)) {
         fail();
@@ -251,45 +269,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!valid) continue;
       const int colbase = (t_begin + t) * kNT + grp * 16;
-      float z[16];  // U + bias (the temperature is folded into kscale)
+      float2 z[8];  // U + bias (the temperature is folded into kscale)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = u[i] + __uint_as_float(braw[i]);
+      for (int i = 0; i < 8; ++i)
+        z[i] = __fadd2_rn(make_float2(u[2 * i], u[2 * i + 1]),
+                          make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])));
       if (colbase + 16 > V) {  // vocabulary tail (last tile only)
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (colbase + i >= V) z[i] = -CUDART_INF_F;
+        for (int i = 0; i < 8; ++i) {
+          if (colbase + 2 * i >= V) z[i].x = -CUDART_INF_F;
+          if (colbase + 2 * i + 1 >= V) z[i].y = -CUDART_INF_F;
+        }
       }
-      if (!(st.m > -CUDART_INF_F)) {  // first tile of the row: fix the reference
-        float mz = z[0];
+      // First tile of the row: fix the reference at the tile's maximum and seed
+      // the race with that element (without a bound every element of the
+      // first tile would take the exact test).  Its e is computed exactly as
+      // the streaming pass below computes it.
+      if (!(st.m > -CUDART_INF_F)) {
+        float mz = z[0].x;
+        int im = 0;
 #pragma unroll
-        for (int i = 1; i < 16; ++i) mz = fmaxf(mz, z[i]);
+        for (int j = 1; j < 16; ++j) {
+          const float zj = (j & 1) ? z[j >> 1].y : z[j >> 1].x;
+          if (zj > mz) {
+            mz = zj;
+            im = j;
+          }
+        }
         if (!(mz > -CUDART_INF_F)) continue;
         st.m = mz * kscale;
         nref = -st.m;
+        const uint4 bits = philox_in_row((uint32_t)(colbase >> 2) + (uint32_t)(im >> 2), prow, p.rk);
+        const uint32_t wm = word_of(bits, im & 3);
+        if (race_candidate(st, tc::ex2(fmaf(mz, kscale, nref)), wm, colbase + im, row_best,
+                           *reinterpret_cast<volatile uint32_t*>(row_best)))
+          c_own = __fdividef(st.bE, st.be) * kFilterUp;
       }
       // Two halves of eight columns, each one straight-line block: two
-      // independent Philox blocks, eight exponentials, split partial sums and
-      // the race filter as one predicate; the cold path is the only branch.
+      // independent Philox blocks, eight exponentials, a tree sum and the race
+      // filter as one predicate; the cold path is the only branch.
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int cb = colbase + 8 * h;
+        // the best score any thread of this row in the CTA has found so far
+        const uint32_t shared_now = *reinterpret_cast<volatile uint32_t*>(row_best);
         uint32_t words[8];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const uint4 bits = philox((uint32_t)((cb >> 2) + q), (uint32_t)k, rid, kPurposeDraft, rk);
+          const uint4 bits = philox_in_row((uint32_t)(cb >> 2) + q, prow, p.rk);
           words[4 * q] = bits.x;
           words[4 * q + 1] = bits.y;
           words[4 * q + 2] = bits.z;
           words[4 * q + 3] = bits.w;
         }
-        float e[8];
+        float2 e[4];
+        {
+          const float2 nref2 = make_float2(nref, nref);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = tc::ex2(fmaf(z[8 * h + i], kscale, nref));
-        float ts = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+          for (int i = 0; i < 4; ++i) {
+            const float2 a = __ffma2_rn(z[4 * h + i], kscale2, nref2);
+            e[i] = make_float2(tc::ex2(a.x), tc::ex2(a.y));
+          }
+        }
+        const float2 s2 = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
+        float ts = s2.x + s2.y;
         if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
-          float mz = z[8 * h];
+          float mz = fmaxf(z[4 * h].x, z[4 * h].y);
 #pragma unroll
-          for (int i = 1; i < 8; ++i) mz = fmaxf(mz, z[8 * h + i]);
+          for (int i = 1; i < 4; ++i) mz = fmaxf(mz, fmaxf(z[4 * h + i].x, z[4 * h + i].y));
           const float mnew = fmaxf(mz * kscale, st.m);
           const float sc = tc::ex2(st.m - mnew);
           st.s *= sc;
@@ -299,9 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
           ts = 0.f;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            e[i] = tc::ex2(fmaf(z[8 * h + i], kscale, nref));
-            ts += e[i];
+          for (int i = 0; i < 4; ++i) {
+            e[i] = make_float2(tc::ex2(fmaf(z[4 * h + i].x, kscale, nref)),
+                               tc::ex2(fmaf(z[4 * h + i].y, kscale, nref)));
+            ts += e[i].x + e[i].y;
           }
         }
         st.s += ts;
@@ -314,26 +362,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // filter factor: the tighter of the own best and the request's shared best
         const float c_filt = fminf(c_own, tc::ex2(st.m - key_value(shared_now)) * kFilterUp);
+        const float2 cf2 = make_float2(c_filt, c_filt), one2 = make_float2(1.f, 1.f);
         bool any = false;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) any |= one_plus_w(words[i]) <= fmaf(e[i], c_filt, 1.0f);
+        for (int i = 0; i < 4; ++i) {
+          const float2 g = __ffma2_rn(e[i], cf2, one2);
+          any |= (one_plus_w(words[2 * i]) <= g.x) | (one_plus_w(words[2 * i + 1]) <= g.y);
+        }
         if (any) {  // rare: elements that could beat the best, in index order
           uint32_t mask = 0;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            mask |= (one_plus_w(words[i]) <= fmaf(e[i], c_filt, 1.0f) ? 1u : 0u) << i;
+          for (int i = 0; i < 4; ++i) {
+            const float2 g = __ffma2_rn(e[i], cf2, one2);
+            mask |= (one_plus_w(words[2 * i]) <= g.x ? 1u : 0u) << (2 * i);
+            mask |= (one_plus_w(words[2 * i + 1]) <= g.y ? 1u : 0u) << (2 * i + 1);
+          }
           if (cb + 8 > V) mask &= (V > cb) ? (1u << (V - cb)) - 1u : 0u;
           while (mask) {
             const int i = __ffs(mask) - 1;
             mask &= mask - 1u;
-            float ei = e[0];
+            float ei = e[0].x;
             uint32_t wi = words[0];
 #pragma unroll
             for (int j = 1; j < 8; ++j) {
-              ei = (i == j) ? e[j] : ei;
+              ei = (i == j) ? ((j & 1) ? e[j >> 1].y : e[j >> 1].x) : ei;
               wi = (i == j) ? words[j] : wi;
             }
-            if (race_candidate(st, ei, wi, cb + i, row_best))
+            if (race_candidate(st, ei, wi, cb + i, row_best, shared_now))
               c_own = __fdividef(st.bE, st.be) * kFilterUp;
           }
         }
@@ -373,19 +428,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x < kEpiWarps * 32) {
     const int row = threadIdx.x >> 2, part = threadIdx.x & 3, m = m0 + row;
     Race acc = race_empty();
-    if (m < p.R)
-      for (int s = part; s < p.nsplit; s += 4) {
-        const Partial w = load_partial(p.partials + (size_t)m * p.nsplit + s);
-        acc = race_merge2(acc, Race{w.f0, w.f1, w.f2, w.f3, w.i0});
+    if (m < p.R) {
+      // splits part, part + 4, ...: twelve loads in flight per round trip
+      // (one round trip for up to 48 splits)
+      const Partial* src = p.partials + (size_t)m * p.nsplit;
+      for (int s0 = part; s0 < p.nsplit; s0 += 48) {
+        Partial w[12];
+#pragma unroll
+        for (int q = 0; q < 12; ++q)
+          if (s0 + 4 * q < p.nsplit) w[q] = load_partial(src + s0 + 4 * q);
+#pragma unroll
+        for (int q = 0; q < 12; ++q)
+          if (s0 + 4 * q < p.nsplit) acc = race_merge2(acc, Race{w[q].f0, w[q].f1, w[q].f2, w[q].f3, w[q].i0});
       }
+    }
     acc = race_merge2(acc, race_shfl_xor(acc, 1));
     acc = race_merge2(acc, race_shfl_xor(acc, 2));
     if (part == 0 && m < p.R) {
       const size_t o = (size_t)m * p.gamma + (k - 1);
       p.x[o] = acc.idx;
       p.q_tok[o] = acc.be / acc.s;
-      // lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s, with m in log2 units
-      p.lse_q[o] = (float)((double)acc.m * 0.6931471805599453 + log((double)acc.s));
+      // lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s with m in log2 units;
+      // s = 2^k f with f in [1, 2): lse = (m + k) ln 2 + ln f, so only a small
+      // logarithm is taken and one fp64 multiply-add keeps m + k exact.
+      int ks;
+      const float f = 2.f * frexpf(acc.s, &ks);
+      p.lse_q[o] = (float)fma((double)acc.m + (double)(ks - 1), 0.6931471805599453, (double)logf(f));
     }
   }
 }
@@ -420,6 +488,7 @@ cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* C
   if (!encode_tiled(&tm_u, udt, sizeof(TL), U, 3, udims, ubox) ||
       !encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ct, 3, cdims, cbox))
     return cudaErrorInvalidValue;
+  p.rk = philox_round_keys(p.key);
   p.stages = pick_stages<TL, KC>();
   const size_t smem = smem_bytes<TL, KC>(p.stages);
   auto kern = draft_tc_kernel<TL, KC>;

@@ -12,6 +12,7 @@ struct DraftTCParams {
   int R, gamma, V, rank, k, nsplit, mtiles, ntiles, stages;
   uint32_t rid_base;
   PhiloxKey key;
+  PhiloxRoundKeys rk;  // round keys of `key` (filled by launch_draft_tc)
   const int32_t* x0;
   const float* draft_temp;
   const void* A;  // bf16 [gamma, V, rank]
@@ -20,7 +21,6 @@ struct DraftTCParams {
   float* lse_q;
   Partial* partials;   // [R, nsplit]
   unsigned* counters;  // [mtiles], zero on entry
-  unsigned* row_best;  // [gamma, R] shared race bounds (order-preserving keys), zero on entry
   uint32_t* status;
 };
 
