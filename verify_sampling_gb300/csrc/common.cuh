@@ -130,6 +130,10 @@ __device__ __forceinline__ float uniform_from_word(uint32_t x) {
 __device__ __forceinline__ float one_plus_w(uint32_t x) {
   return __uint_as_float(0x3f800000u | (~x & 0x7fffffu));
 }
+// -(1 + (1 - u) - 2^-24): the same value negated (one logic operation).
+__device__ __forceinline__ float neg_one_plus_w(uint32_t x) {
+  return __uint_as_float(0xbf800000u | (~x & 0x7fffffu));
+}
 
 // E = -ln(u) > 0, an Exp(1) variate.  logf is accurate to about one ulp of its
 // result, which keeps E accurate relative to itself even for u near 1 (u - 1

@@ -46,6 +46,7 @@ using namespace fused;
 // the row's score to the CTA and return true.
 __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word, int v,
                                                uint32_t* row_best, uint32_t shared_seen) {
+  if (!(e > 0.f)) return false;  // an underflowed (or NaN) weight never wins
   const float E = -logf(uniform_from_word(word));
   if (!race_beats(e, E, v, st.be, st.bE, st.idx)) return false;
   st.be = e;
@@ -300,19 +301,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         st.m = mz * kscale;
         nref = -st.m;
         const uint4 bits = philox_in_row((uint32_t)(colbase >> 2) + (uint32_t)(im >> 2), prow, p.rk);
-        const uint32_t wm = word_of(bits, im & 3);
-        if (race_candidate(st, tc::ex2(fmaf(mz, kscale, nref)), wm, colbase + im, row_best,
-                           *reinterpret_cast<volatile uint32_t*>(row_best)))
+        if (race_candidate(st, tc::ex2(fmaf(mz, kscale, nref)), word_of(bits, im & 3), colbase + im,
+                           row_best, *reinterpret_cast<volatile uint32_t*>(row_best)))
           c_own = __fdividef(st.bE, st.be) * kFilterUp;
       }
-      // Two halves of eight columns, each one straight-line block: two
-      // independent Philox blocks, eight exponentials, a tree sum and the race
-      // filter as one predicate; the cold path is the only branch.
+      // e = 2^(z kscale - ref) for the 16 columns and their sum (a tree)
+      float2 e[8];
+      {
+        const float2 nref2 = make_float2(nref, nref);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 a = __ffma2_rn(z[i], kscale2, nref2);
+          e[i] = make_float2(tc::ex2(a.x), tc::ex2(a.y));
+        }
+      }
+      float2 s4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s4[i] = __fadd2_rn(e[2 * i], e[2 * i + 1]);
+      const float2 s2 = __fadd2_rn(__fadd2_rn(s4[0], s4[1]), __fadd2_rn(s4[2], s4[3]));
+      float ts = s2.x + s2.y;
+      if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
+        float mz = fmaxf(z[0].x, z[0].y);
+#pragma unroll
+        for (int i = 1; i < 8; ++i) mz = fmaxf(mz, fmaxf(z[i].x, z[i].y));
+        const float mnew = fmaxf(mz * kscale, st.m);
+        const float sc = tc::ex2(st.m - mnew);
+        st.s *= sc;
+        st.be *= sc;
+        st.m = mnew;
+        nref = -mnew;
+        c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+        ts = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          e[i] = make_float2(tc::ex2(fmaf(z[i].x, kscale, nref)), tc::ex2(fmaf(z[i].y, kscale, nref)));
+          ts += e[i].x + e[i].y;
+        }
+      }
+      st.s += ts;
+      if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
+        st.s *= 0x1p-64f;
+        st.be *= 0x1p-64f;
+        st.m += 64.f;
+        nref -= 64.f;
+        c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+      }
+      // Filter factor for the tile: the tighter of the thread's own best and
+      // the best any thread of this row in the CTA has published.  An element
+      // passes when f <= e c + 1, f = 1 + (1 - u) - 2^-24; with g = e c + 1 >= 1
+      // and f in [1, 2) the difference g - f is exact, so its sign decides.
+      float2 cf2;
+      cf2.x = fminf(c_own, tc::ex2(st.m - key_value(*reinterpret_cast<volatile uint32_t*>(row_best))) *
+                               kFilterUp);
+      cf2.y = cf2.x;
+      const float2 one2 = make_float2(1.f, 1.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int cb = colbase + 8 * h;
-        // the best score any thread of this row in the CTA has found so far
-        const uint32_t shared_now = *reinterpret_cast<volatile uint32_t*>(row_best);
         uint32_t words[8];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -322,74 +367,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           words[4 * q + 2] = bits.z;
           words[4 * q + 3] = bits.w;
         }
-        float2 e[4];
-        {
-          const float2 nref2 = make_float2(nref, nref);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 a = __ffma2_rn(z[4 * h + i], kscale2, nref2);
-            e[i] = make_float2(tc::ex2(a.x), tc::ex2(a.y));
-          }
-        }
-        const float2 s2 = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
-        float ts = s2.x + s2.y;
-        if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
-          float mz = fmaxf(z[4 * h].x, z[4 * h].y);
-#pragma unroll
-          for (int i = 1; i < 4; ++i) mz = fmaxf(mz, fmaxf(z[4 * h + i].x, z[4 * h + i].y));
-          const float mnew = fmaxf(mz * kscale, st.m);
-          const float sc = tc::ex2(st.m - mnew);
-          st.s *= sc;
-          st.be *= sc;
-          st.m = mnew;
-          nref = -mnew;
-          c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
-          ts = 0.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            e[i] = make_float2(tc::ex2(fmaf(z[4 * h + i].x, kscale, nref)),
-                               tc::ex2(fmaf(z[4 * h + i].y, kscale, nref)));
-            ts += e[i].x + e[i].y;
-          }
-        }
-        st.s += ts;
-        if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
-          st.s *= 0x1p-64f;
-          st.be *= 0x1p-64f;
-          st.m += 64.f;
-          nref -= 64.f;
-          c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
-        }
-        // filter factor: the tighter of the own best and the request's shared best
-        const float c_filt = fminf(c_own, tc::ex2(st.m - key_value(shared_now)) * kFilterUp);
-        const float2 cf2 = make_float2(c_filt, c_filt), one2 = make_float2(1.f, 1.f);
-        bool any = false;
+        float2 d[4];  // g - f per element
+        uint32_t all_neg = 0xffffffffu;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 g = __ffma2_rn(e[i], cf2, one2);
-          any |= (one_plus_w(words[2 * i]) <= g.x) | (one_plus_w(words[2 * i + 1]) <= g.y);
+          d[i] = __fadd2_rn(__ffma2_rn(e[4 * h + i], cf2, one2),
+                            make_float2(neg_one_plus_w(words[2 * i]), neg_one_plus_w(words[2 * i + 1])));
+          all_neg &= __float_as_uint(d[i].x) & __float_as_uint(d[i].y);
         }
-        if (any) {  // rare: elements that could beat the best, in index order
+        if (!(all_neg >> 31)) {  // rare: elements that could beat the best, in index order
           uint32_t mask = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 g = __ffma2_rn(e[i], cf2, one2);
-            mask |= (one_plus_w(words[2 * i]) <= g.x ? 1u : 0u) << (2 * i);
-            mask |= (one_plus_w(words[2 * i + 1]) <= g.y ? 1u : 0u) << (2 * i + 1);
+            mask |= ((__float_as_uint(d[i].x) >> 31) ^ 1u) << (2 * i);
+            mask |= ((__float_as_uint(d[i].y) >> 31) ^ 1u) << (2 * i + 1);
           }
           if (cb + 8 > V) mask &= (V > cb) ? (1u << (V - cb)) - 1u : 0u;
           while (mask) {
             const int i = __ffs(mask) - 1;
             mask &= mask - 1u;
-            float ei = e[0].x;
+            float ei = e[4 * h].x;
             uint32_t wi = words[0];
 #pragma unroll
             for (int j = 1; j < 8; ++j) {
-              ei = (i == j) ? ((j & 1) ? e[j >> 1].y : e[j >> 1].x) : ei;
+              ei = (i == j) ? ((j & 1) ? e[4 * h + (j >> 1)].y : e[4 * h + (j >> 1)].x) : ei;
               wi = (i == j) ? words[j] : wi;
             }
-            if (race_candidate(st, ei, wi, cb + i, row_best, shared_now))
+            if (race_candidate(st, ei, wi, cb + i, row_best, *reinterpret_cast<volatile uint32_t*>(row_best))) {
               c_own = __fdividef(st.bE, st.be) * kFilterUp;
+              cf2.x = fminf(cf2.x, c_own);
+              cf2.y = cf2.x;
+            }
           }
         }
       }
