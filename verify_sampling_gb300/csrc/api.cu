@@ -274,6 +274,7 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   p.rank = rank;
   p.rid_base = a.request_id_base;
   p.key = philox_key(seed);
+  p.rk = philox_round_keys(p.key);
   p.inv_target_temp = sample ? 1.0f / a.target_temp : 1.0f;
   p.tgt = a.tgt;
   p.tgt_row_off = a.tgt_row_off;
@@ -294,14 +295,15 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   p.p_tok = a.p_tok;
   p.lse_t = a.lse_t;
   p.status = a.status;
-  if (sample) {
+  {
     int dev = 0, major = 0, sms = 0;
-    p.tc_residual =
+    const bool dev_ok =
         cudaGetDevice(&dev) == cudaSuccess &&
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        major == 10 && sms >= 1 && sms <= kMaxDeviceSms &&
-        resid_tc_supported(a.tgt_dtype, logit_dtype, fac_dtype, rank, a.V, a.tgt, p.U, p.A, p.Ct);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    if (!dev_ok) return SPEC_ERR_CUDA;
+    p.tc_residual = sample && major == 10 && sms >= 1 && sms <= kMaxDeviceSms &&
+                    resid_tc_supported(a.tgt_dtype, logit_dtype, fac_dtype, rank, a.V, a.tgt, p.U, p.A, p.Ct);
     p.device_sms = sms;
   }
   size_t cnt_off = 0, cnt_bytes = 0;

@@ -9,7 +9,7 @@
 //     z[m, v] = (U[m, k, v] + A_k[x_{m,k-1}, :] . C_k[:, v]) / T_k,
 // so the bias is again a rank-r GEMM: the requests of one position form the
 // M dimension (gathered, up to 128 per tile), the vocabulary the N dimension.
-// p_v = exp(L_v / T_t - m_t) / s_t uses the softmax max/sum of the target row
+// p_v = 2^(L_v log2e / T_t - m_t) / s_t uses the softmax reference/sum of the target row
 // that the verify row pass stored.
 //
 // Layout and pipelines follow the fused draft kernel (fused_tc.cuh): one CTA
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float kq = kLog2e / p.draft_temp[k - 1];
     const float nq = valid ? -p.lse_q[rk1] * kLog2e : 0.f;
     const float kt = kLog2e * p.inv_target_temp;
-    const float nt = valid ? -p.row_m[rj] * kLog2e : 0.f;
+    const float nt = valid ? -p.row_m[rj] : 0.f;  // row_m is in log2 units
     const float inv_s = valid ? 1.0f / p.row_s[rj] : 0.f;
     unsigned* row_best = p.row_best + req;
     const PhiloxRoundKeys rk = philox_round_keys(p.key);

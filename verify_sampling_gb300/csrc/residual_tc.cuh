@@ -16,7 +16,7 @@ struct ResidTCParams {
   const void* A;  // bf16 [gamma, V, rank]
   const float* lse_q;
   const int32_t* tgt_row_off;
-  const float* row_m;       // [R, gamma + 1] target-row softmax max (natural units)
+  const float* row_m;       // [R, gamma + 1] target-row softmax reference (log2 units)
   const float* row_s;       // [R, gamma + 1] target-row softmax sum
   const int* res_cnt;       // [gamma] requests whose first rejection is at j = k
   const int* res_list;      // [gamma, R] those requests

@@ -8,15 +8,16 @@
 // target's ("数学上的美感").  A fully accepted prefix earns one bonus token from
 // the next target row (the "1 +" of B in DSpark "2.2").
 //
-// Kernel 1 (rows): grid (nsplit, gamma + 1, R); CTAs of rows j > l_r + 1 exit
-// at once.  Each CTA reduces its vocabulary slice of row (r, j); the last CTA
-// of the row finishes the row (lse, accept test, bonus/argmax token); the last
-// row of the request resolves the request (first rejection, outputs).
+// Kernel 1 (rows): persistent CTAs over (request, vocabulary chunk) units,
+// reading only the scheduled rows; the last chunk of a row finishes the row
+// (lse, accept test, bonus/argmax token); the last row of the request resolves
+// the request (first rejection, outputs).
 // Kernel 2 (residual): grid (nsplit, R); only requests with a rejection work:
 // they recompute q at j* and draw the residual Gumbel-max.
 #include "verify.cuh"
 
 #include "draft_tc.cuh"
+#include "fused_tc.cuh"
 #include "residual_tc.cuh"
 
 namespace spec {
@@ -26,7 +27,7 @@ namespace {
 __device__ __forceinline__ int clamp_ell(const VerifyParams& p, int r) {
   int l = p.ell[r];
   if (l < 0 || l > p.gamma) {
-    if (threadIdx.x == 0) set_status(p.status, SPEC_STATUS_BAD_ELL);
+    if ((threadIdx.x & 31) == 0) set_status(p.status, SPEC_STATUS_BAD_ELL);
     l = l < 0 ? 0 : p.gamma;
   }
   return l;
@@ -35,7 +36,7 @@ __device__ __forceinline__ int clamp_ell(const VerifyParams& p, int r) {
 __device__ __forceinline__ size_t target_row(const VerifyParams& p, int r, int j) {
   long row = (long)p.tgt_row_off[r] + (j - 1);
   if (row < 0) {
-    if (threadIdx.x == 0) set_status(p.status, SPEC_STATUS_BAD_ROW);
+    if ((threadIdx.x & 31) == 0) set_status(p.status, SPEC_STATUS_BAD_ROW);
     row = 0;
   }
   return (size_t)row;
@@ -75,148 +76,399 @@ __device__ void resolve_request(const VerifyParams& p, int r, int l) {
 
 }  // namespace
 
-template <typename TT>
-__global__ void __launch_bounds__(kVerifyThreads) verify_rows_kernel(VerifyParams p) {
-  __shared__ Race red[kVerifyThreads / 32];
-  const int r = blockIdx.z, j = blockIdx.y + 1, split = blockIdx.x;
-  const int l = clamp_ell(p, r);
-  if (j > l + 1) return;
-  const int V = p.V, G1 = p.gamma + 1;
-  const uint32_t rid = p.rid_base + (uint32_t)r;
-  const size_t row = target_row(p, r, j);
-  const TT* L = reinterpret_cast<const TT*>(p.tgt) + row * (size_t)V;
-  const bool bonus = (j == l + 1);
-  const int nvb = (V + 3) / 4;
-  const int per = (nvb + p.nsplit - 1) / p.nsplit;
-  const int vb_begin = split * per, vb_end = min(nvb, vb_begin + per);
-  const float inv_t = p.inv_target_temp;
-  Partial* part = p.ws.row_part + ((size_t)r * G1 + (j - 1)) * p.nsplit;
+// ----------------------------------------------------------- row pass ----
+// Warp-level persistent work: a unit is one chunk (kRowChunk entries) of one
+// row (r, j); units run over (r, j, chunk) with the chunk fastest.  A warp
+// claims 32 consecutive units with one atomic, keeps those of scheduled rows
+// (j <= l_r + 1; a ballot over the claimed range) and streams each in batches
+// of 32 entries per lane (four groups of 8 consecutive entries, 16-byte
+// streaming loads); the other warps of the SM keep their loads in flight
+// meanwhile.  No block-wide barrier is used.  Log2 units: e = 2^(L log2e / T
+// - ref), the reference fixed at the lane's first batch maximum (moved if a
+// later batch overflows the sum).
+//   j <= l_r (sample): softmax partial;
+//   j == l_r + 1 (sample): softmax plus the bonus Gumbel race (purpose 3): each
+//     lane seeds its race with its first batch maximum, the warp shares the best
+//     seed, and only elements with 1 - u <= e * bE / be take the logarithm;
+//   greedy: argmax (lowest index on ties).
+// The warp that completes a row's last chunk merges the row's partials and
+// finishes the row; the one that finishes a request's last row resolves it.
 
-  if (p.mode == SPEC_VERIFY_GREEDY) {
-    ArgMax st = argmax_empty();
-    for (int vb = vb_begin + threadIdx.x; vb < vb_end; vb += blockDim.x)
+constexpr int kBatch = 32 * 32;  // entries per warp batch
+
+// Eight consecutive entries from v0 (a multiple of 8) as floats; entries at or
+// past V read as -inf.  `vec`: whole 16-byte pieces inside the row may be
+// loaded at once (16-byte aligned rows).
+__device__ __forceinline__ void load8(const float* L, long v0, long V, bool vec, float (&x)[8]) {
 #pragma unroll
-      for (int lane = 0; lane < 4; ++lane) {
-        const int v = vb * 4 + lane;
-        if (v < V) argmax_push(st, ld_f(L, (size_t)v), v);
-      }
-    ArgMax* am_red = reinterpret_cast<ArgMax*>(red);
-    st = block_reduce(
-        st, am_red,
-        [](const ArgMax& a, int off) {
-          return ArgMax{__shfl_down_sync(0xffffffffu, a.val, off),
-                        __shfl_down_sync(0xffffffffu, a.idx, off)};
-        },
-        [](const ArgMax& a, const ArgMax& b) { return argmax_merge(a, b); });
-    if (threadIdx.x == 0) {
-      Partial w{};
-      w.f0 = st.val;
-      w.i0 = st.idx;
-      part[split] = w;
-    }
-  } else if (bonus) {
-    Race st = race_empty();
-    const PhiloxKey key = p.key;
-    for (int vb = vb_begin + threadIdx.x; vb < vb_end; vb += blockDim.x) {
-      const uint4 bits = philox((uint32_t)vb, (uint32_t)j, rid, kPurposeBonus, key);
+  for (int h = 0; h < 2; ++h) {
+    const long b = v0 + 4 * h;
+    if (vec && b + 4 <= V) {
+      const float4 f = __ldcs(reinterpret_cast<const float4*>(L + b));
+      x[4 * h] = f.x;
+      x[4 * h + 1] = f.y;
+      x[4 * h + 2] = f.z;
+      x[4 * h + 3] = f.w;
+    } else {
 #pragma unroll
-      for (int lane = 0; lane < 4; ++lane) {
-        const int v = vb * 4 + lane;
-        if (v < V) race_push(st, ld_f(L, (size_t)v) * inv_t, neg_log_uniform(word_of(bits, lane)), v);
-      }
-    }
-    st = block_reduce(
-        st, red, [](const Race& a, int off) { return race_shfl_down(a, off); },
-        [](const Race& a, const Race& b) { return race_merge(a, b); });
-    if (threadIdx.x == 0) {
-      Partial w{};
-      w.f0 = st.m;
-      w.f1 = st.s;
-      w.f2 = st.be;
-      w.f3 = st.bE;
-      w.i0 = st.idx;
-      part[split] = w;
-    }
-  } else {
-    Soft st = soft_empty();
-    for (int vb = vb_begin + threadIdx.x; vb < vb_end; vb += blockDim.x)
-#pragma unroll
-      for (int lane = 0; lane < 4; ++lane) {
-        const int v = vb * 4 + lane;
-        if (v < V) soft_push(st, ld_f(L, (size_t)v) * inv_t);
-      }
-    Soft* s_red = reinterpret_cast<Soft*>(red);
-    st = block_reduce(
-        st, s_red,
-        [](const Soft& a, int off) {
-          return Soft{__shfl_down_sync(0xffffffffu, a.m, off), __shfl_down_sync(0xffffffffu, a.s, off)};
-        },
-        [](const Soft& a, const Soft& b) { return soft_merge(a, b); });
-    if (threadIdx.x == 0) {
-      Partial w{};
-      w.f0 = st.m;
-      w.f1 = st.s;
-      part[split] = w;
+      for (int i = 0; i < 4; ++i) x[4 * h + i] = (b + i < V) ? __ldcs(L + b + i) : -CUDART_INF_F;
     }
   }
-
-  const size_t rj = (size_t)r * G1 + (j - 1);
-  if (!last_block_arrives(p.ws.row_cnt + rj, (unsigned)p.nsplit)) return;
-
-  // Last CTA of row (r, j): finish the row.
-  __shared__ bool request_done;
-  if (threadIdx.x == 0) {
-    if (p.mode == SPEC_VERIFY_GREEDY) {
-      ArgMax acc = argmax_empty();
-      for (int s = 0; s < p.nsplit; ++s) {
-        const Partial w = load_partial(part + s);
-        acc = argmax_merge(acc, ArgMax{w.f0, w.i0});
-      }
-      p.ws.row_res[rj] = acc.idx;
-    } else {
-      float m, s;
-      int token = 0;
-      if (bonus) {
-        Race acc = race_empty();
-        for (int t = 0; t < p.nsplit; ++t) {
-          const Partial w = load_partial(part + t);
-          acc = race_merge(acc, Race{w.f0, w.f1, w.f2, w.f3, w.i0});
-        }
-        m = acc.m;
-        s = acc.s;
-        token = acc.idx;
-      } else {
-        Soft acc = soft_empty();
-        for (int t = 0; t < p.nsplit; ++t) {
-          const Partial w = load_partial(part + t);
-          acc = soft_merge(acc, Soft{w.f0, w.f1});
-        }
-        m = acc.m;
-        s = acc.s;
-        int xj = p.x[(size_t)r * p.gamma + (j - 1)];
-        if (xj < 0 || xj >= V) {
-          set_status(p.status, SPEC_STATUS_BAD_TOKEN);
-          xj = 0;
-        }
-        // p(x_j) = exp(L[x_j]/T - m) / s; accept iff u < p / q (q <= 0: accept).
-        const float px = expf(ld_f(L, (size_t)xj) * inv_t - m) / s;
-        const float q = p.q_tok[(size_t)r * p.gamma + (j - 1)];
-        const float u = uniform_from_word(philox(0u, (uint32_t)j, rid, kPurposeAccept, p.key).x);
-        token = (q <= 0.f || u < px / q) ? 1 : 0;
-        if (p.p_tok) p.p_tok[(size_t)r * p.gamma + (j - 1)] = px;
-      }
-      p.ws.row_m[rj] = m;
-      p.ws.row_s[rj] = s;
-      p.ws.row_res[rj] = token;
-      if (p.lse_t) p.lse_t[rj] = m + logf(s);
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* L, long v0, long V, bool vec, float (&x)[8]) {
+  if (vec && v0 + 8 <= V) {
+    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(L + v0));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      x[2 * h] = __uint_as_float(w[h] << 16);
+      x[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
     }
-    __threadfence();
-    const unsigned prev = atomicAdd(p.ws.req_cnt + r, 1u);
-    request_done = (prev == (unsigned)l);
-    if (request_done) {
-      p.ws.req_cnt[r] = 0u;
-      __threadfence();
-      resolve_request(p, r, l);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = (v0 + i < V) ? __bfloat162float(L[v0 + i]) : -CUDART_INF_F;
+  }
+}
+
+// Merge of row partials in log2 units: the softmax parts always, the race
+// parts (idx < 0: none) by the race rule.
+__device__ __forceinline__ Race row_merge(const Race& a, const Race& b) {
+  if (!(b.m > -CUDART_INF_F)) return a;
+  if (!(a.m > -CUDART_INF_F)) return b;
+  const float m = fmaxf(a.m, b.m);
+  const float sa = tc::ex2(a.m - m), sb = tc::ex2(b.m - m);
+  Race o;
+  o.m = m;
+  o.s = a.s * sa + b.s * sb;
+  const float ea = a.be * sa, eb = b.be * sb;
+  if (race_beats(ea, a.bE, a.idx, eb, b.bE, b.idx)) {
+    o.be = ea;
+    o.bE = a.bE;
+    o.idx = a.idx;
+  } else {
+    o.be = eb;
+    o.bE = b.bE;
+    o.idx = b.idx;
+  }
+  return o;
+}
+__device__ __forceinline__ Race row_shfl_xor(const Race& st, int mask) {
+  return Race{__shfl_xor_sync(0xffffffffu, st.m, mask), __shfl_xor_sync(0xffffffffu, st.s, mask),
+              __shfl_xor_sync(0xffffffffu, st.be, mask), __shfl_xor_sync(0xffffffffu, st.bE, mask),
+              __shfl_xor_sync(0xffffffffu, st.idx, mask)};
+}
+__device__ __forceinline__ ArgMax argmax_shfl_xor(const ArgMax& a, int mask) {
+  return ArgMax{__shfl_xor_sync(0xffffffffu, a.val, mask), __shfl_xor_sync(0xffffffffu, a.idx, mask)};
+}
+
+// Finish row (r, j) from its merged state (lane 0 of the finishing warp).
+__device__ void finish_row(const VerifyParams& p, int r, int j, int l, const Race& acc, float ks,
+                           const void* Lrow, bool bf16, bool bonus) {
+  const size_t rj = (size_t)r * (p.gamma + 1) + (j - 1);
+  int token = 0;
+  if (bonus) {
+    token = acc.idx;
+  } else {
+    int xj = p.x[(size_t)r * p.gamma + (j - 1)];
+    if (xj < 0 || xj >= p.V) {
+      set_status(p.status, SPEC_STATUS_BAD_TOKEN);
+      xj = 0;
+    }
+    const float lx = bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(Lrow)[xj])
+                          : reinterpret_cast<const float*>(Lrow)[xj];
+    // p(x_j) = 2^(L[x_j] log2e / T - m) / s; accept iff u < p / q (q <= 0: accept)
+    const float px = tc::ex2(fmaf(lx, ks, -acc.m)) / acc.s;
+    const float q = p.q_tok[(size_t)r * p.gamma + (j - 1)];
+    const float u = uniform_from_word(philox(0u, (uint32_t)j, p.rid_base + (uint32_t)r, kPurposeAccept, p.key).x);
+    token = (q <= 0.f || u < px / q) ? 1 : 0;
+    if (p.p_tok) p.p_tok[(size_t)r * p.gamma + (j - 1)] = px;
+  }
+  p.ws.row_m[rj] = acc.m;
+  p.ws.row_s[rj] = acc.s;
+  p.ws.row_res[rj] = token;
+  if (p.lse_t) {  // ln s = (k - 1) ln 2 + ln f with s = 2^k (f / 2), f in [1, 2)
+    int kx;
+    const float f = 2.f * frexpf(acc.s, &kx);
+    p.lse_t[rj] = (float)fma((double)acc.m + (double)(kx - 1), 0.6931471805599453, (double)logf(f));
+  }
+  (void)l;
+}
+
+// Plan: the packed list of scheduled rows, rows[b] = r * (gamma + 1) + j - 1
+// for j = 1 .. l_r + 1 in request order, and their number B (one CTA).
+__global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyParams p) {
+  __shared__ int warp_sum[kPlanThreads / 32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G1 = p.gamma + 1;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < p.R; r0 += kPlanThreads) {  // uniform trip count
+    const int r = r0 + tid;
+    const int n = (r < p.R) ? clamp_ell(p, r) + 1 : 0;
+    int incl = n;  // inclusive warp scan
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int before = carry;
+    for (int w = 0; w < warp; ++w) before += warp_sum[w];
+    const int start = before + incl - n;
+    for (int q = 0; q < n; ++q) p.ws.row_list[start + q] = r * G1 + q;
+    __syncthreads();
+    if (tid == kPlanThreads - 1) carry = start + n;
+    __syncthreads();
+  }
+  if (tid == 0) *p.ws.n_rows = carry;
+}
+
+template <typename TT>
+__global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyParams p) {
+  const int lane = threadIdx.x & 31;
+  const long V = p.V;
+  const int G1 = p.gamma + 1, cpr = p.nsplit;
+  const float ks = fused::kLog2e * p.inv_target_temp;  // log2 units per logit
+  const bool greedy = p.mode == SPEC_VERIFY_GREEDY;
+  const bool vec = ((size_t)V * sizeof(TT)) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.tgt) & 15) == 0;
+
+  const unsigned long long units = (unsigned long long)(*p.ws.n_rows) * cpr;
+  // one unit per claim; the next claim is issued before the current unit runs
+  unsigned long long next = 0;
+  if (lane == 0) next = atomicAdd(p.ws.unit_cnt, 1ull);
+  for (;;) {
+    const unsigned long long unit = __shfl_sync(0xffffffffu, next, 0);
+    if (unit >= units) break;
+    if (lane == 0) next = atomicAdd(p.ws.unit_cnt, 1ull);
+    {
+      const int c = (int)(unit % (unsigned long long)cpr);
+      const int code = p.ws.row_list[unit / (unsigned long long)cpr];
+      const int r = code / G1, j = code % G1 + 1;
+      const int l = clamp_ell(p, r);
+      const uint32_t rid = p.rid_base + (uint32_t)r;
+      const bool bonus = !greedy && j == l + 1;
+      const TT* L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, r, j) * (size_t)V;
+      const long c0 = (long)c * kRowChunk, c1 = c0 + kRowChunk < V ? c0 + kRowChunk : V;
+
+      Race st = race_empty();  // log2 units; be, bE, idx: bonus race
+      ArgMax am = argmax_empty();
+      float c_own = CUDART_INF_F;  // bonus: filter factor bE / be (with slack)
+      PhiloxRow prow{};
+      if (bonus) prow = philox_row((uint32_t)j, rid, kPurposeBonus, p.rk);
+      for (long b0 = c0; b0 < c1; b0 += kBatch) {
+        float x[4][8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) load8(L, b0 + g * 256 + lane * 8, c1, vec, x[g]);
+        if (greedy) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int v = (int)(b0 + g * 256 + lane * 8 + q);
+              if (v < c1 && (am.idx < 0 || x[g][q] > am.val)) {
+                am.val = x[g][q];
+                am.idx = v;
+              }
+            }
+          continue;
+        }
+        // reference: the first batch's maximum (per lane); a later batch moves
+        // it only when its sum overflows
+        bool seed = false;
+        int im = 0;
+        float mx = -CUDART_INF_F;
+        if (!(st.m > -CUDART_INF_F)) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (x[g][q] > mx) {
+                mx = x[g][q];
+                im = g * 8 + q;
+              }
+          if (mx > -CUDART_INF_F) {
+            st.m = mx * ks;
+            seed = bonus;
+          }
+        }
+        // Lanes without a finite entry yet (e.g. past V in a tail chunk) take
+        // part in the warp-wide steps below but contribute nothing; the batch
+        // is skipped only when the whole warp has nothing.
+        const bool have = st.m > -CUDART_INF_F;
+        if (!__any_sync(0xffffffffu, have)) continue;
+        float2 e2[4][4];  // the loaded values die here (an overflow reloads them)
+        if (have) {
+          float ts = 0.f;
+          {
+            const float2 ks2 = make_float2(ks, ks), nref2 = make_float2(-st.m, -st.m);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 a = __ffma2_rn(make_float2(x[g][2 * q], x[g][2 * q + 1]), ks2, nref2);
+                e2[g][q] = make_float2(tc::ex2(a.x), tc::ex2(a.y));
+              }
+              const float2 t = __fadd2_rn(__fadd2_rn(e2[g][0], e2[g][1]), __fadd2_rn(e2[g][2], e2[g][3]));
+              ts += t.x + t.y;
+            }
+          }
+          if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
+#pragma unroll
+            for (int g = 0; g < 4; ++g) load8(L, b0 + g * 256 + lane * 8, c1, vec, x[g]);
+            float mz = -CUDART_INF_F;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+              for (int q = 0; q < 8; ++q) mz = fmaxf(mz, x[g][q]);
+            const float mnew = fmaxf(mz * ks, st.m);
+            const float sc = tc::ex2(st.m - mnew);
+            st.s *= sc;
+            st.be *= sc;
+            st.m = mnew;
+            if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
+            ts = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                e2[g][q] = make_float2(tc::ex2(fmaf(x[g][2 * q], ks, -st.m)), tc::ex2(fmaf(x[g][2 * q + 1], ks, -st.m)));
+                ts += e2[g][q].x + e2[g][q].y;
+              }
+          }
+          st.s += ts;
+          if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
+            st.s *= 0x1p-64f;
+            st.be *= 0x1p-64f;
+            st.m += 64.f;
+            if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                e2[g][q].x *= 0x1p-64f;
+                e2[g][q].y *= 0x1p-64f;
+              }
+          }
+          if (seed) {  // this lane's first finite batch: seed its race with the maximum
+            const int vm = (int)(b0 + (im >> 3) * 256 + lane * 8 + (im & 7));
+            const uint4 bm = philox_in_row((uint32_t)(vm >> 2), prow, p.rk);
+            float em = 0.f;  // e of entry im (unrolled select: no local-memory indexing)
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+              for (int q = 0; q < 8; ++q) em = (im == g * 8 + q) ? ((q & 1) ? e2[g][q >> 1].y : e2[g][q >> 1].x) : em;
+            st.be = em;
+            st.bE = -logf(uniform_from_word(word_of(bm, vm & 3)));
+            st.idx = vm;
+            c_own = (st.bE / st.be) * fused::kFilterUp;
+          }
+        }
+        if (!bonus) continue;  // uniform
+        // ---- bonus race over this batch ----
+        // the warp's best lowered score (lanes without a best give -inf); all lanes
+        float gbest = (st.idx >= 0) ? st.m + fused::lg2(st.be) - fused::lg2(st.bE) - fused::kPublishMargin
+                                    : -CUDART_INF_F;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) gbest = fmaxf(gbest, __shfl_xor_sync(0xffffffffu, gbest, off));
+        if (have) {
+          const float cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
+          const float2 cf2 = make_float2(cf, cf), one2 = make_float2(1.f, 1.f);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const long v0 = b0 + g * 256 + lane * 8;
+            uint32_t words[8];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const uint4 bb = philox_in_row((uint32_t)(v0 >> 2) + q, prow, p.rk);
+              words[4 * q] = bb.x;
+              words[4 * q + 1] = bb.y;
+              words[4 * q + 2] = bb.z;
+              words[4 * q + 3] = bb.w;
+            }
+            uint32_t all_neg = 0xffffffffu;
+            float2 d[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              d[q] = __fadd2_rn(__ffma2_rn(e2[g][q], cf2, one2),
+                                make_float2(neg_one_plus_w(words[2 * q]), neg_one_plus_w(words[2 * q + 1])));
+              all_neg &= __float_as_uint(d[q].x) & __float_as_uint(d[q].y);
+            }
+            if (!(all_neg >> 31)) {  // rare: exact race test in index order
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float dq = (q & 1) ? d[q >> 1].y : d[q >> 1].x;
+                const float eq = (q & 1) ? e2[g][q >> 1].y : e2[g][q >> 1].x;
+                if (!(__float_as_uint(dq) >> 31) && eq > 0.f && v0 + q < c1) {
+                  const float E = -logf(uniform_from_word(words[q]));
+                  if (race_beats(eq, E, (int)(v0 + q), st.be, st.bE, st.idx)) {
+                    st.be = eq;
+                    st.bE = E;
+                    st.idx = (int)(v0 + q);
+                    c_own = (st.bE / st.be) * fused::kFilterUp;
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      // warp merge of the unit, partial, and the row / request completion
+      Partial w{};
+      if (greedy) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) am = argmax_merge(am, argmax_shfl_xor(am, off));
+        w.f0 = am.val;
+        w.i0 = am.idx;
+      } else {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) st = row_merge(st, row_shfl_xor(st, off));
+        w.f0 = st.m;
+        w.f1 = st.s;
+        w.f2 = st.be;
+        w.f3 = st.bE;
+        w.i0 = st.idx;
+      }
+      const size_t rj = (size_t)r * G1 + (j - 1);
+      Partial* part = p.ws.row_part + rj * cpr;
+      bool last = false;
+      if (lane == 0) {
+        part[c] = w;
+        __threadfence();
+        last = atomicAdd(p.ws.row_cnt + rj, 1u) == (unsigned)(cpr - 1);
+        if (last) __threadfence();
+      }
+      if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+      if (lane == 0) p.ws.row_cnt[rj] = 0u;
+      if (greedy) {
+        ArgMax acc = argmax_empty();
+        for (int s = lane; s < cpr; s += 32) {
+          const Partial q = load_partial(part + s);
+          acc = argmax_merge(acc, ArgMax{q.f0, q.i0});
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc = argmax_merge(acc, argmax_shfl_xor(acc, off));
+        if (lane == 0) p.ws.row_res[rj] = acc.idx;
+      } else {
+        Race acc = race_empty();
+        for (int s = lane; s < cpr; s += 32) {
+          const Partial q = load_partial(part + s);
+          acc = row_merge(acc, Race{q.f0, q.f1, q.f2, q.f3, q.i0});
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc = row_merge(acc, row_shfl_xor(acc, off));
+        if (lane == 0) finish_row(p, r, j, l, acc, ks, L, sizeof(TT) == 2, bonus);
+      }
+      if (lane == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(p.ws.req_cnt + r, 1u);
+        if (prev == (unsigned)l) {
+          p.ws.req_cnt[r] = 0u;
+          __threadfence();
+          resolve_request(p, r, l);
+        }
+      }
     }
   }
 }
@@ -234,7 +486,7 @@ __global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p
   const int V = p.V, G1 = p.gamma + 1, rank = p.rank;
   const uint32_t rid = p.rid_base + (uint32_t)r;
   const size_t rj = (size_t)r * G1 + (jstar - 1);
-  const float m_t = p.ws.row_m[rj], s_t = p.ws.row_s[rj];
+  const float m_t = p.ws.row_m[rj], s_t = p.ws.row_s[rj];  // m_t in log2 units
   const float inv_s_t = 1.0f / s_t;
   const TT* L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, r, jstar) * (size_t)V;
   const int k = jstar;
@@ -262,7 +514,7 @@ __global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p
         float bias = 0.f;
         for (int i = 0; i < rank; ++i) bias = fmaf(arow[i], ld_f(Ct, (size_t)v * rank + i), bias);
         const float zq = (ld_f(U, (size_t)v) + bias) * inv_tq;
-        const float et = expf(ld_f(L, (size_t)v) * inv_tt - m_t);
+        const float et = exp2f(fmaf(ld_f(L, (size_t)v), inv_tt * fused::kLog2e, -m_t));
         const float pv = et * inv_s_t;
         const float qv = expf(zq - lse_q);
         const float E = neg_log_uniform(word_of(bits, lane));
@@ -308,8 +560,8 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Scratch layout: arrays that need no initialisation first, then the
 // counters and flags that every call zeroes in one memset.
-enum { kRowPart, kResPart, kRowM, kRowS, kRowRes, kReqJstar, kResList, kRtPart,
-       kRowCnt, kReqCnt, kResCnt, kResNum, kRtCnt, kRtBest, kFallback, kLayoutN };
+enum { kRowPart, kResPart, kRowM, kRowS, kRowRes, kReqJstar, kResList, kRtPart, kRowList, kNRows,
+       kUnitCnt, kRowCnt, kReqCnt, kResCnt, kResNum, kRtCnt, kRtBest, kFallback, kLayoutN };
 
 static size_t layout(int R, int gamma, int V, size_t off[kLayoutN]) {
   const size_t rows = (size_t)R * (gamma + 1);
@@ -318,15 +570,15 @@ static size_t layout(int R, int gamma, int V, size_t off[kLayoutN]) {
   const size_t sizes[kLayoutN] = {rows * ns * sizeof(Partial), (size_t)R * nr * sizeof(Partial),
                                   rows * sizeof(float), rows * sizeof(float), rows * sizeof(int),
                                   (size_t)R * sizeof(int), (size_t)gamma * R * sizeof(int),
-                                  mt * 128 * kMaxDeviceSms * sizeof(Partial),
-                                  rows * sizeof(unsigned), (size_t)R * sizeof(unsigned),
+                                  mt * 128 * kMaxDeviceSms * sizeof(Partial), rows * sizeof(int),
+                                  sizeof(int), sizeof(unsigned long long), rows * sizeof(unsigned), (size_t)R * sizeof(unsigned),
                                   (size_t)R * sizeof(unsigned), (size_t)gamma * sizeof(int),
                                   mt * sizeof(unsigned), (size_t)R * sizeof(unsigned),
                                   (size_t)R * sizeof(int)};
   size_t o = 0;
   for (int i = 0; i < kLayoutN; ++i) {
     off[i] = o;
-    o = (i < kRowCnt) ? align_up(o + sizes[i]) : o + sizes[i];
+    o = (i < kUnitCnt) ? align_up(o + sizes[i]) : o + sizes[i];  // counters packed after
   }
   return align_up(o);
 }
@@ -350,6 +602,8 @@ VerifyScratch verify_scratch_carve(void* base, int R, int gamma, int V, size_t* 
   s.req_jstar = reinterpret_cast<int*>(b + off[kReqJstar]);
   s.res_list = reinterpret_cast<int*>(b + off[kResList]);
   s.rt_part = reinterpret_cast<Partial*>(b + off[kRtPart]);
+  s.row_list = reinterpret_cast<int*>(b + off[kRowList]);
+  s.n_rows = reinterpret_cast<int*>(b + off[kNRows]);
   s.row_cnt = reinterpret_cast<unsigned*>(b + off[kRowCnt]);
   s.req_cnt = reinterpret_cast<unsigned*>(b + off[kReqCnt]);
   s.res_cnt = reinterpret_cast<unsigned*>(b + off[kResCnt]);
@@ -357,7 +611,8 @@ VerifyScratch verify_scratch_carve(void* base, int R, int gamma, int V, size_t* 
   s.rt_cnt = reinterpret_cast<unsigned*>(b + off[kRtCnt]);
   s.rt_best = reinterpret_cast<unsigned*>(b + off[kRtBest]);
   s.fallback = reinterpret_cast<int*>(b + off[kFallback]);
-  *counters_offset = off[kRowCnt];
+  s.unit_cnt = reinterpret_cast<unsigned long long*>(b + off[kUnitCnt]);
+  *counters_offset = off[kUnitCnt];
   *counters_bytes = total - off[kRowCnt];
   return s;
 }
@@ -366,7 +621,8 @@ VerifyScratch verify_scratch_carve(void* base, int R, int gamma, int V, size_t* 
 template <typename TT, typename TL, typename TF>
 static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_dtype,
                                 cudaStream_t stream) {
-  const dim3 g1((unsigned)p.nsplit, (unsigned)(p.gamma + 1), (unsigned)p.R);
+  verify_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+  const unsigned g1 = (unsigned)(2 * std::max(1, p.device_sms));
   verify_rows_kernel<TT><<<g1, kVerifyThreads, 0, stream>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || p.mode == SPEC_VERIFY_GREEDY) return err;

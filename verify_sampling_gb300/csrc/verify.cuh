@@ -8,16 +8,20 @@
 namespace spec {
 
 constexpr int kVerifyThreads = 256;
+constexpr int kRowChunk = 8192;  // vocabulary entries per row-pass work unit
+constexpr int kPlanThreads = 1024;
 
 // Per-call scratch carved out of the caller's workspace.
 struct VerifyScratch {
   Partial* row_part;  // [R, gamma + 1, nsplit]
   Partial* res_part;  // [R, nsplit] (two races per record)
-  float* row_m;       // [R, gamma + 1] softmax max of L / T_t
-  float* row_s;       // [R, gamma + 1] softmax sum
+  float* row_m;       // [R, gamma + 1] softmax reference of L / T_t, log2 units
+  float* row_s;       // [R, gamma + 1] softmax sum of 2^(L log2e / T_t - row_m)
   int* row_res;       // [R, gamma + 1] accept bit (sample) / argmax (greedy) / bonus token
   int* req_jstar;     // [R] residual position (0: none)
   int* res_list;      // [gamma, R] requests per rejected position (fused residual)
+  int* row_list;      // [R * (gamma + 1)] scheduled rows r * (gamma + 1) + j - 1, packed
+  int* n_rows;        // [1] number of scheduled rows
   Partial* rt_part;   // [max_mtiles, 128, kMaxDeviceSms] fused-residual partials
   unsigned* row_cnt;  // [R, gamma + 1]   } zeroed together
   unsigned* req_cnt;  // [R]              } at the start
@@ -26,12 +30,14 @@ struct VerifyScratch {
   unsigned* rt_cnt;   // [max_mtiles]     }
   unsigned* rt_best;  // [R]              }
   int* fallback;      // [R]              }
+  unsigned long long* unit_cnt;  // [1] row-pass work counter }
 };
 
 struct VerifyParams {
   int mode, R, gamma, V, nsplit, rank;
   uint32_t rid_base;
   PhiloxKey key;
+  PhiloxRoundKeys rk;  // round keys of `key`
   float inv_target_temp;
   const void* tgt;
   const int32_t* tgt_row_off;
@@ -56,11 +62,11 @@ struct VerifyParams {
   VerifyScratch ws;
 };
 
+// Row-pass work units per row (vocabulary chunks of kRowChunk entries).
 inline int verify_nsplit(int R, int gamma, int V) {
-  const long rows = (long)R * (gamma + 1);
-  const int target_ctas = 4 * 152 * 2;
-  const int max_split = std::max(1, (V + 2047) / 2048);
-  return (int)std::max<long>(1, std::min<long>(max_split, (target_ctas + rows - 1) / rows));
+  (void)R;
+  (void)gamma;
+  return std::max(1, (V + kRowChunk - 1) / kRowChunk);
 }
 
 inline int residual_nsplit(int R, int V) {
