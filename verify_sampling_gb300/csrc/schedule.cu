@@ -6,12 +6,12 @@
 // adds the top-K cap and the global search.  History article, "杀招三": the
 // same rule walked through.
 //
-// Layout of the work: N = R * gamma 64-bit keys (~bits(a) << 32 | id) are
-// bitonic-sorted ascending in shared memory, which orders a descending and ties
-// by id = r * gamma + j - 1 ascending (request, then position).  tau_n is an
-// fp64 inclusive scan of the sorted survivals, Theta_n = tau_n * SPS(R + n);
-// the early-stop index is the first n with Theta_{n+1} <= Theta_n and the
-// global index the smallest argmax.
+// Layout of the work: the N = R * gamma keys ~bits(a) are radix-sorted
+// ascending (stable, so a descending with ties by id = r * gamma + j - 1
+// ascending: request, then position) in shared memory.  tau_n is an fp64
+// inclusive scan of the sorted survivals, Theta_n = tau_n * SPS(R + n); the
+// early-stop index is the first n with Theta_{n+1} <= Theta_n and the global
+// index the smallest argmax.
 #include "schedule.cuh"
 
 namespace spec {
@@ -19,6 +19,7 @@ namespace spec {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kHistCells = 32 * 257;  // radix digit histograms, [warp][257]
 
 __device__ __forceinline__ double sps_at(const float* sps, int n_sps, double b_lo, double b_step,
                                          double B) {
@@ -31,16 +32,6 @@ __device__ __forceinline__ double sps_at(const float* sps, int n_sps, double b_l
   const int i = (int)fi;
   const double f = __dsub_rn(t, fi);
   return __dadd_rn(__dmul_rn(__dsub_rn(1.0, f), (double)sps[i]), __dmul_rn(f, (double)sps[i + 1]));
-}
-
-__device__ __forceinline__ double warp_incl_scan(double v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v = __dadd_rn(v, o);
-  }
-  return v;
 }
 
 __device__ __forceinline__ int warp_incl_scan_int(int v) {
@@ -57,93 +48,198 @@ __device__ __forceinline__ int warp_incl_scan_int(int v) {
 
 __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int N = p.R * p.gamma;
-  const int npow2 = p.npow2;
-  uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);                 // [npow2 + 8]
-  double* theta = reinterpret_cast<double*>(smem_raw);                     // aliases keys
-  int* ids = reinterpret_cast<int*>(smem_raw + sizeof(uint64_t) * (npow2 + 8));  // [N]
-  int* ell_s = ids + N;                                                    // [R]
-  __shared__ double seg_sum[kThreads];
-  __shared__ double warp_tot[32];
+  const int N = p.R * p.gamma, Np = p.npad;
+  // [Np] each, in this order: keyA, valA, keyB, valB (keyB and valB together
+  // hold Theta once the sort is done)
+  uint32_t* keyA = reinterpret_cast<uint32_t*>(smem_raw);
+  int* valA = reinterpret_cast<int*>(keyA + Np);
+  uint32_t* keyB = reinterpret_cast<uint32_t*>(valA + Np);
+  int* valB = reinterpret_cast<int*>(keyB + Np);
+  int* hist = valB + Np;         // [32 warps][257]: digit d of warp w at w * 257 + d
+  int* ell_s = hist + kHistCells;  // [R]
+  double* theta = reinterpret_cast<double*>(keyB);  // after the sort: [nmax + 1] over keyB, valB
+  __shared__ unsigned long long seg_q[kThreads];
   __shared__ int warp_itot[32];
   __shared__ int nstar_s;
   __shared__ double best_s[32];
   __shared__ int bestn_s[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // 1. keys: a >= 0 as float bits (monotone for non-negative floats).
-  for (int i = tid; i < npow2; i += kThreads) {
-    uint64_t key = ~0ull;
-    if (i < N) {
-      float a = p.a[i];
-      if (!(a >= 0.f) || isinf(a)) {  // negative, NaN or inf
-        set_status(p.status, SPEC_STATUS_BAD_SURVIVAL);
-        a = 0.f;
-      }
-      const uint32_t bits = __float_as_uint(a + 0.0f);  // -0 -> +0
-      key = ((uint64_t)(~bits) << 32) | (uint32_t)i;
+  // 1. keys: ~bits(a) ascending is a descending (float bits are monotone for
+  // a >= 0); the sort below is stable, so equal a keep id order (request, then
+  // position).
+  for (int i = tid; i < N; i += kThreads) {
+    float a = p.a[i];
+    if (!(a >= 0.f) || isinf(a)) {  // negative, NaN or inf
+      set_status(p.status, SPEC_STATUS_BAD_SURVIVAL);
+      a = 0.f;
     }
-    keys[i] = key;
+    keyA[i] = ~__float_as_uint(a + 0.0f);  // -0 -> +0
+    valA[i] = i;
   }
   __syncthreads();
 
-  // 2. bitonic sort, ascending.
-  for (int kk = 2; kk <= npow2; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < npow2; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t a = keys[i], b = keys[ixj];
-          const bool up = (i & kk) == 0;
-          if ((a > b) == up) {
-            keys[i] = b;
-            keys[ixj] = a;
-          }
+  // 2. stable LSD radix sort, 8-bit digits, 4 passes.  Warp w owns a
+  // contiguous segment of the array; ranks inside a warp step come from
+  // __match_any_sync, offsets from a scan of the per-warp digit histograms in
+  // (digit, warp) order, which keeps equal digits in array order.
+  {
+    const int seg = (((N + 31) / 32) + 31) & ~31;  // per-warp segment, multiple of 32
+    const int wb = warp * seg;
+    uint32_t *ks = keyA, *kd = keyB;
+    int *vs = valA, *vd = valB;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 8 * pass;
+      for (int i = tid; i < kHistCells; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      for (int s0 = 0; s0 < seg; s0 += 32) {
+        const int idx = wb + s0 + lane;
+        const bool valid = idx < N;
+        const uint32_t d = valid ? (ks[idx] >> shift) & 255u : 256u;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (valid && lane == __ffs(peers) - 1) hist[warp * 257 + d] += __popc(peers);
+      }
+      __syncthreads();
+      {
+        // cells in (digit, warp) order: cell c = d * 32 + w, eight per thread
+        int loc[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = tid * 8 + q;
+          loc[q] = hist[(c & 31) * 257 + (c >> 5)];
+          sum += loc[q];
+        }
+        const int incl = warp_incl_scan_int(sum);
+        if (lane == 31) warp_itot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+          const int wt = warp_itot[lane];
+          warp_itot[lane] = warp_incl_scan_int(wt) - wt;
+        }
+        __syncthreads();
+        int run = warp_itot[warp] + incl - sum;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = tid * 8 + q;
+          hist[(c & 31) * 257 + (c >> 5)] = run;
+          run += loc[q];
         }
       }
       __syncthreads();
+      for (int s0 = 0; s0 < seg; s0 += 32) {
+        const int idx = wb + s0 + lane;
+        const bool valid = idx < N;
+        uint32_t key = 0u, d = 256u;
+        int val = 0;
+        if (valid) {
+          key = ks[idx];
+          val = vs[idx];
+          d = (key >> shift) & 255u;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const int base = valid ? hist[warp * 257 + d] : 0;
+        __syncwarp();
+        if (valid) {
+          const int pos = base + __popc(peers & ((1u << lane) - 1u));
+          kd[pos] = key;
+          vd[pos] = val;
+          if (lane == __ffs(peers) - 1) hist[warp * 257 + d] = base + __popc(peers);
+        }
+        __syncwarp();
+      }
+      __syncthreads();
+      uint32_t* tk = ks;
+      ks = kd;
+      kd = tk;
+      int* tv = vs;
+      vs = vd;
+      vd = tv;
     }
   }
+  // four passes: the sorted keys and ids are back in keyA / valA
 
-  // 3. ids and sorted survivals; zero the per-request counts.
-  for (int i = tid; i < N; i += kThreads) ids[i] = (int)(keys[i] & 0xffffffffu);
+  // 3. zero the per-request counts; SPS(R + n) for every admissible n, in
+  // parallel (theta[n] holds it until step 4 multiplies in tau_n).
+  const int nmax = min(p.K, N);
   for (int i = tid; i < p.R; i += kThreads) ell_s[i] = 0;
+  for (int n = tid; n <= nmax; n += kThreads) {
+    double v = 0.0;
+    if (n > 0) {
+      if (p.unit_grid) {
+        // b_step = 1 and integral b_lo: t = B - b_lo is an integer, so the
+        // interpolation weight is 0 and the value is the table entry itself
+        const long t = (long)(p.R + n) - p.b_lo_int;
+        v = (double)p.sps[t <= 0 ? 0 : (t >= p.n_sps - 1 ? p.n_sps - 1 : t)];
+      } else {
+        v = sps_at(p.sps, p.n_sps, p.b_lo, p.b_step, (double)(p.R + n));
+      }
+    }
+    theta[n] = v;
+  }
   __syncthreads();
 
-  // 4. tau_n, Theta_n (fp64).  Thread t owns sorted positions [t*per, (t+1)*per).
-  const int nmax = min(p.K, N);
+  // 4. tau_n, Theta_n = tau_n * SPS(R + n).  tau is an exact prefix sum in
+  // 64-bit fixed point scaled to the largest survival a_1 (the first sorted
+  // entry): each a_k is truncated to a multiple of 2^-shift with
+  // a_1 * 2^shift < 2^49, so the 8192-term sums stay below 2^62 and the total
+  // truncation is below 2^-36 a_1 <= 2^-36 tau_n.  One conversion to fp64 per
+  // position.  Thread t owns sorted positions [t*per, (t+1)*per).
   const int per = (N + kThreads - 1) / kThreads;
   const int lo = tid * per, hi = min(N, lo + per);
-  double local = 0.0;
-  for (int i = lo; i < hi; ++i) local = __dadd_rn(local, (double)__uint_as_float(~(uint32_t)(keys[i] >> 32)));
-  double incl = warp_incl_scan(local);
-  if (lane == 31) warp_tot[warp] = incl;
+  const int cnt = hi - lo;
+  int e1;  // a_1 < 2^e1
+  frexpf(__uint_as_float(~keyA[0]), &e1);
+  const int shift = 49 - e1;
+  auto fixed = [&](float a) -> unsigned long long {
+    // a = m * 2^(ex - 24) with m the 24-bit significand; a * 2^shift, truncated
+    if (!(a > 0.f)) return 0ull;
+    int ex;
+    const float fr = frexpf(a, &ex);  // a = fr * 2^ex, fr in [0.5, 1)
+    const unsigned long long m = (unsigned long long)(fr * 16777216.0f);  // exact: fr * 2^24
+    const int sh = ex - 24 + shift;
+    if (sh >= 0) return m << sh;  // sh <= 25 since a <= a_1
+    return sh > -64 ? (m >> (-sh)) : 0ull;
+  };
+  unsigned long long qv[kSchedMaxCandidates / kThreads];
+  unsigned long long local = 0ull;
+#pragma unroll
+  for (int i = 0; i < kSchedMaxCandidates / kThreads; ++i) {
+    qv[i] = (i < cnt) ? fixed(__uint_as_float(~keyA[lo + i])) : 0ull;
+    local += qv[i];
+  }
+  unsigned long long incl = local;  // inclusive warp scan
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  __shared__ unsigned long long warp_q[32];
+  if (lane == 31) warp_q[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    double wt = warp_tot[lane];
-    double wi = warp_incl_scan(wt);
-    warp_tot[lane] = __dsub_rn(wi, wt);  // exclusive prefix of warp totals
-  }
-  __syncthreads();
-  const double excl = __dadd_rn(warp_tot[warp], __dsub_rn(incl, local));
-  seg_sum[tid] = excl;
-  // Sorted survivals of my segment before theta overwrites the keys.
-  float mine[16];
-  const int cnt = hi - lo;
-  for (int i = 0; i < cnt && i < 16; ++i) mine[i] = __uint_as_float(~(uint32_t)(keys[lo + i] >> 32));
-  __syncthreads();
-  {
-    double tau = excl;
-    if (tid == 0) theta[0] = 0.0;
-    for (int i = 0; i < cnt; ++i) {
-      tau = __dadd_rn(tau, (double)mine[i]);
-      const int n = lo + i + 1;
-      if (n <= nmax)
-        theta[n] = __dmul_rn(tau, sps_at(p.sps, p.n_sps, p.b_lo, p.b_step, (double)(p.R + n)));
+    const unsigned long long wt = warp_q[lane];
+    unsigned long long wi = wt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long o = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += o;
     }
+    warp_q[lane] = wi - wt;  // exclusive prefix of warp totals
   }
   __syncthreads();
-
+  const double unit = ldexp(1.0, -shift);  // exact power of two
+  {
+    unsigned long long run = warp_q[warp] + incl - local;
+#pragma unroll
+    for (int i = 0; i < kSchedMaxCandidates / kThreads; ++i)
+      if (i < cnt) {
+        run += qv[i];
+        const int n = lo + i + 1;
+        if (n <= nmax) theta[n] = __dmul_rn(__dmul_rn((double)run, unit), theta[n]);
+      }
+    seg_q[tid] = warp_q[warp] + incl - local;
+  }
+  __syncthreads();
   // 5. choose n*.
   if (p.mode == SPEC_SCHED_EARLY_STOP) {
     int first = nmax;
@@ -195,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
   const int nstar = nstar_s;
 
   // 6. l_r, row offsets, stats, order.
-  for (int n = tid; n < nstar; n += kThreads) atomicAdd(&ell_s[ids[n] / p.gamma], 1);
+  for (int n = tid; n < nstar; n += kThreads) atomicAdd(&ell_s[valA[n] / p.gamma], 1);
   __syncthreads();
   {
     // exclusive scan of (1 + l_r) over R entries, per-thread segments
@@ -221,8 +317,8 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
     if (p.R == 0 && tid == 0) p.row_off[0] = 0;
   }
   if (p.order)
-    for (int i = tid; i < N; i += kThreads) p.order[i] = ids[i];
-  // tau at n*: the owner of sorted position n* - 1 recomputes its prefix.
+    for (int i = tid; i < N; i += kThreads) p.order[i] = valA[i];
+  // tau at n*: the owner of sorted position n* - 1 sums its prefix again.
   if (nstar == 0) {
     if (tid == 0) {
       p.stats[0] = 0.0;
@@ -231,27 +327,28 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
       p.stats[3] = 0.0;
     }
   } else if (nstar - 1 >= lo && nstar - 1 < hi) {
-    double tau = seg_sum[tid];
-    for (int i = 0; i < nstar - lo; ++i) tau = __dadd_rn(tau, (double)mine[i]);
+    unsigned long long run = seg_q[tid];
+    for (int i = lo; i < nstar; ++i) run += fixed(__uint_as_float(~keyA[i]));
     p.stats[0] = (double)nstar;
     p.stats[1] = (double)(p.R + nstar);
-    p.stats[2] = tau;
+    p.stats[2] = __dmul_rn((double)run, unit);
     p.stats[3] = theta[nstar];
   }
 }
 
+// keys and ids twice (radix ping-pong; the second pair later holds Theta as
+// doubles: Np >= N + 1), the digit histograms and the per-request counts.
+static int sched_npad(int R, int gamma) { return ((R * gamma + 1) + 31) & ~31; }
+
 size_t schedule_smem_bytes(int R, int gamma) {
-  const int N = R * gamma;
-  int npow2 = 2;
-  while (npow2 < N) npow2 <<= 1;
-  return sizeof(uint64_t) * (size_t)(npow2 + 8) + sizeof(int) * (size_t)(N + R);
+  const size_t Np = (size_t)sched_npad(R, gamma);
+  return sizeof(uint32_t) * 4 * Np + sizeof(int) * ((size_t)kHistCells + (size_t)R);
 }
 
 cudaError_t launch_schedule(SchedParams p, cudaStream_t stream) {
-  const int N = p.R * p.gamma;
-  int npow2 = 2;
-  while (npow2 < N) npow2 <<= 1;
-  p.npow2 = npow2;
+  p.npad = sched_npad(p.R, p.gamma);
+  p.unit_grid = p.b_step == 1.0 && p.b_lo == floor(p.b_lo) && fabs(p.b_lo) < 1e9;
+  p.b_lo_int = p.unit_grid ? (long)p.b_lo : 0;
   const size_t smem = schedule_smem_bytes(p.R, p.gamma);
   cudaError_t err =
       cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -8,8 +8,10 @@ namespace spec {
 constexpr int kSchedMaxCandidates = 8192;  // R * gamma, one thread block
 
 struct SchedParams {
-  int R, gamma, n_sps, K, mode, npow2;
+  int R, gamma, n_sps, K, mode, npad;
   double b_lo, b_step;
+  bool unit_grid;  // b_step == 1 and b_lo integral: SPS(B) is a table entry
+  long b_lo_int;
   const float* a;
   const float* sps;
   int32_t* ell;
