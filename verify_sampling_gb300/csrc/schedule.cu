@@ -34,6 +34,20 @@ __device__ __forceinline__ double sps_at(const float* sps, int n_sps, double b_l
   return __dadd_rn(__dmul_rn(__dsub_rn(1.0, f), (double)sps[i]), __dmul_rn(f, (double)sps[i + 1]));
 }
 
+// Lanes of the warp whose digit d (8 bits) equals this lane's, among the
+// lanes with `valid` set: one ballot per bit.
+__device__ __forceinline__ unsigned digit_peers(uint32_t d, bool valid) {
+  unsigned peers = __ballot_sync(0xffffffffu, valid);
+  if (!valid) peers = ~peers;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const bool bit = (d >> b) & 1u;
+    const unsigned bal = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? bal : ~bal;
+  }
+  return peers;
+}
+
 __device__ __forceinline__ int warp_incl_scan_int(int v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -81,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
 
   // 2. stable LSD radix sort, 8-bit digits, 4 passes.  Warp w owns a
   // contiguous segment of the array; ranks inside a warp step come from
-  // __match_any_sync, offsets from a scan of the per-warp digit histograms in
+  // per-bit ballots, offsets from a scan of the per-warp digit histograms in
   // (digit, warp) order, which keeps equal digits in array order.
   {
     const int seg = (((N + 31) / 32) + 31) & ~31;  // per-warp segment, multiple of 32
@@ -95,8 +109,8 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
       for (int s0 = 0; s0 < seg; s0 += 32) {
         const int idx = wb + s0 + lane;
         const bool valid = idx < N;
-        const uint32_t d = valid ? (ks[idx] >> shift) & 255u : 256u;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const uint32_t d = valid ? (ks[idx] >> shift) & 255u : 0u;
+        const unsigned peers = digit_peers(d, valid);
         if (valid && lane == __ffs(peers) - 1) hist[warp * 257 + d] += __popc(peers);
       }
       __syncthreads();
@@ -129,14 +143,14 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
       for (int s0 = 0; s0 < seg; s0 += 32) {
         const int idx = wb + s0 + lane;
         const bool valid = idx < N;
-        uint32_t key = 0u, d = 256u;
+        uint32_t key = 0u, d = 0u;
         int val = 0;
         if (valid) {
           key = ks[idx];
           val = vs[idx];
           d = (key >> shift) & 255u;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const unsigned peers = digit_peers(d, valid);
         const int base = valid ? hist[warp * 257 + d] : 0;
         __syncwarp();
         if (valid) {
@@ -187,24 +201,22 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
   const int per = (N + kThreads - 1) / kThreads;
   const int lo = tid * per, hi = min(N, lo + per);
   const int cnt = hi - lo;
-  int e1;  // a_1 < 2^e1
-  frexpf(__uint_as_float(~keyA[0]), &e1);
-  const int shift = 49 - e1;
-  auto fixed = [&](float a) -> unsigned long long {
-    // a = m * 2^(ex - 24) with m the 24-bit significand; a * 2^shift, truncated
-    if (!(a > 0.f)) return 0ull;
-    int ex;
-    const float fr = frexpf(a, &ex);  // a = fr * 2^ex, fr in [0.5, 1)
-    const unsigned long long m = (unsigned long long)(fr * 16777216.0f);  // exact: fr * 2^24
-    const int sh = ex - 24 + shift;
-    if (sh >= 0) return m << sh;  // sh <= 25 since a <= a_1
+  // From the bits: a = m * 2^(E' - 150) with E' = max(E, 1) and m the
+  // significand (hidden bit for E > 0); a_1 < 2^(E1' - 126).  So
+  // a * 2^shift = m * 2^(E' - E1' + 25) for shift = 175 - E1'.
+  const int e1 = max((int)((~keyA[0] >> 23) & 0xffu), 1);
+  auto fixed = [&](uint32_t bits) -> unsigned long long {
+    const int E = (int)((bits >> 23) & 0xffu);
+    const unsigned long long m = (bits & 0x7fffffu) | (E > 0 ? 0x800000u : 0u);
+    const int sh = max(E, 1) - e1 + 25;  // <= 25 since a <= a_1
+    if (sh >= 0) return m << sh;
     return sh > -64 ? (m >> (-sh)) : 0ull;
   };
   unsigned long long qv[kSchedMaxCandidates / kThreads];
   unsigned long long local = 0ull;
 #pragma unroll
   for (int i = 0; i < kSchedMaxCandidates / kThreads; ++i) {
-    qv[i] = (i < cnt) ? fixed(__uint_as_float(~keyA[lo + i])) : 0ull;
+    qv[i] = (i < cnt) ? fixed(~keyA[lo + i]) : 0ull;
     local += qv[i];
   }
   unsigned long long incl = local;  // inclusive warp scan
@@ -227,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
     warp_q[lane] = wi - wt;  // exclusive prefix of warp totals
   }
   __syncthreads();
-  const double unit = ldexp(1.0, -shift);  // exact power of two
+  const double unit = ldexp(1.0, e1 - 175);  // 2^-shift, exact
   {
     unsigned long long run = warp_q[warp] + incl - local;
 #pragma unroll
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
     }
   } else if (nstar - 1 >= lo && nstar - 1 < hi) {
     unsigned long long run = seg_q[tid];
-    for (int i = lo; i < nstar; ++i) run += fixed(__uint_as_float(~keyA[i]));
+    for (int i = lo; i < nstar; ++i) run += fixed(~keyA[i]);
     p.stats[0] = (double)nstar;
     p.stats[1] = (double)(p.R + nstar);
     p.stats[2] = __dmul_rn((double)run, unit);
