@@ -85,9 +85,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr uint32_t kCBytes = KC * kNT * 128;
-  constexpr uint32_t kUBytes = RowTile<TL>::kBytes;
-  constexpr uint32_t kTBytes = RowTile<TT>::kBytes;
-  constexpr uint32_t kStageBytes = round1024(kCBytes + kUBytes + kTBytes);
   unsigned char* sA = smem;
   unsigned char* sStage = smem + KC * 16384;
 
@@ -138,8 +135,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_begin = (int)((long)split * p.ntiles / nsplit);
   const int t_end = (int)((long)(split + 1) * p.ntiles / nsplit);
   const int T = t_end - t_begin;
-  const int S = p.stages;
   const int G1 = G + 1;
+  // Stages sized for this tile's gathered rows (often far fewer than 128):
+  // C tile, then the U rows, then the target rows, each row padded.
+  const uint32_t u_bytes = (uint32_t)nrows * RowTile<TL>::kPitch;
+  const uint32_t stage_bytes = round1024(kCBytes + u_bytes + (uint32_t)nrows * RowTile<TT>::kPitch);
+  const uint32_t fit = ((uint32_t)p.smem_bytes - 1024u - KC * 16384u) / stage_bytes;
+  const int S = (int)(fit < (uint32_t)kMaxStages ? fit : (uint32_t)kMaxStages);
 
   for (int i = threadIdx.x; i < 128; i += blockDim.x) {
     int r = -1, trow = 0;
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) fail();
         break;
       }
-      unsigned char* st = sStage + r.idx * kStageBytes;
+      unsigned char* st = sStage + r.idx * stage_bytes;
       const int n0 = (t_begin + t) * kNT;
       // columns of this tile inside the vocabulary (a multiple of 16 bytes in
       // both dtypes, because V times the element size is)
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = lane; i < nrows; i += 32) {
         const size_t urow = (size_t)s_req[i] * p.gamma + (k - 1);
         tc::bulk_load(st + kCBytes + i * RowTile<TL>::kPitch, U + urow * p.V + n0, ub, &full_r[r.idx]);
-        tc::bulk_load(st + kCBytes + kUBytes + i * RowTile<TT>::kPitch,
+        tc::bulk_load(st + kCBytes + u_bytes + i * RowTile<TT>::kPitch,
                       tgt + (size_t)s_trow[i] * p.V + n0, tb, &full_r[r.idx]);
       }
       issued = t + 1;
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t b_base = tc::smem_u32(sStage + r.idx * kStageBytes);
+        const uint32_t b_base = tc::smem_u32(sStage + r.idx * stage_bytes);
 #pragma unroll
         for (int kk = 0; kk < KC * 4; ++kk) {
           const int kc = kk >> 2, ko = (kk & 3) * 32;
@@ -252,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3, grp = warp >> 2;
     const int row = quad * 32 + lane;
     const bool valid = row < nrows;
+    // the stages hold exactly nrows rows: lanes past them read row 0 (unused)
+    const int lrow = valid ? row : 0;
     const int V = p.V, rank = p.rank;
     const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
     for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
@@ -306,12 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t braw[16];
         float u[16];
         tc::tmem_ld16(t_lane + (uint32_t)(rb.idx * kNT), braw);
-        load_row16(sStage + r.idx * kStageBytes + kCBytes, row, grp, u, TL());
+        load_row16(sStage + r.idx * stage_bytes + kCBytes, lrow, grp, u, TL());
         tc::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 16; ++c) qv[c] = tc::ex2(fmaf(u[c] + __uint_as_float(braw[c]), kq, nq));
       }
-      load_row16(sStage + r.idx * kStageBytes + kCBytes + kUBytes, row, grp, L, TT());
+      load_row16(sStage + r.idx * stage_bytes + kCBytes + u_bytes, lrow, grp, L, TT());
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -408,6 +412,8 @@ size_t smem_bytes(int stages) {
   return 1024 + (size_t)KC * 16384 +
          (size_t)stages * round1024(KC * kNT * 128 + RowTile<TL>::kBytes + RowTile<TT>::kBytes);
 }
+// The kernel splits whatever shared memory it gets into stages sized for its
+// rows; at least two stages of a full 128-row tile must fit.
 
 template <typename TT, typename TL, int KC>
 cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void* U, const void* Ct,
@@ -418,10 +424,10 @@ cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void*
   const uint32_t cbox[3] = {64, (uint32_t)kNT, 1};
   if (!encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ct, 3, cdims, cbox))
     return cudaErrorInvalidValue;
-  int s = kMaxStages;
-  while (s > 2 && smem_bytes<TT, TL, KC>(s) > kSmemBudget) --s;
-  p.stages = s;
-  const size_t smem = smem_bytes<TT, TL, KC>(s);
+  // all of the per-CTA shared memory but 4 KB left for the static arrays
+  const size_t smem = 227 * 1024 - 4096;
+  if (smem_bytes<TT, TL, KC>(2) > smem) return cudaErrorInvalidValue;
+  p.smem_bytes = (int)smem;
   auto kern = resid_tc_kernel<TT, TL, KC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;

@@ -6,7 +6,7 @@
 namespace spec {
 
 struct ResidTCParams {
-  int R, gamma, V, rank, stages, ntiles, max_mtiles;
+  int R, gamma, V, rank, smem_bytes, ntiles, max_mtiles;
   uint32_t rid_base;
   PhiloxKey key;
   float inv_target_temp;

@@ -95,6 +95,7 @@ __device__ void resolve_request(const VerifyParams& p, int r, int l) {
 // finishes the row; the one that finishes a request's last row resolves it.
 
 constexpr int kBatch = 32 * 32;  // entries per warp batch
+constexpr int kRingStages = 3;   // bulk-copy batches in flight per warp
 
 // Eight consecutive entries from v0 (a multiple of 8) as floats; entries at or
 // past V read as -inf.  `vec`: whole 16-byte pieces inside the row may be
@@ -127,6 +128,39 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* L, long v0, long V, b
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = (v0 + i < V) ? __bfloat162float(L[v0 + i]) : -CUDART_INF_F;
+  }
+}
+
+// The same from a shared-memory batch: entry `off` (a multiple of 8) of a
+// stage holding n valid entries; entries past n read as -inf.
+template <typename TT>
+__device__ __forceinline__ void load8s_t(const unsigned char* sx, int off, int n, float (&x)[8]);
+template <>
+__device__ __forceinline__ void load8s_t<float>(const unsigned char* sx, int off, int n, float (&x)[8]) {
+  const float* f = reinterpret_cast<const float*>(sx) + off;
+  if (off + 8 <= n) {
+    const float4 a = *reinterpret_cast<const float4*>(f), b = *reinterpret_cast<const float4*>(f + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = (off + i < n) ? f[i] : -CUDART_INF_F;
+  }
+}
+template <>
+__device__ __forceinline__ void load8s_t<__nv_bfloat16>(const unsigned char* sx, int off, int n, float (&x)[8]) {
+  const uint16_t* h = reinterpret_cast<const uint16_t*>(sx) + off;
+  if (off + 8 <= n) {
+    const uint4 q = *reinterpret_cast<const uint4*>(h);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = (off + i < n) ? __uint_as_float((uint32_t)h[i] << 16) : -CUDART_INF_F;
   }
 }
 
@@ -225,117 +259,210 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyParams 
   if (tid == 0) *p.ws.n_rows = carry;
 }
 
-template <typename TT>
+template <typename TT, bool kGreedy>
 __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyParams p) {
-  const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(128) unsigned char ring_smem[];
+  __shared__ __align__(8) uint64_t ring_bar[kVerifyThreads / 32][kRingStages];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long V = p.V;
   const int G1 = p.gamma + 1, cpr = p.nsplit;
   const float ks = fused::kLog2e * p.inv_target_temp;  // log2 units per logit
-  const bool greedy = p.mode == SPEC_VERIFY_GREEDY;
+  constexpr bool greedy = kGreedy;
   const bool vec = ((size_t)V * sizeof(TT)) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.tgt) & 15) == 0;
 
+  // Aligned rows are read through a ring of kRingStages bulk copies per warp
+  // (lane 0 keeps up to kRingStages batches in flight, across unit borders);
+  // otherwise straight from global memory.
+  constexpr uint32_t kStageB = kBatch * sizeof(TT);
+  const bool bulk = vec && p.row_ring;
+  unsigned char* ring = ring_smem + (size_t)warp * kRingStages * kStageB;
+  if (bulk && lane == 0) {
+    for (int i = 0; i < kRingStages; ++i) tc::mbar_init(&ring_bar[warp][i], 1);
+    tc::fence_barrier_init();
+  }
+  __syncwarp();
+
   const unsigned long long units = (unsigned long long)(*p.ws.n_rows) * cpr;
-  // one unit per claim; the next claim is issued before the current unit runs
-  unsigned long long next = 0;
-  if (lane == 0) next = atomicAdd(p.ws.unit_cnt, 1ull);
-  for (;;) {
-    const unsigned long long unit = __shfl_sync(0xffffffffu, next, 0);
-    if (unit >= units) break;
-    if (lane == 0) next = atomicAdd(p.ws.unit_cnt, 1ull);
+  // A work unit: chunk c of row (r, j); row pointer L, entries [c0, c1).
+  struct Unit {
+    int ok, c, r, j, l, c0, c1;
+    const TT* L;
+  };
+  // per warp: the current unit, the one after it, and lane 0's issue state
+  __shared__ Unit s_cur[kVerifyThreads / 32], s_next[kVerifyThreads / 32];
+  __shared__ uint32_t s_iss[kVerifyThreads / 32];
+  __shared__ int s_iss_cur[kVerifyThreads / 32], s_ib0[kVerifyThreads / 32];
+  auto describe = [&](unsigned long long u) {
+    Unit d{};
+    d.ok = u < units;
+    if (d.ok) {
+      d.c = (int)(u % (unsigned long long)cpr);
+      const int code = p.ws.row_list[u / (unsigned long long)cpr];
+      d.r = code / G1;
+      d.j = code % G1 + 1;
+      d.l = clamp_ell(p, d.r);
+      d.L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, d.r, d.j) * (size_t)V;
+      d.c0 = d.c * kRowChunk;
+      d.c1 = (long)d.c0 + kRowChunk < V ? d.c0 + kRowChunk : (int)V;
+    }
+    return d;
+  };
+  auto claim_next = [&]() {  // lane 0 claims and describes the next unit
+    if (lane == 0) s_next[warp] = describe(atomicAdd(p.ws.unit_cnt, 1ull));
+    __syncwarp();
+  };
+  if (lane == 0) {
+    s_cur[warp] = describe(atomicAdd(p.ws.unit_cnt, 1ull));
+    s_iss[warp] = 0u;
+    s_iss_cur[warp] = 1;
+    s_ib0[warp] = s_cur[warp].c0;
+  }
+  __syncwarp();
+  claim_next();
+  uint32_t con = 0;  // ring batches consumed
+  // lane 0: keep up to kRingStages batches in flight, from the current unit,
+  // then from the next one
+  auto issue_some = [&]() {
+    uint32_t iss = s_iss[warp];
+    int iss_cur = s_iss_cur[warp], ib0 = s_ib0[warp];
+    while (iss - con < (uint32_t)kRingStages) {
+      const Unit& d = iss_cur ? s_cur[warp] : s_next[warp];
+      if (!d.ok) break;
+      if (ib0 >= d.c1) {
+        if (!iss_cur) break;
+        iss_cur = 0;
+        ib0 = s_next[warp].c0;
+        continue;
+      }
+      const int slot = (int)(iss % kRingStages);
+      const int n = d.c1 - ib0 < kBatch ? d.c1 - ib0 : kBatch;
+      const uint32_t bytes = (uint32_t)n * (uint32_t)sizeof(TT);
+      tc::fence_proxy_async();  // the stage's earlier reads come before the async write
+      tc::mbar_expect_tx(&ring_bar[warp][slot], bytes);
+      tc::bulk_load(ring + (size_t)slot * kStageB, d.L + ib0, bytes, &ring_bar[warp][slot]);
+      ib0 += kBatch;
+      ++iss;
+    }
+    s_iss[warp] = iss;
+    s_iss_cur[warp] = iss_cur;
+    s_ib0[warp] = ib0;
+  };
+  if (bulk && lane == 0) issue_some();
+  bool failed = false;
+  while (s_cur[warp].ok) {
     {
-      const int c = (int)(unit % (unsigned long long)cpr);
-      const int code = p.ws.row_list[unit / (unsigned long long)cpr];
-      const int r = code / G1, j = code % G1 + 1;
-      const int l = clamp_ell(p, r);
+      const int c = s_cur[warp].c, r = s_cur[warp].r, j = s_cur[warp].j, l = s_cur[warp].l;
       const uint32_t rid = p.rid_base + (uint32_t)r;
       const bool bonus = !greedy && j == l + 1;
-      const TT* L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, r, j) * (size_t)V;
-      const long c0 = (long)c * kRowChunk, c1 = c0 + kRowChunk < V ? c0 + kRowChunk : V;
+      const TT* L = s_cur[warp].L;
+      const int c0 = s_cur[warp].c0, c1 = s_cur[warp].c1;
 
       Race st = race_empty();  // log2 units; be, bE, idx: bonus race
       ArgMax am = argmax_empty();
       float c_own = CUDART_INF_F;  // bonus: filter factor bE / be (with slack)
       PhiloxRow prow{};
       if (bonus) prow = philox_row((uint32_t)j, rid, kPurposeBonus, p.rk);
-      for (long b0 = c0; b0 < c1; b0 += kBatch) {
-        float x[4][8];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) load8(L, b0 + g * 256 + lane * 8, c1, vec, x[g]);
+      // one batch of 32 entries per lane: x from the ring stage (bulk) or from
+      // global memory; `fetch` may be called again by the overflow path
+      auto batch = [&](int b0, const unsigned char* sx) {
+        // eight consecutive entries of group g (from the stage, or global memory)
+        auto get = [&](int g, float (&x)[8]) {
+          const int off = g * 256 + lane * 8;
+          if (sx) load8s_t<TT>(sx, off, c1 - b0, x);
+          else load8(L, (long)b0 + off, c1, vec, x);
+        };
         if (greedy) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
+          for (int g = 0; g < 4; ++g) {
+            float x[8];
+            get(g, x);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const int v = (int)(b0 + g * 256 + lane * 8 + q);
-              if (v < c1 && (am.idx < 0 || x[g][q] > am.val)) {
-                am.val = x[g][q];
+              const int v = b0 + g * 256 + lane * 8 + q;
+              if (v < c1 && (am.idx < 0 || x[q] > am.val)) {
+                am.val = x[q];
                 am.idx = v;
               }
             }
-          continue;
+          }
+          return;
         }
-        // reference: the first batch's maximum (per lane); a later batch moves
-        // it only when its sum overflows
-        bool seed = false;
-        int im = 0;
-        float mx = -CUDART_INF_F;
+        // First finite entries of this lane: fix the reference at this batch's
+        // maximum (log2 units) and, in the bonus row, seed the race with it.
         if (!(st.m > -CUDART_INF_F)) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
+          float mx = -CUDART_INF_F;
+          int im = 0;
+#pragma unroll 1
+          for (int g = 0; g < 4; ++g) {
+            float x[8];
+            get(g, x);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              if (x[g][q] > mx) {
-                mx = x[g][q];
+              if (x[q] > mx) {
+                mx = x[q];
                 im = g * 8 + q;
               }
+          }
           if (mx > -CUDART_INF_F) {
             st.m = mx * ks;
-            seed = bonus;
+            if (bonus) {  // its e is computed exactly as in the pass below
+              const int vm = b0 + (im >> 3) * 256 + lane * 8 + (im & 7);
+              const uint4 bm = philox_in_row((uint32_t)(vm >> 2), prow, p.rk);
+              st.be = tc::ex2(fmaf(mx, ks, -st.m));
+              st.bE = -logf(uniform_from_word(word_of(bm, vm & 3)));
+              st.idx = vm;
+              c_own = (st.bE / st.be) * fused::kFilterUp;
+            }
           }
         }
         // Lanes without a finite entry yet (e.g. past V in a tail chunk) take
-        // part in the warp-wide steps below but contribute nothing; the batch
-        // is skipped only when the whole warp has nothing.
+        // part in the warp-wide steps but contribute nothing; the batch is
+        // skipped only when the whole warp has nothing.
         const bool have = st.m > -CUDART_INF_F;
-        if (!__any_sync(0xffffffffu, have)) continue;
-        float2 e2[4][4];  // the loaded values die here (an overflow reloads them)
-        if (have) {
-          float ts = 0.f;
+        if (!__any_sync(0xffffffffu, have)) return;
+        // bonus: the warp's best lowered score bounds every lane's filter
+        float gbest = -CUDART_INF_F;
+        if (bonus) {
+          gbest = (st.idx >= 0) ? st.m + fused::lg2(st.be) - fused::lg2(st.bE) - fused::kPublishMargin
+                                : -CUDART_INF_F;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) gbest = fmaxf(gbest, __shfl_xor_sync(0xffffffffu, gbest, off));
+        }
+        if (!have) return;
+        float cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          float x[8];
+          get(g, x);
+          float2 e[4];
+          float ts;
           {
             const float2 ks2 = make_float2(ks, ks), nref2 = make_float2(-st.m, -st.m);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float2 a = __ffma2_rn(make_float2(x[g][2 * q], x[g][2 * q + 1]), ks2, nref2);
-                e2[g][q] = make_float2(tc::ex2(a.x), tc::ex2(a.y));
-              }
-              const float2 t = __fadd2_rn(__fadd2_rn(e2[g][0], e2[g][1]), __fadd2_rn(e2[g][2], e2[g][3]));
-              ts += t.x + t.y;
+            for (int q = 0; q < 4; ++q) {
+              const float2 a = __ffma2_rn(make_float2(x[2 * q], x[2 * q + 1]), ks2, nref2);
+              e[q] = make_float2(tc::ex2(a.x), tc::ex2(a.y));
             }
+            const float2 t = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
+            ts = t.x + t.y;
           }
           if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
+            float mz = x[0];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) load8(L, b0 + g * 256 + lane * 8, c1, vec, x[g]);
-            float mz = -CUDART_INF_F;
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-              for (int q = 0; q < 8; ++q) mz = fmaxf(mz, x[g][q]);
+            for (int q = 1; q < 8; ++q) mz = fmaxf(mz, x[q]);
             const float mnew = fmaxf(mz * ks, st.m);
             const float sc = tc::ex2(st.m - mnew);
             st.s *= sc;
             st.be *= sc;
             st.m = mnew;
             if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
+            cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
             ts = 0.f;
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                e2[g][q] = make_float2(tc::ex2(fmaf(x[g][2 * q], ks, -st.m)), tc::ex2(fmaf(x[g][2 * q + 1], ks, -st.m)));
-                ts += e2[g][q].x + e2[g][q].y;
-              }
+            for (int q = 0; q < 4; ++q) {
+              e[q] = make_float2(tc::ex2(fmaf(x[2 * q], ks, -st.m)), tc::ex2(fmaf(x[2 * q + 1], ks, -st.m)));
+              ts += e[q].x + e[q].y;
+            }
           }
           st.s += ts;
           if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
@@ -343,77 +470,69 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
             st.be *= 0x1p-64f;
             st.m += 64.f;
             if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                e2[g][q].x *= 0x1p-64f;
-                e2[g][q].y *= 0x1p-64f;
-              }
-          }
-          if (seed) {  // this lane's first finite batch: seed its race with the maximum
-            const int vm = (int)(b0 + (im >> 3) * 256 + lane * 8 + (im & 7));
-            const uint4 bm = philox_in_row((uint32_t)(vm >> 2), prow, p.rk);
-            float em = 0.f;  // e of entry im (unrolled select: no local-memory indexing)
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-              for (int q = 0; q < 8; ++q) em = (im == g * 8 + q) ? ((q & 1) ? e2[g][q >> 1].y : e2[g][q >> 1].x) : em;
-            st.be = em;
-            st.bE = -logf(uniform_from_word(word_of(bm, vm & 3)));
-            st.idx = vm;
-            c_own = (st.bE / st.be) * fused::kFilterUp;
-          }
-        }
-        if (!bonus) continue;  // uniform
-        // ---- bonus race over this batch ----
-        // the warp's best lowered score (lanes without a best give -inf); all lanes
-        float gbest = (st.idx >= 0) ? st.m + fused::lg2(st.be) - fused::lg2(st.bE) - fused::kPublishMargin
-                                    : -CUDART_INF_F;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) gbest = fmaxf(gbest, __shfl_xor_sync(0xffffffffu, gbest, off));
-        if (have) {
-          const float cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
-          const float2 cf2 = make_float2(cf, cf), one2 = make_float2(1.f, 1.f);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const long v0 = b0 + g * 256 + lane * 8;
-            uint32_t words[8];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const uint4 bb = philox_in_row((uint32_t)(v0 >> 2) + q, prow, p.rk);
-              words[4 * q] = bb.x;
-              words[4 * q + 1] = bb.y;
-              words[4 * q + 2] = bb.z;
-              words[4 * q + 3] = bb.w;
-            }
-            uint32_t all_neg = 0xffffffffu;
-            float2 d[4];
+            cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              d[q] = __fadd2_rn(__ffma2_rn(e2[g][q], cf2, one2),
-                                make_float2(neg_one_plus_w(words[2 * q]), neg_one_plus_w(words[2 * q + 1])));
-              all_neg &= __float_as_uint(d[q].x) & __float_as_uint(d[q].y);
+              e[q].x *= 0x1p-64f;
+              e[q].y *= 0x1p-64f;
             }
-            if (!(all_neg >> 31)) {  // rare: exact race test in index order
+          }
+          if (!bonus) continue;
+          // ---- bonus race over this group ----
+          const int v0 = b0 + g * 256 + lane * 8;
+          uint32_t words[8];
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float dq = (q & 1) ? d[q >> 1].y : d[q >> 1].x;
-                const float eq = (q & 1) ? e2[g][q >> 1].y : e2[g][q >> 1].x;
-                if (!(__float_as_uint(dq) >> 31) && eq > 0.f && v0 + q < c1) {
-                  const float E = -logf(uniform_from_word(words[q]));
-                  if (race_beats(eq, E, (int)(v0 + q), st.be, st.bE, st.idx)) {
-                    st.be = eq;
-                    st.bE = E;
-                    st.idx = (int)(v0 + q);
-                    c_own = (st.bE / st.be) * fused::kFilterUp;
-                  }
+          for (int q = 0; q < 2; ++q) {
+            const uint4 bb = philox_in_row((uint32_t)(v0 >> 2) + q, prow, p.rk);
+            words[4 * q] = bb.x;
+            words[4 * q + 1] = bb.y;
+            words[4 * q + 2] = bb.z;
+            words[4 * q + 3] = bb.w;
+          }
+          const float2 cf2 = make_float2(cf, cf), one2 = make_float2(1.f, 1.f);
+          uint32_t all_neg = 0xffffffffu;
+          float2 d[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            d[q] = __fadd2_rn(__ffma2_rn(e[q], cf2, one2),
+                              make_float2(neg_one_plus_w(words[2 * q]), neg_one_plus_w(words[2 * q + 1])));
+            all_neg &= __float_as_uint(d[q].x) & __float_as_uint(d[q].y);
+          }
+          if (!(all_neg >> 31)) {  // rare: exact race test in index order
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float dq = (q & 1) ? d[q >> 1].y : d[q >> 1].x;
+              const float eq = (q & 1) ? e[q >> 1].y : e[q >> 1].x;
+              if (!(__float_as_uint(dq) >> 31) && eq > 0.f && v0 + q < c1) {
+                const float E = -logf(uniform_from_word(words[q]));
+                if (race_beats(eq, E, v0 + q, st.be, st.bE, st.idx)) {
+                  st.be = eq;
+                  st.bE = E;
+                  st.idx = v0 + q;
+                  c_own = (st.bE / st.be) * fused::kFilterUp;
+                  cf = fminf(cf, c_own);
                 }
               }
             }
           }
         }
+      };
+      for (int b0 = c0; b0 < c1; b0 += kBatch) {
+        if (!bulk) {
+          batch(b0, nullptr);
+          continue;
+        }
+        const int slot = (int)(con % kRingStages);
+        if (!tc::mbar_wait(&ring_bar[warp][slot], (uint32_t)(con / kRingStages) & 1u, fused::kWaitNs)) {
+          failed = true;
+          break;
+        }
+        batch(b0, ring + (size_t)slot * kStageB);
+        __syncwarp();  // every lane is done with the stage
+        ++con;
+        if (lane == 0) issue_some();
       }
+      if (__any_sync(0xffffffffu, failed)) break;
       // warp merge of the unit, partial, and the row / request completion
       Partial w{};
       if (greedy) {
@@ -439,7 +558,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
         last = atomicAdd(p.ws.row_cnt + rj, 1u) == (unsigned)(cpr - 1);
         if (last) __threadfence();
       }
-      if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+      if (__shfl_sync(0xffffffffu, last, 0)) {
       if (lane == 0) p.ws.row_cnt[rj] = 0u;
       if (greedy) {
         ArgMax acc = argmax_empty();
@@ -469,7 +588,24 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
           resolve_request(p, r, l);
         }
       }
+      }
     }
+    // next unit; lane 0 moves its issue position into it
+    __syncwarp();
+    if (lane == 0) {
+      s_cur[warp] = s_next[warp];
+      if (s_iss_cur[warp]) s_ib0[warp] = s_cur[warp].c0;  // the finished unit was issued in full
+      s_iss_cur[warp] = 1;
+    }
+    __syncwarp();
+    claim_next();
+    if (bulk && lane == 0) issue_some();
+  }
+  if (failed && bulk && lane == 0) {
+    // a ring wait gave up: let the copies still in flight land before exiting
+    set_status(p.status, SPEC_STATUS_TIMEOUT);
+    for (uint32_t n = con; n != s_iss[warp]; ++n)
+      tc::mbar_wait(&ring_bar[warp][n % kRingStages], (uint32_t)(n / kRingStages) & 1u, fused::kWaitNs);
   }
 }
 
@@ -623,7 +759,13 @@ static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_
                                 cudaStream_t stream) {
   verify_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   const unsigned g1 = (unsigned)(2 * std::max(1, p.device_sms));
-  verify_rows_kernel<TT><<<g1, kVerifyThreads, 0, stream>>>(p);
+  // per-warp rings of bulk-copied batches
+  const size_t ring = (size_t)(kVerifyThreads / 32) * kRingStages * kBatch * sizeof(TT);
+  VerifyParams pr = p;
+  auto kern = p.mode == SPEC_VERIFY_GREEDY ? verify_rows_kernel<TT, true> : verify_rows_kernel<TT, false>;
+  pr.row_ring = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring) == cudaSuccess;
+  if (!pr.row_ring) (void)cudaGetLastError();
+  kern<<<g1, kVerifyThreads, pr.row_ring ? ring : 0, stream>>>(pr);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || p.mode == SPEC_VERIFY_GREEDY) return err;
   const dim3 g2((unsigned)residual_nsplit(p.R, p.V), (unsigned)p.R);

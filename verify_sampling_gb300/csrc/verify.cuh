@@ -58,6 +58,7 @@ struct VerifyParams {
   float* lse_t;
   uint32_t* status;
   bool tc_residual;      // residual on the fused tensor-core kernel
+  bool row_ring;         // row pass: per-warp bulk-copy rings in dynamic shared memory
   int device_sms;
   VerifyScratch ws;
 };
