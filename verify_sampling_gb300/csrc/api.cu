@@ -24,9 +24,9 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // Partials: the larger of the generic kernel's [R, nsplit] and the fused
 // kernel's [R, splits <= kMaxDeviceSms]; counters: one per request (generic)
 // or per 128-request tile (fused).
-size_t draft_scratch_bytes(int R, int V) {
+size_t draft_scratch_bytes(int R, int gamma, int V) {
   const size_t ns = (size_t)std::max(draft_nsplit(R, V), kMaxDeviceSms);
-  return align256((size_t)R * ns * sizeof(Partial)) + align256((size_t)R * sizeof(unsigned));
+  return align256((size_t)R * ns * sizeof(Partial)) + align256((size_t)R * (1 + gamma) * sizeof(unsigned));
 }
 
 // The fused tensor-core path needs bf16 factors with r a multiple of 64, 16-byte
@@ -104,7 +104,7 @@ const char* spec_error_string(int code) {
 size_t spec_workspace_bytes(int stage, int R, int gamma, int V, int r) {
   switch (stage) {
     case SPEC_STAGE_DRAFT:
-      return draft_sizes_ok(R, gamma, V, r) ? draft_scratch_bytes(R, V) : 0;
+      return draft_sizes_ok(R, gamma, V, r) ? draft_scratch_bytes(R, gamma, V) : 0;
     case SPEC_STAGE_SCHEDULE:
       return 0;
     case SPEC_STAGE_VERIFY:
@@ -118,7 +118,7 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
   int rc = check_draft_args(args);
   if (rc != SPEC_OK) return rc;
   const spec_draft_args& a = *args;
-  const size_t need = draft_scratch_bytes(a.R, a.V);
+  const size_t need = draft_scratch_bytes(a.R, a.gamma, a.V);
   rc = check_workspace(a.workspace, a.workspace_bytes, need);
   if (rc != SPEC_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -148,7 +148,7 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
   p.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
   p.status = a.status;
   // counters [R] and the fused kernel's shared race bounds [gamma, R], zeroed together
-  if (cudaMemsetAsync(p.counters, 0, (size_t)a.R * sizeof(unsigned), s) != cudaSuccess)
+  if (cudaMemsetAsync(p.counters, 0, (size_t)a.R * (1 + a.gamma) * sizeof(unsigned), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
   int sms = 0;
   if (draft_tc_ok(a, &sms)) {
@@ -170,6 +170,7 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
     t.lse_q = a.lse_q;
     t.partials = p.partials;
     t.counters = p.counters;
+    t.row_best = p.counters + a.R;
     t.status = a.status;
     if (launch_draft_tc(t, a.logit_dtype, a.U, a.Ct, s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (a.P_out && launch_draft_steps(p, a.logit_dtype, a.fac_dtype, true, s, /*probs_only=*/true) !=

@@ -78,12 +78,13 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
                   al(a.U, 16) && al(a.A, 16) && al(a.Ct, 16) && major == 10 && sms >= 1 &&
                   sms <= kMaxDeviceSms;
 
-  // Exact scratch for the path taken: partials [R, splits], then counters [R].
+  // Exact scratch for the path taken: partials [R, splits], then counters [R]
+  // and the race bounds [gamma, R].
   const int nsplit_generic = draft_nsplit(a.R, a.V);
   const int nsplit_tc = tc ? draft_tc_nsplit(a.R, a.V, sms) : 0;
   const size_t part_bytes =
       round256((size_t)a.R * (tc ? nsplit_tc : nsplit_generic) * sizeof(Partial));
-  const size_t cnt_bytes = (size_t)a.R * sizeof(unsigned);
+  const size_t cnt_bytes = (size_t)a.R * (1 + a.gamma) * sizeof(unsigned);
   if (part_bytes + cnt_bytes > kStaticScratchBytes) return SPEC_ERR_UNSUPPORTED;
   char* ws = static_cast<char*>(scratch_address(dev));
   if (!ws) return SPEC_ERR_CUDA;
@@ -129,6 +130,7 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
     t.lse_q = a.lse_q;
     t.partials = p.partials;
     t.counters = p.counters;
+    t.row_best = p.counters + a.R;
     t.status = a.status;
     if (launch_draft_tc(t, a.logit_dtype, a.U, a.Ct, s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (a.P_out && launch_draft_steps(p, a.logit_dtype, a.fac_dtype, true, s, true) != cudaSuccess)

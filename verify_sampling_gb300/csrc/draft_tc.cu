@@ -25,8 +25,10 @@
 // (e, E); the logarithm E is computed only for candidates, selected by an exact
 // filter: since E >= 1 - u, an element can reach a score g only if
 // 1 - u <= e * 2^(ref - g).  The bound g is the larger of the thread's own best
-// and the best score any thread of the same row in the CTA has published so
-// far (a shared-memory word per row, raised with atomicMax).  Published scores
+// and the best score any thread of the same row has published so far: a
+// shared-memory word per row, raised with atomicMax, into which one thread per
+// row copies the row's global word (raised by new CTA-level bests) every
+// tile.  Published scores
 // are real scores lowered by a margin, so the row's winner always passes; the
 // filter only decides which elements need the exact comparison.  The race
 // starts from the first tile's largest element, so the first tile does not
@@ -43,9 +45,11 @@ namespace {
 using namespace fused;
 
 // Cold path: exact race test of one filtered element; on a new best, publish
-// the row's score to the CTA and return true.
+// the row's score to the CTA (and, when it raises the CTA's bound, to the
+// row's word in global memory) and return true.
 __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word, int v,
-                                               uint32_t* row_best, uint32_t shared_seen) {
+                                               uint32_t* row_best, uint32_t shared_seen,
+                                               unsigned* global_best) {
   if (!(e > 0.f)) return false;  // an underflowed (or NaN) weight never wins
   const float E = -logf(uniform_from_word(word));
   if (!race_beats(e, E, v, st.be, st.bE, st.idx)) return false;
@@ -56,7 +60,10 @@ __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word,
   // covers the approximate logarithms
   const float score = st.m + lg2(e) - lg2(E) - kPublishMargin;
   const uint32_t key = ordered_key(score);
-  if (key > shared_seen) atomicMax(row_best, key);  // shared memory
+  if (key > shared_seen) {
+    atomicMax(row_best, key);  // shared memory
+    atomicMax(global_best, key);
+  }
   return true;
 }
 
@@ -245,12 +252,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     float nref = 0.f;  // -st.m once the reference is set
     const PhiloxRow prow = philox_row((uint32_t)k, p.rid_base + (uint32_t)m, kPurposeDraft, p.rk);
     uint32_t* row_best = &s_best[row];
+    unsigned* global_best = p.row_best + (size_t)(k - 1) * p.R + (valid ? m : 0);
+    uint32_t global_seen = 0;  // one thread per row imports the global bound, one tile late
     uint32_t uoff[4];
     u_offsets(row, grp, uoff, TL());
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
     Ring r{0, 0u}, rb{0, 0u};
     for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
       if (abort_flag) break;
+      if (grp == 0 && valid) {  // the row's bound from the other CTAs (loaded last tile)
+        if (global_seen) atomicMax(row_best, global_seen);
+        global_seen = __ldcg(global_best);
+      }
       if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
           !tc::mbar_wait(&full_u[r.idx], r.phase, kWaitNs)) {
         fail();
@@ -302,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nref = -st.m;
         const uint4 bits = philox_in_row((uint32_t)(colbase >> 2) + (uint32_t)(im >> 2), prow, p.rk);
         if (race_candidate(st, tc::ex2(fmaf(mz, kscale, nref)), word_of(bits, im & 3), colbase + im,
-                           row_best, *reinterpret_cast<volatile uint32_t*>(row_best)))
+                           row_best, *reinterpret_cast<volatile uint32_t*>(row_best), global_best))
           c_own = __fdividef(st.bE, st.be) * kFilterUp;
       }
       // e = 2^(z kscale - ref) for the 16 columns and their sum (a tree)
@@ -355,49 +368,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                                kFilterUp);
       cf2.y = cf2.x;
       const float2 one2 = make_float2(1.f, 1.f);
+      // All four Philox blocks and the filter of the 16 columns in one
+      // straight-line block (the compiler interleaves the chains with the
+      // arithmetic); one branch to the rare exact tests.
+      uint32_t words[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int cb = colbase + 8 * h;
-        uint32_t words[8];
+      for (int q = 0; q < 4; ++q) {
+        const uint4 bits = philox_in_row((uint32_t)(colbase >> 2) + q, prow, p.rk);
+        words[4 * q] = bits.x;
+        words[4 * q + 1] = bits.y;
+        words[4 * q + 2] = bits.z;
+        words[4 * q + 3] = bits.w;
+      }
+      uint32_t all_neg = 0xffffffffu;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint4 bits = philox_in_row((uint32_t)(cb >> 2) + q, prow, p.rk);
-          words[4 * q] = bits.x;
-          words[4 * q + 1] = bits.y;
-          words[4 * q + 2] = bits.z;
-          words[4 * q + 3] = bits.w;
+      for (int i = 0; i < 8; ++i) {
+        const float2 d = __fadd2_rn(__ffma2_rn(e[i], cf2, one2),
+                                    make_float2(neg_one_plus_w(words[2 * i]), neg_one_plus_w(words[2 * i + 1])));
+        all_neg &= __float_as_uint(d.x) & __float_as_uint(d.y);
+      }
+      if (!(all_neg >> 31)) {  // rare: elements that could beat the best, in index order
+        uint32_t mask = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 d = __fadd2_rn(__ffma2_rn(e[i], cf2, one2),
+                                      make_float2(neg_one_plus_w(words[2 * i]), neg_one_plus_w(words[2 * i + 1])));
+          mask |= ((__float_as_uint(d.x) >> 31) ^ 1u) << (2 * i);
+          mask |= ((__float_as_uint(d.y) >> 31) ^ 1u) << (2 * i + 1);
         }
-        float2 d[4];  // g - f per element
-        uint32_t all_neg = 0xffffffffu;
+        if (colbase + 16 > V) mask &= (V > colbase) ? (1u << (V - colbase)) - 1u : 0u;
+        while (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1u;
+          float ei = e[0].x;
+          uint32_t wi = words[0];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          d[i] = __fadd2_rn(__ffma2_rn(e[4 * h + i], cf2, one2),
-                            make_float2(neg_one_plus_w(words[2 * i]), neg_one_plus_w(words[2 * i + 1])));
-          all_neg &= __float_as_uint(d[i].x) & __float_as_uint(d[i].y);
-        }
-        if (!(all_neg >> 31)) {  // rare: elements that could beat the best, in index order
-          uint32_t mask = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            mask |= ((__float_as_uint(d[i].x) >> 31) ^ 1u) << (2 * i);
-            mask |= ((__float_as_uint(d[i].y) >> 31) ^ 1u) << (2 * i + 1);
+          for (int j = 1; j < 16; ++j) {
+            ei = (i == j) ? ((j & 1) ? e[j >> 1].y : e[j >> 1].x) : ei;
+            wi = (i == j) ? words[j] : wi;
           }
-          if (cb + 8 > V) mask &= (V > cb) ? (1u << (V - cb)) - 1u : 0u;
-          while (mask) {
-            const int i = __ffs(mask) - 1;
-            mask &= mask - 1u;
-            float ei = e[4 * h].x;
-            uint32_t wi = words[0];
-#pragma unroll
-            for (int j = 1; j < 8; ++j) {
-              ei = (i == j) ? ((j & 1) ? e[4 * h + (j >> 1)].y : e[4 * h + (j >> 1)].x) : ei;
-              wi = (i == j) ? words[j] : wi;
-            }
-            if (race_candidate(st, ei, wi, cb + i, row_best, *reinterpret_cast<volatile uint32_t*>(row_best))) {
-              c_own = __fdividef(st.bE, st.be) * kFilterUp;
-              cf2.x = fminf(cf2.x, c_own);
-              cf2.y = cf2.x;
-            }
+          if (race_candidate(st, ei, wi, colbase + i, row_best, *reinterpret_cast<volatile uint32_t*>(row_best),
+                             global_best)) {
+            c_own = __fdividef(st.bE, st.be) * kFilterUp;
+            cf2.x = fminf(cf2.x, c_own);
+            cf2.y = cf2.x;
           }
         }
       }

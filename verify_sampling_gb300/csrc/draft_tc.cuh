@@ -21,6 +21,7 @@ struct DraftTCParams {
   float* lse_q;
   Partial* partials;   // [R, nsplit]
   unsigned* counters;  // [mtiles], zero on entry
+  unsigned* row_best;  // [gamma, R] best race score per row over all CTAs (ordered keys), zero on entry
   uint32_t* status;
 };
 

@@ -49,13 +49,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// try_wait that may suspend the thread until the phase completes, for at most
+// `hint_ns` nanoseconds, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
 // Wait for the phase of the given parity to complete, giving up after
-// `limit_ns` nanoseconds (returns false then).  The fast path costs one try.
+// `limit_ns` nanoseconds (returns false then).  The fast path costs one try;
+// after that the thread sleeps in the try (up to 1 ms at a time) instead of
+// spinning, so waiting warps take no issue slots from working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
