@@ -11,6 +11,8 @@ Each wrapper cites the passage of the pages it follows (see ``oracle.cpp``):
   * confidence -- DSpark summary, "2.1 置信度头" (+ sequential temperature scaling)
   * schedule   -- DSpark summary, "2.2 硬件感知前缀调度器" and "挑战2"; history "杀招三"
   * verify     -- history article, "1.1运行机制" (rejection sampling); DSpark Figure 1
+  * schedule, threshold mode -- DSpark summary, comparison table (SpecDec++) and Figure 5
+  * accept_stats -- LightSpec article, "无需额外训练，基于运行时统计的动态调度"
 """
 from __future__ import annotations
 
@@ -27,7 +29,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 DRAFT_GUMBEL, ACCEPT_U, RESIDUAL_GUMBEL, BONUS_GUMBEL = 0, 1, 2, 3
 MODE_SAMPLE, MODE_GREEDY = 0, 1
-SCHED_EARLY_STOP, SCHED_GLOBAL = 0, 1
+SCHED_EARLY_STOP, SCHED_GLOBAL, SCHED_THRESHOLD = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -65,11 +67,13 @@ def lib() -> ctypes.CDLL:
         L.orc_draft.restype = i32
         L.orc_confidence.argtypes = [i32, i32, i32, i32, i32, P, i64, P, P, P, P, P, P, P]
         L.orc_confidence.restype = i32
-        L.orc_schedule.argtypes = [i32, i32, P, P, i32, f64, f64, i32, i32, P, P, P, P, P, P]
+        L.orc_schedule.argtypes = [i32, i32, P, P, i32, f64, f64, i32, i32, f64, P, P, P, P, P, P]
         L.orc_schedule.restype = i32
         L.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, P, i64, P, P, i32, P, P,
                                  u64, u32, P, P, P, P, P]
         L.orc_verify.restype = i32
+        L.orc_accept_stats.argtypes = [i32, i32, P, P, i32, i32, f64, i32, P, P, P, P]
+        L.orc_accept_stats.restype = i32
         _lib = L
     return _lib
 
@@ -185,8 +189,10 @@ class ScheduleOut:
     theta_seq: np.ndarray
 
 
-def schedule(a, sps, b_lo: float, b_step: float, K: int, mode: int = SCHED_EARLY_STOP) -> ScheduleOut:
-    """a [R, gamma] survival probabilities; sps table at B_i = b_lo + i*b_step."""
+def schedule(a, sps, b_lo: float, b_step: float, K: int, mode: int = SCHED_EARLY_STOP,
+             threshold: float = 0.0) -> ScheduleOut:
+    """a [R, gamma] survival probabilities; sps table at B_i = b_lo + i*b_step.
+    ``threshold`` is used by SCHED_THRESHOLD only (admit a >= threshold)."""
     a = _f64(a)
     R, gamma = a.shape
     s = _f64(sps)
@@ -197,7 +203,8 @@ def schedule(a, sps, b_lo: float, b_step: float, K: int, mode: int = SCHED_EARLY
     order = np.zeros(R * gamma, np.int32)
     nmax = min(K, R * gamma)
     th = np.zeros(nmax + 1)
-    rc = lib().orc_schedule(R, gamma, _ptr(a), _ptr(s), s.size, b_lo, b_step, K, mode, _ptr(ell),
+    rc = lib().orc_schedule(R, gamma, _ptr(a), _ptr(s), s.size, b_lo, b_step, K, mode,
+                            float(threshold), _ptr(ell),
                             _ptr(row_off), _ptr(stats), ctypes.byref(mg), _ptr(order), _ptr(th))
     if rc != 0:
         raise ValueError(f"orc_schedule failed ({rc})")
@@ -245,3 +252,23 @@ def verify(mode: int, tgt, row_off, ell, x, q_tok, target_temp: float, U, A, Ct,
     if rc != 0:
         raise ValueError(f"orc_verify failed ({rc})")
     return VerifyOut(acc, out, n_out, mg, js)
+
+
+# ----------------------------------------------------- acceptance statistics --
+def accept_stats(ell, accept_len, ema, count, bucket: int, beta: float, min_count: int = 1):
+    """One round's EMA update of acceptance rates per MTP length (LightSpec
+    runtime statistics).  ``ema`` [n_buckets, gamma] f64 and ``count``
+    [n_buckets, gamma] int64 are updated IN PLACE; returns (estimate [gamma],
+    bad) with the interpolated rates of ``bucket`` after the update."""
+    ell, acc = _i32(ell), _i32(accept_len)
+    assert ema.dtype == np.float64 and count.dtype == np.int64
+    assert ema.flags.c_contiguous and count.flags.c_contiguous and ema.shape == count.shape
+    n_buckets, gamma = ema.shape
+    est = np.zeros(gamma)
+    bad = ctypes.c_int()
+    rc = lib().orc_accept_stats(ell.size, gamma, _ptr(ell), _ptr(acc), bucket, n_buckets,
+                                float(beta), int(min_count), _ptr(ema), _ptr(count), _ptr(est),
+                                ctypes.byref(bad))
+    if rc != 0:
+        raise ValueError(f"orc_accept_stats failed ({rc})")
+    return est, bad.value

@@ -267,15 +267,22 @@ int orc_confidence(int R, int gamma, int d, int e, int V, const float* h, int64_
 // beats the best so far, stop at the first drop).  [DSpark] "挑战2" adds the
 // top-K cap on the number admitted and the global search without early stop.
 //   mode 0 = early stop, mode 1 = global argmax over all sorted prefixes.
+//   mode 2 = static confidence threshold ([DSpark] comparison table: SpecDec++
+//            schedules by a fixed confidence threshold; Figure 5 sweeps it):
+//            every candidate whose survival a_{r,j} (the predicted probability
+//            that the prefix up to j is accepted) is >= threshold, i.e. the
+//            sorted prefix of those, still capped by K.  Theta is reported but
+//            not used; the decisions are exact comparisons (margin +inf).
 // Ties in the sort keep (request, position) order.  stats = {n, B, tau, Theta}.
 // margin = smallest relative Theta difference among the comparisons made.
 // order (nullable, [R*gamma]) receives the sorted candidate ids r*gamma + j-1;
 // theta (nullable, [min(K,R*gamma)+1]) receives Theta_0..Theta_nmax.
 int orc_schedule(int R, int gamma, const double* a, const double* sps, int n_sps, double b_lo,
-                 double b_step, int K, int mode, int32_t* ell, int32_t* row_off, double* stats,
-                 double* margin, int32_t* order, double* theta) {
-  if (R < 0 || gamma <= 0 || n_sps <= 0 || b_step <= 0.0 || K < 0 || (mode != 0 && mode != 1))
+                 double b_step, int K, int mode, double threshold, int32_t* ell,
+                 int32_t* row_off, double* stats, double* margin, int32_t* order, double* theta) {
+  if (R < 0 || gamma <= 0 || n_sps <= 0 || b_step <= 0.0 || K < 0 || mode < 0 || mode > 2)
     return -1;
+  if (mode == 2 && std::isnan(threshold)) return -1;
   const int N = R * gamma;
   std::vector<int> ids((size_t)N);
   for (int i = 0; i < N; ++i) ids[(size_t)i] = i;
@@ -302,6 +309,8 @@ int orc_schedule(int R, int gamma, const double* a, const double* sps, int n_sps
       else
         break;
     }
+  } else if (mode == 2) {
+    while (nstar < nmax && a[ids[(size_t)nstar]] >= threshold) ++nstar;
   } else {
     for (int n = 1; n <= nmax; ++n)
       if (th[(size_t)n] > th[(size_t)nstar]) nstar = n;
@@ -452,4 +461,80 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
   return 0;
 }
 
+// ------------------------------------------------- acceptance statistics ---
+// LightSpec article, "无需额外训练，基于运行时统计的动态调度": acceptance rates
+// are kept per batch-size class and per MTP length as exponential moving
+// averages updated every round; a length with too few samples is estimated by
+// interpolating the rates of the neighbouring lengths.
+//
+// One round's update of class `bucket` (rows of ema / count are classes, columns
+// are the lengths L = 1..gamma):
+//   n_L = number of requests with l_r = L, S_L = sum of their accept_len,
+//   m_L = S_L / (L * n_L)  (the fraction of the L drafted tokens accepted);
+//   for every L with n_L > 0: ema = m_L if no sample was seen before, else
+//   ema = ema + beta * (m_L - ema) (as one fused multiply-add); count += n_L.
+// Requests with l_r = 0 carry no draft and are skipped; an l_r outside
+// [0, gamma] or an accept_len outside [0, l_r] is skipped and counted in *bad.
+// estimate (nullable, [gamma]): for the updated class, the entry itself where
+// count >= max(min_count, 1); otherwise linear interpolation in L between the
+// nearest usable lengths below and above, the nearest one where only one side
+// has a usable length, NaN where none has.
+int orc_accept_stats(int R, int gamma, const int32_t* ell, const int32_t* accept_len, int bucket,
+                     int n_buckets, double beta, int min_count, double* ema, int64_t* count,
+                     double* estimate, int* bad) {
+  if (R < 0 || gamma < 1 || n_buckets < 1 || bucket < 0 || bucket >= n_buckets ||
+      !(beta > 0.0 && beta <= 1.0))
+    return -1;
+  std::vector<int64_t> n((size_t)gamma + 1, 0), S((size_t)gamma + 1, 0);
+  int nbad = 0;
+  for (int req = 0; req < R; ++req) {
+    const int l = ell[req], acc = accept_len[req];
+    if (l < 0 || l > gamma || acc < 0 || acc > l) {
+      ++nbad;
+      continue;
+    }
+    if (l == 0) continue;
+    n[(size_t)l] += 1;
+    S[(size_t)l] += acc;
+  }
+  double* e = ema + (size_t)bucket * gamma;
+  int64_t* c = count + (size_t)bucket * gamma;
+  for (int L = 1; L <= gamma; ++L) {
+    if (n[(size_t)L] == 0) continue;
+    const double m = (double)S[(size_t)L] / ((double)L * (double)n[(size_t)L]);
+    if (c[L - 1] == 0)
+      e[L - 1] = m;
+    else
+      e[L - 1] = std::fma(beta, m - e[L - 1], e[L - 1]);
+    c[L - 1] += n[(size_t)L];
+  }
+  if (estimate) {
+    const int64_t need = std::max(min_count, 1);
+    for (int L = 1; L <= gamma; ++L) {
+      if (c[L - 1] >= need) {
+        estimate[L - 1] = e[L - 1];
+        continue;
+      }
+      int lo = 0, hi = 0;
+      for (int q = L - 1; q >= 1 && !lo; --q)
+        if (c[q - 1] >= need) lo = q;
+      for (int q = L + 1; q <= gamma && !hi; ++q)
+        if (c[q - 1] >= need) hi = q;
+      if (lo && hi) {
+        const double w = (double)(L - lo) / (double)(hi - lo);
+        estimate[L - 1] = std::fma(w, e[hi - 1] - e[lo - 1], e[lo - 1]);
+      } else if (lo) {
+        estimate[L - 1] = e[lo - 1];
+      } else if (hi) {
+        estimate[L - 1] = e[hi - 1];
+      } else {
+        estimate[L - 1] = std::numeric_limits<double>::quiet_NaN();
+      }
+    }
+  }
+  if (bad) *bad = nbad;
+  return 0;
+}
+
 }  // extern "C"
+

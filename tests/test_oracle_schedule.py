@@ -143,3 +143,89 @@ def test_sps_lookup_linear_and_clamped():
 def test_zero_cap_admits_nothing():
     out = oracle.schedule(np.full((3, 2), 0.9), [1.0], 0, 1, 0, oracle.SCHED_EARLY_STOP)
     assert out.n == 0 and list(out.ell) == [0, 0, 0] and list(out.row_off) == [0, 1, 2, 3]
+
+
+# ------------------------------------------------------- threshold admission --
+# DSpark summary, comparison table (SpecDec++: a static confidence threshold) and
+# Figure 5 (a threshold sweep): mode SCHED_THRESHOLD admits every candidate whose
+# survival a_{r,j} reaches the threshold, capped by K.
+
+def _non_increasing(rng, R, gamma):
+    a = np.cumprod(rng.uniform(0.3, 1.0, (R, gamma)), axis=1)
+    return a.astype(np.float32).astype(np.float64)
+
+
+def test_threshold_admits_per_request_counts():
+    """Without a binding cap, l_r is the number of positions of r with a >= theta
+    (counted per request, not through the sorted list)."""
+    rng = np.random.default_rng(11)
+    for _ in range(30):
+        R, gamma = int(rng.integers(1, 12)), int(rng.integers(1, 12))
+        a = _non_increasing(rng, R, gamma)
+        theta = float(rng.uniform(0.0, 1.0))
+        out = oracle.schedule(a, [1.0], 0.0, 1.0, R * gamma, oracle.SCHED_THRESHOLD, theta)
+        want = [int(sum(1 for j in range(gamma) if a[r, j] >= theta)) for r in range(R)]
+        assert list(out.ell) == want
+        assert out.n == sum(want) and out.B == R + sum(want)
+        assert out.tau == pytest.approx(float(a[a >= theta].sum()), rel=1e-12, abs=0)
+        assert out.margin == float("inf")
+
+
+def test_threshold_cap_keeps_the_largest_survivals():
+    rng = np.random.default_rng(12)
+    for _ in range(30):
+        R, gamma = int(rng.integers(1, 10)), int(rng.integers(1, 10))
+        a = _non_increasing(rng, R, gamma)
+        a[rng.random((R, gamma)) < 0.2] = 0.5  # planted ties
+        a = np.minimum.accumulate(a, axis=1)
+        theta = float(rng.uniform(0.0, 0.9))
+        K = int(rng.integers(0, R * gamma + 1))
+        out = oracle.schedule(a, [1.0], 0.0, 1.0, K, oracle.SCHED_THRESHOLD, theta)
+        ids = [i for i in range(R * gamma) if a.reshape(-1)[i] >= theta]
+        ids.sort(key=lambda i: (-a.reshape(-1)[i], i))
+        chosen = ids[:K]
+        want = np.zeros(R, int)
+        for i in chosen:
+            want[i // gamma] += 1
+        assert list(out.ell) == list(want)
+
+
+def test_threshold_ends():
+    a = np.array([[0.9, 0.6, 0.2], [0.8, 0.8, 0.1]])
+    everything = oracle.schedule(a, [1.0], 0.0, 1.0, 6, oracle.SCHED_THRESHOLD, 0.0)
+    assert list(everything.ell) == [3, 3]
+    nothing = oracle.schedule(a, [1.0], 0.0, 1.0, 6, oracle.SCHED_THRESHOLD, 0.95)
+    assert nothing.n == 0 and list(nothing.row_off) == [0, 1, 2]
+    equal = oracle.schedule(a, [1.0], 0.0, 1.0, 6, oracle.SCHED_THRESHOLD, 0.8)
+    assert list(equal.ell) == [1, 2]  # a >= theta includes equality
+    with pytest.raises(ValueError):
+        oracle.schedule(a, [1.0], 0.0, 1.0, 6, oracle.SCHED_THRESHOLD, float("nan"))
+
+
+def test_threshold_sweep_raises_acceptance_rate():
+    """Figure 5: raising the threshold filters the likely rejections, so the
+    accepted fraction of the admitted tokens rises.  With calibrated
+    confidences (position j of r is accepted with probability c_{r,j} once the
+    positions before it were), the expected accepted count of an admitted
+    prefix is the sum of its survivals: the predicted rate tau / n must be
+    non-decreasing in theta, and a simulation of the verifier agrees with it."""
+    rng = np.random.default_rng(13)
+    R, gamma = 256, 8
+    c = rng.uniform(0.4, 1.0, (R, gamma))
+    a = np.cumprod(c, axis=1)
+    thresholds = [0.0, 0.2, 0.4, 0.6, 0.8]
+    rates = []
+    for th in thresholds:
+        out = oracle.schedule(a, [1.0], 0.0, 1.0, R * gamma, oracle.SCHED_THRESHOLD, th)
+        assert out.n > 0
+        rates.append(out.tau / out.n)
+        trials = 400
+        acc = 0
+        for _ in range(trials):
+            ok = rng.random((R, gamma)) < c
+            first_fail = np.where(ok.all(axis=1), gamma, np.argmin(ok, axis=1))
+            acc += int(np.minimum(first_fail, out.ell).sum())
+        sim = acc / (trials * out.n)
+        assert sim == pytest.approx(out.tau / out.n, abs=0.01)
+    assert all(x <= y for x, y in zip(rates, rates[1:]))
+    assert rates[-1] > rates[0] + 0.1
