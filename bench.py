@@ -43,7 +43,24 @@ def _args():
     p.add_argument("--config", default="c5", choices=["c2", "c3", "c5", "c5p", "greedy"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--sched-mode", default="workload",
+                   choices=["workload", "early_stop", "global", "threshold"],
+                   help="scheduler admission rule (default: the workload's own)")
+    p.add_argument("--sched-threshold", type=float, default=0.3,
+                   help="survival threshold of --sched-mode threshold")
+    p.add_argument("--accept-stats", action="store_true",
+                   help="fold every round into the per-length acceptance EMA table")
     return p.parse_args()
+
+
+def _workload(args):
+    import dataclasses
+    import synth
+    wl = synth.WORKLOADS[args.config]
+    if args.sched_mode != "workload":
+        mode = {"early_stop": 0, "global": 1, "threshold": 2}[args.sched_mode]
+        wl = dataclasses.replace(wl, sched_mode=mode, sched_threshold=args.sched_threshold)
+    return wl
 
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, taken with
@@ -134,7 +151,7 @@ def _oracle_round(wl, inp_cpu, seed: int, n_req: int) -> tuple[int, float]:
                              inp_cpu["sts_temp"].numpy())
     K = max(1, round(wl.K * n_req / wl.R))
     s = oracle.schedule(a, inp_cpu["sps"].numpy(), inp_cpu["b_lo"], inp_cpu["b_step"], K,
-                        wl.sched_mode)
+                        wl.sched_mode, wl.sched_threshold)
     G = wl.gamma
     rows = f(inp_cpu["tgt"][:n_req]).reshape(-1, wl.V)
     oracle.verify(oracle.MODE_SAMPLE, rows, (np.arange(n_req) * (G + 1)).astype(np.int32), s.ell,
@@ -185,7 +202,8 @@ def run_reference(args, wl):
             "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * tot_sec / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "R": wl.R, "gamma": wl.gamma, "V": wl.V, "r": wl.r},
+            "config": {"workload": wl.name, "R": wl.R, "gamma": wl.gamma, "V": wl.V, "r": wl.r,
+                       **_sched_config(wl)},
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
                              "sample": f"{n} of {wl.R} requests per step, full round"},
             "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
@@ -215,11 +233,19 @@ def combine_over_ranks(ms: float, positions: float, device, world: int) -> tuple
     return float(tm.item()), float(tp.item())
 
 
+def _sched_config(wl) -> dict:
+    names = {0: "early_stop", 1: "global", 2: "threshold"}
+    out = {"sched_mode": names[wl.sched_mode]}
+    if wl.sched_mode == 2:
+        out["sched_threshold"] = wl.sched_threshold
+    return out
+
+
 # ------------------------------------------------------------------ ours ----
 def main():
     args = _args()
     import synth
-    wl = synth.WORKLOADS[args.config]
+    wl = _workload(args)
     if args.impl == "reference":
         return run_reference(args, wl)
 
@@ -249,6 +275,11 @@ def main():
                                        dtype=torch.uint8, device=dev)
     bufs["ws_verify"] = torch.empty(vs.workspace_bytes(vs.STAGE_VERIFY, R, G, V), dtype=torch.uint8,
                                     device=dev)
+    acc_tab = None
+    if args.accept_stats and not greedy:
+        acc_tab = {"ema": torch.zeros(1, G, dtype=torch.float64, device=dev),
+                   "count": torch.zeros(1, G, dtype=torch.int64, device=dev),
+                   "estimate": torch.zeros(G, dtype=torch.float64, device=dev)}
     stream = torch.cuda.current_stream()
     nev = max(1, args.steps)
     ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
@@ -267,7 +298,7 @@ def main():
         if timed:
             ev["d1"][i].record(stream)
         s = vs.schedule(d["a"], g["sps"], g["b_lo"], g["b_step"], wl.K, wl.sched_mode,
-                        out=bufs.get("sched"))
+                        threshold=wl.sched_threshold, out=bufs.get("sched"))
         bufs["sched"] = s
         if timed:
             ev["s1"][i].record(stream)
@@ -276,6 +307,9 @@ def main():
                       request_id_base=rid_base, out=bufs.get("verify"),
                       workspace=bufs["ws_verify"])
         bufs["verify"] = v
+        if acc_tab is not None:
+            vs.accept_stats(s["ell"], v["accept_len"], acc_tab["ema"], acc_tab["count"], 0, 0.1,
+                            estimate=acc_tab["estimate"])
         if timed:
             ev["v1"][i].record(stream)
             stats_hist[i].copy_(s["stats"], non_blocking=True)
@@ -330,7 +364,7 @@ def main():
         kernel = "draft_step (one launch per position k)"
         # per round: gamma draft steps, confidence, schedule, verify rows,
         # fused residual, residual fallback (gated, exits at once when unused)
-        launches = G + 5
+        launches = G + 5 + (1 if acc_tab is not None else 0)
     achieved = per_launch / (dur_ms / 1000.0) / 1e9
     traffic = None if greedy else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
@@ -346,7 +380,9 @@ def main():
                        "logits": str(wl.logit_dtype).replace("torch.", ""),
                        "factors": str(wl.fac_dtype).replace("torch.", ""),
                        "l2": "inputs larger than L2 (no flush)",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       **_sched_config(wl), **({"accept_stats": True} if acc_tab is not None
+                                               else {})},
             "stage_ms_per_step": {k: round(v / args.steps, 4) for k, v in stage_ms.items()},
             "mean_verify_rows": B_sum / args.steps,
             "roofline": roofline, "gpu_launches": launches * args.steps, "clocks": clk}
@@ -386,6 +422,7 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
             devb[n].copy_(host[n], non_blocking=True)
         res = vs.run_round(d_in, devb["tgt"].view(-1, wl.V), g["tgt_row_off"], g["sps"],
                            g["b_lo"], g["b_step"], wl.K, 9000 + i, sched_mode=wl.sched_mode,
+                           sched_threshold=wl.sched_threshold,
                            bufs={"draft": bufs["draft"], "ws_draft": bufs["ws_draft"],
                                  "ws_verify": bufs["ws_verify"]})
         v, s = res["verify"], res["sched"]

@@ -67,7 +67,7 @@ enum spec_status_code {
 
 enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 };
 enum spec_verify_mode { SPEC_VERIFY_SAMPLE = 0, SPEC_VERIFY_GREEDY = 1 };
-enum spec_sched_mode { SPEC_SCHED_EARLY_STOP = 0, SPEC_SCHED_GLOBAL = 1 };
+enum spec_sched_mode { SPEC_SCHED_EARLY_STOP = 0, SPEC_SCHED_GLOBAL = 1, SPEC_SCHED_THRESHOLD = 2 };
 enum spec_stage { SPEC_STAGE_DRAFT = 0, SPEC_STAGE_SCHEDULE = 1, SPEC_STAGE_VERIFY = 2 };
 
 /* Bits of the device status word. */
@@ -164,7 +164,12 @@ int spec_draft_sample_static(const spec_draft_args *args, uint64_t seed, spec_st
  *                            linear interpolation inside, clamped outside
  *   K       cap on sum_r l_r (>= 0)
  *   mode    SPEC_SCHED_EARLY_STOP: admit while Theta_{n+1} > Theta_n (strict),
- *           Theta_0 = 0;  SPEC_SCHED_GLOBAL: n = smallest argmax_n Theta_n
+ *           Theta_0 = 0;  SPEC_SCHED_GLOBAL: n = smallest argmax_n Theta_n;
+ *           SPEC_SCHED_THRESHOLD: a static confidence threshold (DSpark
+ *           summary, comparison table: SpecDec++; Figure 5 sweeps it) -- n =
+ *           the number of survivals with a >= threshold (compared in fp64,
+ *           exactly), capped by K; SPS only enters the reported Theta
+ *   threshold  used by SPEC_SCHED_THRESHOLD only; NaN is an argument error
  * Sort order: a descending, then request ascending, then position ascending.
  * tau and Theta are computed in fp64.
  * Outputs: ell [R] int32; row_off [R + 1] int32 with row_off[r + 1] = row_off[r]
@@ -187,9 +192,50 @@ typedef struct spec_sched_args {
   void *workspace;
   size_t workspace_bytes;
   uint32_t *status;
+  double threshold;
 } spec_sched_args;
 
 int spec_schedule(const spec_sched_args *args, spec_stream_t stream);
+
+/* ----------------------------------------------------- acceptance stats -
+ * LightSpec article, "无需额外训练，基于运行时统计的动态调度": acceptance rates are
+ * kept per request-scale / batch-size class and per MTP length as exponential
+ * moving averages updated every round, and a length with too few samples is
+ * estimated by interpolating over the other lengths.  One call folds a
+ * verified round into class `bucket` (one thread block, no workspace):
+ *   n_L = #{r : ell[r] = L}, S_L = sum of their accept_len, for L = 1..gamma;
+ *   where n_L > 0:  m_L = S_L / (L * n_L)  (fp64, correctly rounded);
+ *                   ema = m_L if count == 0, else fma(beta, m_L - ema, ema);
+ *                   count += n_L.
+ * Requests with ell = 0 carry no draft and are skipped.  An ell outside
+ * [0, gamma] or an accept_len outside [0, ell] is skipped and sets
+ * SPEC_STATUS_BAD_ELL.
+ *   ell, accept_len  [R] int32 device (spec_schedule / spec_verify outputs)
+ *   ema    [n_buckets, gamma] f64 device, in/out (zero it before the first call)
+ *   count  [n_buckets, gamma] int64 device, in/out (zero before the first call)
+ *   estimate [gamma] f64 device, nullable: rates of class `bucket` after the
+ *          update -- the entry where count >= max(min_count, 1), else linear
+ *          interpolation in L between the nearest such lengths below and
+ *          above (fma(w, e_hi - e_lo, e_lo), w = (L - lo) / (hi - lo)), the
+ *          nearest one when only one side has any, NaN when none has
+ *   beta   in (0, 1];  0 <= bucket < n_buckets;  gamma <= 1024;  R >= 0
+ * Every operation is the fp64 one written above, so results are
+ * reproducible bit for bit.
+ */
+typedef struct spec_accept_stats_args {
+  int R, gamma;
+  const int32_t *ell;
+  const int32_t *accept_len;
+  int bucket, n_buckets;
+  double beta;
+  int min_count;
+  double *ema;
+  int64_t *count;
+  double *estimate;
+  uint32_t *status;
+} spec_accept_stats_args;
+
+int spec_accept_stats(const spec_accept_stats_args *args, spec_stream_t stream);
 
 /* ----------------------------------------------------------------- verify -
  * History article, "1.1运行机制" (rejection sampling): accept x_j with

@@ -49,13 +49,14 @@ class Workload:
     conf_dtype: torch.dtype
     mode: str            # "sample" (full round) or "greedy" (verify only)
     K: int
-    sched_mode: int      # 0 early stop, 1 global
+    sched_mode: int      # 0 early stop, 1 global, 2 static threshold
     target: str          # "noise", "zipf" or "planted_argmax"
     sps_kind: str        # "linear16", "linear", "sawtooth"
     u_std: float
     peak: float
     seed: int
     sts_ramp: bool = False
+    sched_threshold: float = 0.0  # read by the static-threshold mode only
 
     def scaled(self, **kw) -> "Workload":
         """Same recipe at other sizes (for parity cases the oracle finishes quickly).

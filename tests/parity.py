@@ -69,10 +69,10 @@ def compare_confidence(inp: dict, out: dict, reqs) -> None:
 
 
 def compare_schedule(inp: dict, a_gpu: torch.Tensor, sched: dict, K: int, mode: int,
-                     rep=None) -> Report:
+                     rep=None, threshold: float = 0.0) -> Report:
     rep = rep or Report()
     os_ = oracle.schedule(to_np(a_gpu).astype(np.float64), to_np(inp["sps"]).astype(np.float64),
-                          inp["b_lo"], inp["b_step"], K, mode)
+                          inp["b_lo"], inp["b_step"], K, mode, threshold)
     stats = to_np(sched["stats"])
     if os_.margin < NEAR_TIE:
         rep.near_ties += 1

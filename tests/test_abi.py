@@ -30,7 +30,8 @@ def _declared_functions():
 def test_every_declared_symbol_is_exported(spec):
     names = _declared_functions()
     assert {"spec_draft_sample", "spec_schedule", "spec_verify", "spec_workspace_bytes",
-            "spec_error_string", "spec_stream_uniforms", "spec_version"} <= set(names)
+            "spec_error_string", "spec_stream_uniforms", "spec_version",
+            "spec_accept_stats"} <= set(names)
     lib = spec.lib()
     for n in names:
         assert hasattr(lib, n), n
@@ -49,8 +50,11 @@ def test_struct_layout_matches_c(spec, tmp_path):
         'printf("spec_draft_args %zu\\n", sizeof(spec_draft_args));\n'
         'printf("spec_sched_args %zu\\n", sizeof(spec_sched_args));\n'
         'printf("spec_verify_args %zu\\n", sizeof(spec_verify_args));\n'
+        'printf("spec_accept_stats_args %zu\\n", sizeof(spec_accept_stats_args));\n'
         "P(spec_draft_args, status) P(spec_draft_args, workspace_bytes) P(spec_draft_args, U)\n"
         "P(spec_sched_args, b_lo) P(spec_sched_args, stats) P(spec_sched_args, status)\n"
+        "P(spec_sched_args, threshold) P(spec_accept_stats_args, beta)\n"
+        "P(spec_accept_stats_args, ema) P(spec_accept_stats_args, status)\n"
         "P(spec_verify_args, target_temp) P(spec_verify_args, draft) P(spec_verify_args, status)\n"
         "return 0;}\n")
     exe = tmp_path / "layout"
@@ -61,12 +65,17 @@ def test_struct_layout_matches_c(spec, tmp_path):
     assert int(got["spec_draft_args"]) == ctypes.sizeof(spec.DraftArgs)
     assert int(got["spec_sched_args"]) == ctypes.sizeof(spec.SchedArgs)
     assert int(got["spec_verify_args"]) == ctypes.sizeof(spec.VerifyArgs)
+    assert int(got["spec_accept_stats_args"]) == ctypes.sizeof(spec.AcceptStatsArgs)
     for key, (cls, field) in {"spec_draft_args.status": (spec.DraftArgs, "status"),
                               "spec_draft_args.workspace_bytes": (spec.DraftArgs, "workspace_bytes"),
                               "spec_draft_args.U": (spec.DraftArgs, "U"),
                               "spec_sched_args.b_lo": (spec.SchedArgs, "b_lo"),
                               "spec_sched_args.stats": (spec.SchedArgs, "stats"),
                               "spec_sched_args.status": (spec.SchedArgs, "status"),
+                              "spec_sched_args.threshold": (spec.SchedArgs, "threshold"),
+                              "spec_accept_stats_args.beta": (spec.AcceptStatsArgs, "beta"),
+                              "spec_accept_stats_args.ema": (spec.AcceptStatsArgs, "ema"),
+                              "spec_accept_stats_args.status": (spec.AcceptStatsArgs, "status"),
                               "spec_verify_args.target_temp": (spec.VerifyArgs, "target_temp"),
                               "spec_verify_args.draft": (spec.VerifyArgs, "draft"),
                               "spec_verify_args.status": (spec.VerifyArgs, "status")}.items():
@@ -110,6 +119,23 @@ def test_host_side_rejections_launch_nothing(spec):
     s.b_step = 1.0
     s.stats = ctypes.c_void_p(260)  # not 8-byte aligned
     assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_ALIGNMENT
+    s.stats = ctypes.c_void_p(256)
+    s.mode, s.threshold = spec.SCHED_THRESHOLD, float("nan")
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_INVALID_ARG
+    s.mode = 3
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_INVALID_ARG
+    st = spec.AcceptStatsArgs()
+    assert lib.spec_accept_stats(None, None) == spec.SPEC_ERR_INVALID_ARG
+    st.R, st.gamma, st.n_buckets, st.bucket, st.beta = 4, 4, 2, 0, 0.5
+    st.ell = st.accept_len = st.ema = st.count = ctypes.c_void_p(256)
+    st.bucket = 2
+    assert lib.spec_accept_stats(ctypes.byref(st), None) == spec.SPEC_ERR_INVALID_ARG
+    st.bucket, st.beta = 1, 0.0
+    assert lib.spec_accept_stats(ctypes.byref(st), None) == spec.SPEC_ERR_INVALID_ARG
+    st.beta, st.gamma = 0.5, 2000
+    assert lib.spec_accept_stats(ctypes.byref(st), None) == spec.SPEC_ERR_UNSUPPORTED
+    st.gamma, st.ema = 4, ctypes.c_void_p(260)
+    assert lib.spec_accept_stats(ctypes.byref(st), None) == spec.SPEC_ERR_ALIGNMENT
     v = spec.VerifyArgs()
     v.mode, v.R, v.gamma, v.V = 0, 2, 2, 10
     v.tgt = v.tgt_row_off = v.ell = v.x = v.accept_len = v.out_tok = v.n_out = ctypes.c_void_p(256)

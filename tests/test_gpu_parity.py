@@ -22,6 +22,8 @@ SMALL = {
     "c2_small": synth.WORKLOADS["c2"].scaled(R=6, gamma=5, V=20001, d=256),
     "c3_small": synth.WORKLOADS["c3"].scaled(R=12, gamma=8, V=8195, d=128),
     "c3_small_global": synth.WORKLOADS["c3"].scaled(R=12, gamma=8, V=8195, d=128, sched_mode=1),
+    "c3_small_threshold": synth.WORKLOADS["c3"].scaled(R=12, gamma=8, V=8195, d=128, sched_mode=2,
+                                                       sched_threshold=0.35),
     "c5_small": synth.WORKLOADS["c5"].scaled(R=8, gamma=6, V=12003, d=200),
     "v3": synth.WORKLOADS["tiny"].scaled(R=3, gamma=2, V=3, r=2, d=4, e=2),
     "v1": synth.WORKLOADS["tiny"].scaled(R=2, gamma=1, V=1, r=1, d=3, e=1),
@@ -33,6 +35,8 @@ SMALL = {
     "tc_c3_small_R130": synth.WORKLOADS["c3"].scaled(R=130, gamma=3, V=4136, d=64),
     "tc_c5_small": synth.WORKLOADS["c5"].scaled(R=8, gamma=6, V=12004, d=200),
     "tc_c5_temp": synth.WORKLOADS["c5"].scaled(R=3, gamma=2, V=3000, d=16, r=64),
+    "tc_c5_threshold": synth.WORKLOADS["c5"].scaled(R=8, gamma=6, V=12004, d=200, sched_mode=2,
+                                                    sched_threshold=0.2),
 }
 SAMPLED = {"tc_c3_small_R130": [0, 1, 2, 64, 127, 128, 129]}
 
@@ -45,7 +49,7 @@ def _run(g, wl, seed, want_P=False, rid_base=0, target_temp=1.0):
     din = synth.draft_inputs(g, request_id_base=rid_base)
     d = vs.draft_sample(din, seed, want_P=want_P)
     s = vs.schedule(d["a"], g["sps"], g["b_lo"], g["b_step"], g["K"], wl.sched_mode,
-                    want_order=True)
+                    threshold=wl.sched_threshold, want_order=True)
     v = vs.verify(vs.VERIFY_SAMPLE, g["tgt"].view(-1, wl.V), g["tgt_row_off"], s["ell"], d["x"],
                   seed, q_tok=d["q_tok"], lse_q=d["lse_q"], target_temp=target_temp, draft=din,
                   request_id_base=rid_base, want_p=True)
@@ -65,7 +69,7 @@ def test_round_parity_small(name):
     reqs = SAMPLED.get(name, range(wl.R))
     rep = compare_draft(g, d, seed, reqs)
     compare_confidence(g, d, reqs)
-    compare_schedule(g, d["a"], s, wl.K, wl.sched_mode, rep)
+    compare_schedule(g, d["a"], s, wl.K, wl.sched_mode, rep, wl.sched_threshold)
     compare_verify(g, d, s["ell"], v, seed, oracle.MODE_SAMPLE, reqs, rep=rep)
     print(f"{name}: checked {rep.checked}, near-ties {rep.near_ties} {rep.notes}")
     # outputs are well formed
@@ -185,7 +189,7 @@ def test_full_size_sampled_parity(name):
     reqs = sorted({0, 1, wl.R // 2, wl.R - 1})
     rep = compare_draft(g, d, seed, reqs)
     compare_confidence(g, d, range(wl.R))
-    compare_schedule(g, d["a"], s, wl.K, wl.sched_mode, rep)
+    compare_schedule(g, d["a"], s, wl.K, wl.sched_mode, rep, wl.sched_threshold)
     compare_verify(g, d, s["ell"], v, seed, oracle.MODE_SAMPLE, reqs, rep=rep)
     print(f"{name}: checked {rep.checked}, near-ties {rep.near_ties} {rep.notes}")
     B = int(to_np(s["stats"])[1])

@@ -28,7 +28,7 @@ SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_ALIGNMENT, SPEC_ER
     SPEC_ERR_CUDA = range(6)
 SPEC_F32, SPEC_BF16 = 0, 1
 VERIFY_SAMPLE, VERIFY_GREEDY = 0, 1
-SCHED_EARLY_STOP, SCHED_GLOBAL = 0, 1
+SCHED_EARLY_STOP, SCHED_GLOBAL, SCHED_THRESHOLD = 0, 1, 2
 STAGE_DRAFT, STAGE_SCHEDULE, STAGE_VERIFY = 0, 1, 2
 STATUS_BAD_TOKEN, STATUS_BAD_ELL, STATUS_BAD_SURVIVAL, STATUS_BAD_ROW = 0x1, 0x2, 0x4, 0x8
 
@@ -51,7 +51,15 @@ class SchedArgs(ctypes.Structure):
                 ("n_sps", ctypes.c_int), ("b_lo", ctypes.c_double), ("b_step", ctypes.c_double),
                 ("K", ctypes.c_int), ("mode", ctypes.c_int), ("ell", _P), ("row_off", _P),
                 ("stats", _P), ("order", _P), ("workspace", _P),
-                ("workspace_bytes", ctypes.c_size_t), ("status", _P)]
+                ("workspace_bytes", ctypes.c_size_t), ("status", _P),
+                ("threshold", ctypes.c_double)]
+
+
+class AcceptStatsArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int), ("gamma", ctypes.c_int), ("ell", _P), ("accept_len", _P),
+                ("bucket", ctypes.c_int), ("n_buckets", ctypes.c_int), ("beta", ctypes.c_double),
+                ("min_count", ctypes.c_int), ("ema", _P), ("count", _P), ("estimate", _P),
+                ("status", _P)]
 
 
 class VerifyArgs(ctypes.Structure):
@@ -82,7 +90,8 @@ def lib() -> ctypes.CDLL:
         L.spec_draft_sample.argtypes = [ctypes.POINTER(DraftArgs), ctypes.c_uint64, _P]
         L.spec_schedule.argtypes = [ctypes.POINTER(SchedArgs), _P]
         L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_uint64, _P]
-        for f in (L.spec_draft_sample, L.spec_schedule, L.spec_verify):
+        L.spec_accept_stats.argtypes = [ctypes.POINTER(AcceptStatsArgs), _P]
+        for f in (L.spec_draft_sample, L.spec_schedule, L.spec_verify, L.spec_accept_stats):
             f.restype = ctypes.c_int
         L.spec_workspace_bytes.argtypes = [ctypes.c_int] * 5
         L.spec_workspace_bytes.restype = ctypes.c_size_t
@@ -223,9 +232,11 @@ def draft_sample(inp: DraftInputs, seed: int, *, want_P: bool = False, out: Opti
 
 # ----------------------------------------------------------------- schedule --
 def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: int,
-             mode: int = SCHED_EARLY_STOP, *, want_order: bool = False, out: Optional[dict] = None,
-             status: Optional[torch.Tensor] = None, stream=None) -> dict:
-    """spec_schedule: l_r, packed row offsets and {n, B, tau, Theta} on the device."""
+             mode: int = SCHED_EARLY_STOP, *, threshold: float = 0.0, want_order: bool = False,
+             out: Optional[dict] = None, status: Optional[torch.Tensor] = None,
+             stream=None) -> dict:
+    """spec_schedule: l_r, packed row offsets and {n, B, tau, Theta} on the device.
+    ``threshold`` is read by SCHED_THRESHOLD only (admit survivals >= threshold)."""
     a = _dev(a, "a")
     sps = _dev(sps, "sps")
     if a.dtype != torch.float32 or sps.dtype != torch.float32:
@@ -242,6 +253,7 @@ def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: 
     s.R, s.gamma = R, gamma
     s.a, s.sps, s.n_sps = _ptr(a), _ptr(sps), sps.numel()
     s.b_lo, s.b_step, s.K, s.mode = float(b_lo), float(b_step), int(K), int(mode)
+    s.threshold = float(threshold)
     s.ell, s.row_off, s.stats = _ptr(outs["ell"]), _ptr(outs["row_off"]), _ptr(outs["stats"])
     s.order = _ptr(outs.get("order"))
     s.status = _ptr(status)
@@ -293,17 +305,47 @@ def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.T
     return outs
 
 
+# ---------------------------------------------------------- acceptance stats --
+def accept_stats(ell: torch.Tensor, accept_len: torch.Tensor, ema: torch.Tensor,
+                 count: torch.Tensor, bucket: int, beta: float, *, min_count: int = 1,
+                 estimate: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                 stream=None) -> Optional[torch.Tensor]:
+    """spec_accept_stats: fold one verified round into the per-length EMA table
+    ``ema`` [n_buckets, gamma] f64 / ``count`` [n_buckets, gamma] int64 (both
+    updated in place on the device); returns ``estimate`` [gamma] f64 if given."""
+    ell, accept_len = _dev(ell, "ell"), _dev(accept_len, "accept_len")
+    ema, count = _dev(ema, "ema"), _dev(count, "count")
+    if ell.dtype != torch.int32 or accept_len.dtype != torch.int32:
+        raise TypeError("ell and accept_len must be int32")
+    if ema.dtype != torch.float64 or count.dtype != torch.int64 or ema.shape != count.shape \
+            or ema.dim() != 2:
+        raise TypeError("ema must be float64 and count int64, both [n_buckets, gamma]")
+    a = AcceptStatsArgs()
+    a.R, (a.n_buckets, a.gamma) = ell.numel(), ema.shape
+    a.ell, a.accept_len = _ptr(ell), _ptr(accept_len)
+    a.bucket, a.beta, a.min_count = int(bucket), float(beta), int(min_count)
+    a.ema, a.count = _ptr(ema), _ptr(count)
+    if estimate is not None:
+        estimate = _dev(estimate, "estimate")
+        if estimate.dtype != torch.float64 or estimate.numel() < a.gamma:
+            raise TypeError("estimate must be float64 with gamma entries")
+    a.estimate = _ptr(estimate)
+    a.status = _ptr(status)
+    _check(lib().spec_accept_stats(ctypes.byref(a), _stream_handle(stream)), "spec_accept_stats")
+    return estimate
+
+
 # -------------------------------------------------------------------- round --
 def run_round(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.Tensor,
               sps: torch.Tensor, b_lo: float, b_step: float, K: int, seed: int, *,
-              sched_mode: int = SCHED_EARLY_STOP, target_temp: float = 1.0,
-              bufs: Optional[dict] = None, stream=None) -> dict:
+              sched_mode: int = SCHED_EARLY_STOP, sched_threshold: float = 0.0,
+              target_temp: float = 1.0, bufs: Optional[dict] = None, stream=None) -> dict:
     """One full round -- draft, schedule, verify -- on one stream, no host sync."""
     bufs = {} if bufs is None else bufs
     d = draft_sample(draft_in, seed, out=bufs.get("draft"), workspace=bufs.get("ws_draft"),
                      status=bufs.get("status"), stream=stream)
-    s = schedule(d["a"], sps, b_lo, b_step, K, sched_mode, out=bufs.get("sched"),
-                 status=bufs.get("status"), stream=stream)
+    s = schedule(d["a"], sps, b_lo, b_step, K, sched_mode, threshold=sched_threshold,
+                 out=bufs.get("sched"), status=bufs.get("status"), stream=stream)
     v = verify(VERIFY_SAMPLE, tgt, tgt_row_off, s["ell"], d["x"], seed, q_tok=d["q_tok"],
                lse_q=d["lse_q"], target_temp=target_temp, draft=draft_in,
                request_id_base=draft_in.request_id_base, out=bufs.get("verify"),

@@ -6,6 +6,7 @@
 #include "draft.cuh"
 #include "draft_tc.cuh"
 #include "schedule.cuh"
+#include "accept_stats.cuh"
 #include "residual_tc.cuh"
 #include "verify.cuh"
 
@@ -204,7 +205,9 @@ int spec_schedule(const spec_sched_args* args, spec_stream_t stream) {
   if (!args) return SPEC_ERR_INVALID_ARG;
   const spec_sched_args& a = *args;
   if (a.R < 1 || a.gamma < 1 || a.n_sps < 1 || a.K < 0 ||
-      (a.mode != SPEC_SCHED_EARLY_STOP && a.mode != SPEC_SCHED_GLOBAL) || !(a.b_step > 0.0) ||
+      (a.mode != SPEC_SCHED_EARLY_STOP && a.mode != SPEC_SCHED_GLOBAL &&
+       a.mode != SPEC_SCHED_THRESHOLD) ||
+      (a.mode == SPEC_SCHED_THRESHOLD && a.threshold != a.threshold) || !(a.b_step > 0.0) ||
       !(a.b_step < 1e300) || !(a.b_lo > -1e300 && a.b_lo < 1e300))
     return SPEC_ERR_INVALID_ARG;
   if (!a.a || !a.sps || !a.ell || !a.row_off || !a.stats) return SPEC_ERR_INVALID_ARG;
@@ -220,6 +223,7 @@ int spec_schedule(const spec_sched_args* args, spec_stream_t stream) {
   p.mode = a.mode;
   p.b_lo = a.b_lo;
   p.b_step = a.b_step;
+  p.threshold = a.threshold;
   p.a = a.a;
   p.sps = a.sps;
   p.ell = a.ell;
@@ -320,4 +324,34 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   return SPEC_OK;
 }
 
+int spec_accept_stats(const spec_accept_stats_args* args, spec_stream_t stream) {
+  if (!args) return SPEC_ERR_INVALID_ARG;
+  const spec_accept_stats_args& a = *args;
+  if (a.R < 0 || a.gamma < 1 || a.n_buckets < 1 || a.bucket < 0 || a.bucket >= a.n_buckets ||
+      !(a.beta > 0.0 && a.beta <= 1.0))
+    return SPEC_ERR_INVALID_ARG;
+  if (!a.ema || !a.count || (a.R > 0 && (!a.ell || !a.accept_len))) return SPEC_ERR_INVALID_ARG;
+  if (a.gamma > kAcceptStatsMaxGamma) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned(a.ell, 4) || !aligned(a.accept_len, 4) || !aligned(a.ema, 8) ||
+      !aligned(a.count, 8) || !aligned(a.estimate, 8) || !aligned(a.status, 4))
+    return SPEC_ERR_ALIGNMENT;
+  AcceptStatsParams p{};
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.bucket = a.bucket;
+  p.n_buckets = a.n_buckets;
+  p.min_count = a.min_count;
+  p.beta = a.beta;
+  p.ell = a.ell;
+  p.accept_len = a.accept_len;
+  p.ema = a.ema;
+  p.count = reinterpret_cast<long long*>(a.count);
+  p.estimate = a.estimate;
+  p.status = a.status;
+  return launch_accept_stats(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
 }  // extern "C"
+

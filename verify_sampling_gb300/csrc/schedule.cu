@@ -11,7 +11,9 @@
 // ascending: request, then position) in shared memory.  tau_n is an fp64
 // inclusive scan of the sorted survivals, Theta_n = tau_n * SPS(R + n); the
 // early-stop index is the first n with Theta_{n+1} <= Theta_n and the global
-// index the smallest argmax.
+// index the smallest argmax.  DSpark summary, comparison table (SpecDec++) and
+// Figure 5: the threshold index is the first sorted n whose survival is below
+// a static threshold.
 #include "schedule.cuh"
 
 namespace spec {
@@ -253,10 +255,15 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
   }
   __syncthreads();
   // 5. choose n*.
-  if (p.mode == SPEC_SCHED_EARLY_STOP) {
+  if (p.mode != SPEC_SCHED_GLOBAL) {
+    // first sorted position that stops the admission
+    const bool thr = p.mode == SPEC_SCHED_THRESHOLD;
     int first = nmax;
-    for (int n = tid; n < nmax; n += kThreads)
-      if (!(theta[n + 1] > theta[n])) first = min(first, n);
+    for (int n = tid; n < nmax; n += kThreads) {
+      const bool stop = thr ? !((double)__uint_as_float(~keyA[n]) >= p.threshold)
+                            : !(theta[n + 1] > theta[n]);
+      if (stop) first = min(first, n);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) first = min(first, __shfl_down_sync(0xffffffffu, first, off));
     if (lane == 0) bestn_s[warp] = first;

@@ -10,6 +10,7 @@ constexpr int kSchedMaxCandidates = 8192;  // R * gamma, one thread block
 struct SchedParams {
   int R, gamma, n_sps, K, mode, npad;
   double b_lo, b_step;
+  double threshold;  // SPEC_SCHED_THRESHOLD: admit survivals >= threshold
   bool unit_grid;  // b_step == 1 and b_lo integral: SPS(B) is a table entry
   long b_lo_int;
   const float* a;
