@@ -13,6 +13,7 @@ Each wrapper cites the passage of the pages it follows (see ``oracle.cpp``):
   * verify     -- history article, "1.1运行机制" (rejection sampling); DSpark Figure 1
   * schedule, threshold mode -- DSpark summary, comparison table (SpecDec++) and Figure 5
   * accept_stats -- LightSpec article, "无需额外训练，基于运行时统计的动态调度"
+  * cstar, calibration -- DSpark summary, "2.1 置信度头" and Figure 6
 """
 from __future__ import annotations
 
@@ -74,6 +75,10 @@ def lib() -> ctypes.CDLL:
         L.orc_verify.restype = i32
         L.orc_accept_stats.argtypes = [i32, i32, P, P, i32, i32, f64, i32, P, P, P, P]
         L.orc_accept_stats.restype = i32
+        L.orc_cstar.argtypes = [i32, i32, i32, P, P, P, P, f64, P, i64, P, P, i32, P, P, P]
+        L.orc_cstar.restype = i32
+        L.orc_calibration.argtypes = [i32, i32, P, P, P, i32, P, P, P, P, P]
+        L.orc_calibration.restype = i32
         _lib = L
     return _lib
 
@@ -272,3 +277,39 @@ def accept_stats(ell, accept_len, ema, count, bucket: int, beta: float, min_coun
     if rc != 0:
         raise ValueError(f"orc_accept_stats failed ({rc})")
     return est, bad.value
+
+
+# --------------------------------------------------- calibration diagnostics --
+def cstar(tgt, row_off, ell, x, target_temp: float, U, A, Ct, x0, draft_temp) -> np.ndarray:
+    """c* = sum_v min(p_v, q_v) for every verified draft row (r, j <= l_r);
+    NaN past l_r.  Layouts as in ``verify``."""
+    tgt = _f32(tgt)
+    V = tgt.shape[-1]
+    tgt = tgt.reshape(-1, V)
+    x = _i32(x)
+    R, gamma = x.shape
+    U, A, Ct = _f32(U), _f32(A), _f32(Ct)
+    out = np.zeros((R, gamma))
+    rc = lib().orc_cstar(R, gamma, V, _ptr(tgt), _ptr(_i32(row_off)), _ptr(_i32(ell)), _ptr(x),
+                         float(target_temp), _ptr(U), gamma * V, _ptr(A), _ptr(Ct), A.shape[2],
+                         _ptr(_i32(x0)), _ptr(_f32(draft_temp)), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_cstar failed ({rc})")
+    return out
+
+
+def calibration(c, ell, accept_len, count, sum_c, sum_acc):
+    """Fold one round's tested positions into the reliability diagram (tables
+    updated IN PLACE: count int64, sum_c f64, sum_acc int64, [n_bins] each);
+    returns (ece, bad)."""
+    c = _f64(c)
+    R, gamma = c.shape
+    assert count.dtype == np.int64 and sum_acc.dtype == np.int64 and sum_c.dtype == np.float64
+    ece = ctypes.c_double()
+    bad = ctypes.c_int()
+    rc = lib().orc_calibration(R, gamma, _ptr(c), _ptr(_i32(ell)), _ptr(_i32(accept_len)),
+                               count.size, _ptr(count), _ptr(sum_c), _ptr(sum_acc),
+                               ctypes.byref(ece), ctypes.byref(bad))
+    if rc != 0:
+        raise ValueError(f"orc_calibration failed ({rc})")
+    return ece.value, bad.value

@@ -536,5 +536,90 @@ int orc_accept_stats(int R, int gamma, const int32_t* ell, const int32_t* accept
   return 0;
 }
 
+// ------------------------------------------------- calibration diagnostics ---
+// [DSpark] "2.1 置信度头": the supervision target of the confidence head is the
+// acceptance probability of the draft distribution against the target one,
+// c* = 1 - (1/2) ||p - q||_1 = sum_v min(p_v, q_v).  For every verified draft
+// row (r, j), j = 1..l_r: p = softmax(L / target_temp) of target row
+// row_off[r] + j - 1 and q = softmax(z) of the draft logits of (r, j) given
+// x_{j-1} (x_0 for j = 1).  c_star [R, gamma] receives it; positions past l_r
+// get NaN (no target row exists for them).
+int orc_cstar(int R, int gamma, int V, const float* tgt, const int32_t* row_off,
+              const int32_t* ell, const int32_t* x, double target_temp, const float* U,
+              int64_t U_rstride, const float* A, const float* Ct, int r, const int32_t* x0,
+              const float* draft_temp, double* c_star) {
+  if (R < 0 || gamma <= 0 || V <= 0 || r <= 0 || !(target_temp > 0.0)) return -1;
+  std::vector<double> zt((size_t)V), zq;
+  for (int req = 0; req < R; ++req) {
+    const int l = ell[req];
+    if (l < 0 || l > gamma) return -2;
+    for (int j = 1; j <= gamma; ++j) {
+      double& out = c_star[(size_t)req * gamma + (j - 1)];
+      if (j > l) {
+        out = std::numeric_limits<double>::quiet_NaN();
+        continue;
+      }
+      const float* row = tgt + (size_t)(row_off[req] + j - 1) * V;
+      for (int v = 0; v < V; ++v) zt[(size_t)v] = (double)row[v] / target_temp;
+      const int xp = (j == 1) ? x0[req] : x[(size_t)req * gamma + (j - 2)];
+      draft_logits(V, r, U + (size_t)req * U_rstride + (size_t)(j - 1) * V,
+                   A + (size_t)(j - 1) * V * r, Ct + (size_t)(j - 1) * V * r, xp,
+                   (double)draft_temp[j - 1], zq);
+      out = orc_accept_prob(V, zt.data(), zq.data());
+    }
+  }
+  return 0;
+}
+
+// [DSpark] Figure 6 and "2.1 置信度头" (sequential temperature scaling): the
+// confidences are judged on a reliability diagram and by the expected
+// calibration error against realised acceptance.  A round's tested positions
+// are j = 1..min(l_r, accept_len_r + 1) of every request (the positions the
+// verifier actually ruled on); position j counts as accepted iff
+// j <= accept_len_r.  Each goes to bin b = min(floor(c_{r,j} * n_bins),
+// n_bins - 1) of the equal-width diagram over [0, 1]: count_b += 1,
+// sum_c_b += c, sum_acc_b += accepted.  The tables accumulate over calls.
+// ECE = (1 / N) sum_b |sum_acc_b - sum_c_b| with N = sum_b count_b (NaN if 0),
+// which is sum_b (n_b / N) |acc_b - conf_b| written without the divisions.
+// Requests with l_r or accept_len_r out of range, and confidences outside
+// [0, 1] or NaN, are skipped and counted in *bad.
+int orc_calibration(int R, int gamma, const double* c, const int32_t* ell,
+                    const int32_t* accept_len, int n_bins, int64_t* count, double* sum_c,
+                    int64_t* sum_acc, double* ece, int* bad) {
+  if (R < 0 || gamma <= 0 || n_bins <= 0) return -1;
+  int nbad = 0;
+  for (int req = 0; req < R; ++req) {
+    const int l = ell[req], acc = accept_len[req];
+    if (l < 0 || l > gamma || acc < 0 || acc > l) {
+      ++nbad;
+      continue;
+    }
+    const int tested = std::min(l, acc + 1);
+    for (int j = 1; j <= tested; ++j) {
+      const double cj = c[(size_t)req * gamma + (j - 1)];
+      if (!(cj >= 0.0 && cj <= 1.0)) {
+        ++nbad;
+        continue;
+      }
+      const int b = std::min((int)std::floor(cj * (double)n_bins), n_bins - 1);
+      count[b] += 1;
+      sum_c[b] += cj;
+      sum_acc[b] += (j <= acc) ? 1 : 0;
+    }
+  }
+  if (ece) {
+    int64_t N = 0;
+    double dev = 0.0;
+    for (int b = 0; b < n_bins; ++b) {
+      N += count[b];
+      dev += std::fabs((double)sum_acc[b] - sum_c[b]);
+    }
+    *ece = (N > 0) ? dev / (double)N : std::numeric_limits<double>::quiet_NaN();
+  }
+  if (bad) *bad = nbad;
+  return 0;
+}
+
 }  // extern "C"
+
 
