@@ -50,6 +50,9 @@ def _args():
                    help="survival threshold of --sched-mode threshold")
     p.add_argument("--accept-stats", action="store_true",
                    help="fold every round into the per-length acceptance EMA table")
+    p.add_argument("--calibration", action="store_true",
+                   help="also compute c* = sum min(p, q) of every verified row and fold the "
+                        "round into the reliability diagram (ECE)")
     return p.parse_args()
 
 
@@ -280,6 +283,7 @@ def main():
         acc_tab = {"ema": torch.zeros(1, G, dtype=torch.float64, device=dev),
                    "count": torch.zeros(1, G, dtype=torch.int64, device=dev),
                    "estimate": torch.zeros(G, dtype=torch.float64, device=dev)}
+    calib = vs.calibration_tables(10, dev) if args.calibration and not greedy else None
     stream = torch.cuda.current_stream()
     nev = max(1, args.steps)
     ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
@@ -304,12 +308,14 @@ def main():
             ev["s1"][i].record(stream)
         v = vs.verify(vs.VERIFY_SAMPLE, g["tgt"].view(-1, V), g["tgt_row_off"], s["ell"], d["x"],
                       seed, q_tok=d["q_tok"], lse_q=d["lse_q"], draft=din,
-                      request_id_base=rid_base, out=bufs.get("verify"),
-                      workspace=bufs["ws_verify"])
+                      request_id_base=rid_base, want_cstar=calib is not None,
+                      out=bufs.get("verify"), workspace=bufs["ws_verify"])
         bufs["verify"] = v
         if acc_tab is not None:
             vs.accept_stats(s["ell"], v["accept_len"], acc_tab["ema"], acc_tab["count"], 0, 0.1,
                             estimate=acc_tab["estimate"])
+        if calib is not None:
+            vs.calibration(d["c"], s["ell"], v["accept_len"], calib)
         if timed:
             ev["v1"][i].record(stream)
             stats_hist[i].copy_(s["stats"], non_blocking=True)
@@ -364,7 +370,7 @@ def main():
         kernel = "draft_step (one launch per position k)"
         # per round: gamma draft steps, confidence, schedule, verify rows,
         # fused residual, residual fallback (gated, exits at once when unused)
-        launches = G + 5 + (1 if acc_tab is not None else 0)
+        launches = G + 5 + (1 if acc_tab is not None else 0) + (3 if calib is not None else 0)
     achieved = per_launch / (dur_ms / 1000.0) / 1e9
     traffic = None if greedy else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
@@ -381,11 +387,14 @@ def main():
                        "factors": str(wl.fac_dtype).replace("torch.", ""),
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}",
-                       **_sched_config(wl), **({"accept_stats": True} if acc_tab is not None
-                                               else {})},
+                       **_sched_config(wl),
+                       **({"accept_stats": True} if acc_tab is not None else {}),
+                       **({"calibration": True} if calib is not None else {})},
             "stage_ms_per_step": {k: round(v / args.steps, 4) for k, v in stage_ms.items()},
             "mean_verify_rows": B_sum / args.steps,
             "roofline": roofline, "gpu_launches": launches * args.steps, "clocks": clk}
+    if calib is not None:
+        line["ece"] = float(calib["ece"].item())
 
     # ----------------------------------------------------- e2e (rank 0) ----
     if rank == 0 and not args.no_e2e and not greedy:

@@ -237,6 +237,41 @@ typedef struct spec_accept_stats_args {
 
 int spec_accept_stats(const spec_accept_stats_args *args, spec_stream_t stream);
 
+/* ---------------------------------------------------------- calibration -
+ * DSpark summary, Figure 6 and "2.1 置信度头": the confidences c_{r,j} (after
+ * sequential temperature scaling) are judged by a reliability diagram and the
+ * expected calibration error (ECE) against realised acceptance.  One call
+ * folds a verified round into an equal-width diagram of n_bins bins over
+ * [0, 1] (one thread block, no workspace):
+ *   tested positions of request r: j = 1..min(l_r, accept_len_r + 1), the
+ *   ones the verifier ruled on; position j counts as accepted iff
+ *   j <= accept_len_r;  bin b = min(floor(c * n_bins), n_bins - 1) (fp64);
+ *   count[b] += 1, sum_c[b] += c, sum_acc[b] += accepted.
+ *   ece (nullable) = sum_b |sum_acc_b - sum_c_b| / sum_b count_b after the
+ *   update, i.e. sum_b (n_b / N) |acc_b - conf_b|; NaN when N = 0.
+ *   c [R, gamma] f32 device (spec_draft_sample's c);  ell, accept_len [R] int32
+ *   count, sum_acc [n_bins] int64 and sum_c [n_bins] f64 device, in/out (zero
+ *   them before the first call);  ece [1] f64 device;  1 <= n_bins <= 1024
+ * Counts are exact; sum_c adds in an unspecified order (fp64 rounding only).
+ * An ell outside [0, gamma] or accept_len outside [0, ell] sets
+ * SPEC_STATUS_BAD_ELL, a c outside [0, 1] or NaN SPEC_STATUS_BAD_SURVIVAL; the
+ * entry is skipped.
+ */
+typedef struct spec_calibration_args {
+  int R, gamma;
+  const float *c;
+  const int32_t *ell;
+  const int32_t *accept_len;
+  int n_bins;
+  int64_t *count;
+  double *sum_c;
+  int64_t *sum_acc;
+  double *ece;
+  uint32_t *status;
+} spec_calibration_args;
+
+int spec_calibration(const spec_calibration_args *args, spec_stream_t stream);
+
 /* ----------------------------------------------------------------- verify -
  * History article, "1.1运行机制" (rejection sampling): accept x_j with
  * probability min(1, p(x_j) / q(x_j)) -- the test is u < p/q with u from the
@@ -263,6 +298,11 @@ int spec_accept_stats(const spec_accept_stats_args *args, spec_stream_t stream);
  * Optional (nullable): p_tok [R, gamma] = p(x_j) for j <= l_r (others 0),
  * lse_t [R, gamma + 1] = log sum exp(L_j / target_temp) of the rows read
  * (sample mode; others 0).
+ * c_star [R, gamma] f32 (nullable; sample mode only, else SPEC_ERR_INVALID_ARG):
+ * the calibration target of the confidence head, DSpark summary "2.1 置信度头":
+ * c* = 1 - TV(p, q) = sum_v min(p_v, q_v) for every verified draft row
+ * j <= l_r (q recomputed from the draft arguments), NaN past l_r.  A
+ * diagnostic: it costs one more pass over the admitted target and draft rows.
  */
 typedef struct spec_verify_args {
   int mode;
@@ -285,6 +325,7 @@ typedef struct spec_verify_args {
   void *workspace;
   size_t workspace_bytes;
   uint32_t *status;
+  float *c_star;
 } spec_verify_args;
 
 int spec_verify(const spec_verify_args *args, uint64_t seed, spec_stream_t stream);

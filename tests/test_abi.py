@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(spec):
     names = _declared_functions()
     assert {"spec_draft_sample", "spec_schedule", "spec_verify", "spec_workspace_bytes",
             "spec_error_string", "spec_stream_uniforms", "spec_version",
-            "spec_accept_stats"} <= set(names)
+            "spec_accept_stats", "spec_calibration"} <= set(names)
     lib = spec.lib()
     for n in names:
         assert hasattr(lib, n), n
@@ -51,10 +51,13 @@ def test_struct_layout_matches_c(spec, tmp_path):
         'printf("spec_sched_args %zu\\n", sizeof(spec_sched_args));\n'
         'printf("spec_verify_args %zu\\n", sizeof(spec_verify_args));\n'
         'printf("spec_accept_stats_args %zu\\n", sizeof(spec_accept_stats_args));\n'
+        'printf("spec_calibration_args %zu\\n", sizeof(spec_calibration_args));\n'
         "P(spec_draft_args, status) P(spec_draft_args, workspace_bytes) P(spec_draft_args, U)\n"
         "P(spec_sched_args, b_lo) P(spec_sched_args, stats) P(spec_sched_args, status)\n"
         "P(spec_sched_args, threshold) P(spec_accept_stats_args, beta)\n"
         "P(spec_accept_stats_args, ema) P(spec_accept_stats_args, status)\n"
+        "P(spec_verify_args, c_star) P(spec_calibration_args, n_bins)\n"
+        "P(spec_calibration_args, ece) P(spec_calibration_args, status)\n"
         "P(spec_verify_args, target_temp) P(spec_verify_args, draft) P(spec_verify_args, status)\n"
         "return 0;}\n")
     exe = tmp_path / "layout"
@@ -66,6 +69,7 @@ def test_struct_layout_matches_c(spec, tmp_path):
     assert int(got["spec_sched_args"]) == ctypes.sizeof(spec.SchedArgs)
     assert int(got["spec_verify_args"]) == ctypes.sizeof(spec.VerifyArgs)
     assert int(got["spec_accept_stats_args"]) == ctypes.sizeof(spec.AcceptStatsArgs)
+    assert int(got["spec_calibration_args"]) == ctypes.sizeof(spec.CalibrationArgs)
     for key, (cls, field) in {"spec_draft_args.status": (spec.DraftArgs, "status"),
                               "spec_draft_args.workspace_bytes": (spec.DraftArgs, "workspace_bytes"),
                               "spec_draft_args.U": (spec.DraftArgs, "U"),
@@ -76,6 +80,10 @@ def test_struct_layout_matches_c(spec, tmp_path):
                               "spec_accept_stats_args.beta": (spec.AcceptStatsArgs, "beta"),
                               "spec_accept_stats_args.ema": (spec.AcceptStatsArgs, "ema"),
                               "spec_accept_stats_args.status": (spec.AcceptStatsArgs, "status"),
+                              "spec_verify_args.c_star": (spec.VerifyArgs, "c_star"),
+                              "spec_calibration_args.n_bins": (spec.CalibrationArgs, "n_bins"),
+                              "spec_calibration_args.ece": (spec.CalibrationArgs, "ece"),
+                              "spec_calibration_args.status": (spec.CalibrationArgs, "status"),
                               "spec_verify_args.target_temp": (spec.VerifyArgs, "target_temp"),
                               "spec_verify_args.draft": (spec.VerifyArgs, "draft"),
                               "spec_verify_args.status": (spec.VerifyArgs, "status")}.items():
@@ -136,12 +144,23 @@ def test_host_side_rejections_launch_nothing(spec):
     assert lib.spec_accept_stats(ctypes.byref(st), None) == spec.SPEC_ERR_UNSUPPORTED
     st.gamma, st.ema = 4, ctypes.c_void_p(260)
     assert lib.spec_accept_stats(ctypes.byref(st), None) == spec.SPEC_ERR_ALIGNMENT
+    ca = spec.CalibrationArgs()
+    assert lib.spec_calibration(None, None) == spec.SPEC_ERR_INVALID_ARG
+    ca.R, ca.gamma, ca.n_bins = 4, 4, 0
+    ca.c = ca.ell = ca.accept_len = ca.count = ca.sum_c = ca.sum_acc = ctypes.c_void_p(256)
+    assert lib.spec_calibration(ctypes.byref(ca), None) == spec.SPEC_ERR_INVALID_ARG
+    ca.n_bins = 2000
+    assert lib.spec_calibration(ctypes.byref(ca), None) == spec.SPEC_ERR_UNSUPPORTED
+    ca.n_bins, ca.sum_c = 10, ctypes.c_void_p(260)
+    assert lib.spec_calibration(ctypes.byref(ca), None) == spec.SPEC_ERR_ALIGNMENT
     v = spec.VerifyArgs()
     v.mode, v.R, v.gamma, v.V = 0, 2, 2, 10
     v.tgt = v.tgt_row_off = v.ell = v.x = v.accept_len = v.out_tok = v.n_out = ctypes.c_void_p(256)
     v.target_temp = 1.0
     assert lib.spec_verify(ctypes.byref(v), 0, None) == spec.SPEC_ERR_INVALID_ARG  # no draft
     v.mode = 7
+    assert lib.spec_verify(ctypes.byref(v), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    v.mode, v.c_star = 1, ctypes.c_void_p(256)  # c* needs sample mode
     assert lib.spec_verify(ctypes.byref(v), 0, None) == spec.SPEC_ERR_INVALID_ARG
     assert lib.spec_stream_uniforms(0, 1, 0, 0, 0, None, None, None) == spec.SPEC_ERR_INVALID_ARG
 

@@ -1,5 +1,6 @@
-"""CUDA path versus the oracle for the scheduler's static-threshold mode and the
-acceptance statistics, through the C ABI (needs a GB300).
+"""CUDA path versus the oracle for the scheduler's static-threshold mode, the
+acceptance statistics and the calibration diagnostics, through the C ABI
+(needs a GB300).
 
 * Threshold mode (DSpark summary, comparison table: SpecDec++; Figure 5): the
   admitted set, row offsets and n, B are bit-exact against the oracle at the
@@ -9,6 +10,10 @@ acceptance statistics, through the C ABI (needs a GB300).
   of the EMA table, the counts and the interpolated estimates are bit-exact
   (every step is one correctly rounded fp64 operation on both sides) over a
   sequence of rounds in several classes, with bad entries flagged.
+* Calibration (DSpark summary, "2.1 置信度头" and Figure 6): c* = sum min(p, q)
+  of every verified row within the probability tolerance, on the generic and
+  the tensor-core passes, small and at full size; the reliability diagram's
+  counts exactly and its sums and ECE to fp64 rounding.
 """
 import numpy as np
 import pytest
@@ -129,3 +134,112 @@ def test_accept_stats_bad_entries_set_status():
     assert int(status.item()) & vs.STATUS_BAD_ELL
     assert np.array_equal(to_np(cnt_g), cnt_o)
     assert np.array_equal(to_np(ema_g), ema_o)
+
+
+# ------------------------------------------------------- calibration (c*) ----
+from parity import PROB_TOL  # noqa: E402
+
+CSTAR_CASES = {
+    "tiny": synth.WORKLOADS["tiny"],                                          # generic, fp32 factors
+    "c3_small": synth.WORKLOADS["c3"].scaled(R=12, gamma=8, V=8195, d=128),  # generic, ragged V
+    "tc_c5_small": synth.WORKLOADS["c5"].scaled(R=8, gamma=6, V=12004, d=200),
+    "tc_c3_R130": synth.WORKLOADS["c3"].scaled(R=130, gamma=3, V=4136, d=64),  # two row tiles
+}
+
+
+def _cstar_oracle(inp, reqs, x, ell, draft_temp):
+    """The oracle's c* of the sampled requests, fed the GPU's tokens and l_r
+    (tensors are indexed where they live, then copied)."""
+    V = inp["U"].shape[-1]
+    G = x.shape[1]
+    reqs = list(reqs)
+    idx = torch.tensor(reqs, device=inp["U"].device)
+    tgt = inp["tgt"].view(-1, V)
+    off = to_np(inp["tgt_row_off"])
+    rows = torch.stack([tgt[int(off[r]) + j] for r in reqs for j in range(G + 1)])
+    sub_off = (np.arange(len(reqs)) * (G + 1)).astype(np.int32)
+    return oracle.cstar(to_np(rows), sub_off, ell[reqs], x[reqs], 1.0, to_np(inp["U"][idx]),
+                        to_np(inp["A"]), to_np(inp["Ct"]), to_np(inp["x0"][idx]), draft_temp)
+
+
+def _cstar_run(g, wl, seed, K):
+    din = synth.draft_inputs(g)
+    d = vs.draft_sample(din, seed)
+    s = vs.schedule(d["a"], g["sps"], g["b_lo"], g["b_step"], K, vs.SCHED_THRESHOLD, threshold=0.0)
+    v = vs.verify(vs.VERIFY_SAMPLE, g["tgt"].view(-1, wl.V), g["tgt_row_off"], s["ell"], d["x"],
+                  seed, q_tok=d["q_tok"], lse_q=d["lse_q"], draft=din, want_cstar=True)
+    torch.cuda.synchronize()
+    return d, s, v
+
+
+def _check_cstar(got, want):
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert fin.any()
+    err = np.abs(got[fin] - want[fin]).max()
+    assert err < PROB_TOL, err
+    assert (got[fin] > 0).all() and (got[fin] <= 1 + 1e-5).all()
+
+
+@pytest.mark.parametrize("name", list(CSTAR_CASES))
+def test_cstar_parity_small(name):
+    wl = CSTAR_CASES[name]
+    inp = synth.make_inputs(wl, "cpu")
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    K = max(1, (wl.R * wl.gamma * 2) // 3)  # a cap that binds: some rows past l_r
+    d, s, v = _cstar_run(g, wl, 31, K)
+    ell, x = to_np(s["ell"]), to_np(d["x"])
+    assert ell.sum() == min(K, wl.R * wl.gamma)
+    want = _cstar_oracle(inp, range(wl.R), x, ell, to_np(inp["draft_temp"]))
+    _check_cstar(to_np(v["c_star"]), want)
+
+
+def test_cstar_full_size_c5_sampled():
+    wl = synth.WORKLOADS["c5"]
+    g = synth.make_inputs(wl, DEV, seed=wl.seed)
+    d, s, v = _cstar_run(g, wl, 4243, wl.K)
+    ell, x = to_np(s["ell"]), to_np(d["x"])
+    order = np.argsort(-ell, kind="stable")
+    reqs = sorted({int(order[0]), int(order[1]), 0, wl.R - 1})
+    want = _cstar_oracle(g, reqs, x, ell, to_np(g["draft_temp"]))
+    _check_cstar(to_np(v["c_star"])[reqs], want)
+    assert np.isnan(to_np(v["c_star"])[ell == 0]).all()
+
+
+def test_calibration_parity_and_accumulation():
+    rng = np.random.default_rng(21)
+    n_bins = 10
+    cnt_o, sc_o, sa_o = np.zeros(n_bins, np.int64), np.zeros(n_bins), np.zeros(n_bins, np.int64)
+    tab = vs.calibration_tables(n_bins, DEV)
+    for rnd in range(6):
+        R, G = 512, 11
+        c = rng.uniform(0, 1, (R, G)).astype(np.float32)
+        c[0, 0], c[1, 0], c[2, 0] = 0.0, 1.0, 0.5  # bin edges
+        ell, acc = _round_inputs(rng, R, G)
+        ece_o, bad = oracle.calibration(c.astype(np.float64), ell, acc, cnt_o, sc_o, sa_o)
+        assert bad == 0
+        vs.calibration(torch.tensor(c, device=DEV), torch.tensor(ell, device=DEV),
+                       torch.tensor(acc, device=DEV), tab)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(tab["count"]), cnt_o)
+        assert np.array_equal(to_np(tab["sum_acc"]), sa_o)
+        assert np.allclose(to_np(tab["sum_c"]), sc_o, rtol=1e-12, atol=0)
+        assert abs(float(tab["ece"].item()) - ece_o) <= 1e-12 * max(1.0, ece_o)
+
+
+def test_calibration_bad_entries_and_empty():
+    tab = vs.calibration_tables(4, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    c = torch.tensor([[0.5, float("nan")], [0.5, 0.5], [1.5, 0.5]], device=DEV)
+    ell = torch.tensor([2, 3, 1], dtype=torch.int32, device=DEV)
+    acc = torch.tensor([2, 0, 0], dtype=torch.int32, device=DEV)
+    vs.calibration(c, ell, acc, tab, status=status)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st & vs.STATUS_BAD_ELL and st & vs.STATUS_BAD_SURVIVAL
+    assert int(tab["count"].sum()) == 1
+    empty = vs.calibration_tables(4, DEV)
+    vs.calibration(torch.zeros((0, 2), device=DEV), torch.zeros(0, dtype=torch.int32, device=DEV),
+                   torch.zeros(0, dtype=torch.int32, device=DEV), empty)
+    torch.cuda.synchronize()
+    assert np.isnan(float(empty["ece"].item()))

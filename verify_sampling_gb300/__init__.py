@@ -62,6 +62,12 @@ class AcceptStatsArgs(ctypes.Structure):
                 ("status", _P)]
 
 
+class CalibrationArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int), ("gamma", ctypes.c_int), ("c", _P), ("ell", _P),
+                ("accept_len", _P), ("n_bins", ctypes.c_int), ("count", _P), ("sum_c", _P),
+                ("sum_acc", _P), ("ece", _P), ("status", _P)]
+
+
 class VerifyArgs(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("R", ctypes.c_int), ("gamma", ctypes.c_int),
                 ("V", ctypes.c_int), ("tgt_dtype", ctypes.c_int),
@@ -69,7 +75,8 @@ class VerifyArgs(ctypes.Structure):
                 ("ell", _P), ("x", _P), ("q_tok", _P), ("lse_q", _P),
                 ("target_temp", ctypes.c_float), ("draft", ctypes.POINTER(DraftArgs)),
                 ("accept_len", _P), ("out_tok", _P), ("n_out", _P), ("p_tok", _P), ("lse_t", _P),
-                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("status", _P)]
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("status", _P),
+                ("c_star", _P)]
 
 
 class SpecError(RuntimeError):
@@ -91,7 +98,9 @@ def lib() -> ctypes.CDLL:
         L.spec_schedule.argtypes = [ctypes.POINTER(SchedArgs), _P]
         L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_uint64, _P]
         L.spec_accept_stats.argtypes = [ctypes.POINTER(AcceptStatsArgs), _P]
-        for f in (L.spec_draft_sample, L.spec_schedule, L.spec_verify, L.spec_accept_stats):
+        L.spec_calibration.argtypes = [ctypes.POINTER(CalibrationArgs), _P]
+        for f in (L.spec_draft_sample, L.spec_schedule, L.spec_verify, L.spec_accept_stats,
+                  L.spec_calibration):
             f.restype = ctypes.c_int
         L.spec_workspace_bytes.argtypes = [ctypes.c_int] * 5
         L.spec_workspace_bytes.restype = ctypes.c_size_t
@@ -266,6 +275,7 @@ def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.T
            x: torch.Tensor, seed: int, *, q_tok: Optional[torch.Tensor] = None,
            lse_q: Optional[torch.Tensor] = None, target_temp: float = 1.0,
            draft: Optional[DraftInputs] = None, request_id_base: int = 0, want_p: bool = False,
+           want_cstar: bool = False,
            out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
            status: Optional[torch.Tensor] = None, stream=None) -> dict:
     """spec_verify: accept lengths and emitted tokens (sample or greedy mode)."""
@@ -278,6 +288,8 @@ def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.T
         "accept_len": torch.empty(R, dtype=torch.int32, device=dev),
         "out_tok": torch.empty(R, gamma + 1, dtype=torch.int32, device=dev),
         "n_out": torch.empty(R, dtype=torch.int32, device=dev)}
+    if want_cstar and "c_star" not in outs:
+        outs["c_star"] = torch.empty(R, gamma, dtype=torch.float32, device=dev)
     if want_p and "p_tok" not in outs:
         outs["p_tok"] = torch.empty(R, gamma, dtype=torch.float32, device=dev)
         outs["lse_t"] = torch.empty(R, gamma + 1, dtype=torch.float32, device=dev)
@@ -296,6 +308,7 @@ def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.T
     v.accept_len, v.out_tok, v.n_out = _ptr(outs["accept_len"]), _ptr(outs["out_tok"]), \
         _ptr(outs["n_out"])
     v.p_tok, v.lse_t = _ptr(outs.get("p_tok")), _ptr(outs.get("lse_t"))
+    v.c_star = _ptr(outs.get("c_star"))
     v.workspace = _ptr(ws)
     v.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     v.status = _ptr(status)
@@ -333,6 +346,40 @@ def accept_stats(ell: torch.Tensor, accept_len: torch.Tensor, ema: torch.Tensor,
     a.status = _ptr(status)
     _check(lib().spec_accept_stats(ctypes.byref(a), _stream_handle(stream)), "spec_accept_stats")
     return estimate
+
+
+def calibration(c: torch.Tensor, ell: torch.Tensor, accept_len: torch.Tensor,
+                tables: dict, *, status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """spec_calibration: fold one verified round into the reliability diagram
+    ``tables`` = {"count": int64 [n_bins], "sum_c": float64 [n_bins],
+    "sum_acc": int64 [n_bins], "ece": float64 [1] (optional)}, updated in place
+    on the device (see ``calibration_tables``)."""
+    c, ell, accept_len = _dev(c, "c"), _dev(ell, "ell"), _dev(accept_len, "accept_len")
+    if c.dtype != torch.float32 or c.dim() != 2:
+        raise TypeError("c must be float32 [R, gamma]")
+    if ell.dtype != torch.int32 or accept_len.dtype != torch.int32:
+        raise TypeError("ell and accept_len must be int32")
+    cnt, sc, sa = (_dev(tables[k], k) for k in ("count", "sum_c", "sum_acc"))
+    if cnt.dtype != torch.int64 or sa.dtype != torch.int64 or sc.dtype != torch.float64 or \
+            not (cnt.numel() == sc.numel() == sa.numel()):
+        raise TypeError("count / sum_acc int64 and sum_c float64, all [n_bins]")
+    a = CalibrationArgs()
+    a.R, a.gamma = c.shape
+    a.c, a.ell, a.accept_len = _ptr(c), _ptr(ell), _ptr(accept_len)
+    a.n_bins = cnt.numel()
+    a.count, a.sum_c, a.sum_acc = _ptr(cnt), _ptr(sc), _ptr(sa)
+    a.ece = _ptr(tables.get("ece"))
+    a.status = _ptr(status)
+    _check(lib().spec_calibration(ctypes.byref(a), _stream_handle(stream)), "spec_calibration")
+    return tables
+
+
+def calibration_tables(n_bins: int, device) -> dict:
+    """Zeroed device tables for ``calibration``."""
+    return {"count": torch.zeros(n_bins, dtype=torch.int64, device=device),
+            "sum_c": torch.zeros(n_bins, dtype=torch.float64, device=device),
+            "sum_acc": torch.zeros(n_bins, dtype=torch.int64, device=device),
+            "ece": torch.zeros(1, dtype=torch.float64, device=device)}
 
 
 # -------------------------------------------------------------------- round --

@@ -243,6 +243,8 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   if (!a.tgt || !a.tgt_row_off || !a.ell || !a.x || !a.accept_len || !a.out_tok || !a.n_out)
     return SPEC_ERR_INVALID_ARG;
   const bool sample = a.mode == SPEC_VERIFY_SAMPLE;
+  if (a.c_star && !sample) return SPEC_ERR_INVALID_ARG;  // c* needs the draft rows
+  if (!aligned(a.c_star, 4)) return SPEC_ERR_ALIGNMENT;
   int fac_dtype = SPEC_BF16, logit_dtype = SPEC_BF16, rank = 1;
   if (sample) {
     if (!a.q_tok || !a.lse_q || !a.draft || !(a.target_temp > 0.f) || !(a.target_temp < 1e30f))
@@ -299,6 +301,7 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   p.n_out = a.n_out;
   p.p_tok = a.p_tok;
   p.lse_t = a.lse_t;
+  p.c_star = a.c_star;
   p.status = a.status;
   {
     int dev = 0, major = 0, sms = 0;
@@ -353,5 +356,34 @@ int spec_accept_stats(const spec_accept_stats_args* args, spec_stream_t stream) 
              : SPEC_ERR_CUDA;
 }
 
+int spec_calibration(const spec_calibration_args* args, spec_stream_t stream) {
+  if (!args) return SPEC_ERR_INVALID_ARG;
+  const spec_calibration_args& a = *args;
+  if (a.R < 0 || a.gamma < 1 || a.n_bins < 1) return SPEC_ERR_INVALID_ARG;
+  if (!a.count || !a.sum_c || !a.sum_acc || (a.R > 0 && (!a.c || !a.ell || !a.accept_len)))
+    return SPEC_ERR_INVALID_ARG;
+  if (a.n_bins > kCalibrationMaxBins) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned(a.c, 4) || !aligned(a.ell, 4) || !aligned(a.accept_len, 4) ||
+      !aligned(a.count, 8) || !aligned(a.sum_c, 8) || !aligned(a.sum_acc, 8) ||
+      !aligned(a.ece, 8) || !aligned(a.status, 4))
+    return SPEC_ERR_ALIGNMENT;
+  CalibrationParams p{};
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.n_bins = a.n_bins;
+  p.c = a.c;
+  p.ell = a.ell;
+  p.accept_len = a.accept_len;
+  p.count = reinterpret_cast<long long*>(a.count);
+  p.sum_c = a.sum_c;
+  p.sum_acc = reinterpret_cast<long long*>(a.sum_acc);
+  p.ece = a.ece;
+  p.status = a.status;
+  return launch_calibration(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
 }  // extern "C"
+
 

@@ -12,6 +12,10 @@
 // p_v = 2^(L_v log2e / T_t - m_t) / s_t uses the softmax reference/sum of the target row
 // that the verify row pass stored.
 //
+// The same pass, instantiated with kCStar, sums min(p_v, q_v) over the
+// vocabulary for every verified draft row instead (DSpark summary, "2.1
+// 置信度头": c* = 1 - TV(p, q), the confidence head's calibration target).
+//
 // Layout and pipelines follow the fused draft kernel (fused_tc.cuh): one CTA
 // per SM, 16 epilogue warps, a TMA producer warp and an MMA warp.  Rows are
 // gathered: the producer loads one 128-byte row box per request and operand
@@ -77,7 +81,7 @@ constexpr uint32_t round1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 using namespace fused;
 
 // 576 threads per CTA leave at most 96 registers per thread.
-template <typename TT, typename TL, int KC>
+template <typename TT, typename TL, int KC, bool kCStar>
 __global__ void __launch_bounds__(kThreads, 1)
     resid_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const TL* __restrict__ U,
                     const TT* __restrict__ tgt, ResidTCParams p) {
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per-request bound).  Requests with no positive residual anywhere are
     // flagged by the final combine and served by the fallback kernel.
     WRace rres = wrace_empty();
+    float csum = 0.f;  // kCStar: this thread's sum of min(p, q)
     float c_res = CUDART_INF_F;
     uint32_t shared_key = 0;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
       if (abort_flag) break;
       const uint32_t shared_now = shared_key;
-      if (valid) shared_key = __ldcg(row_best);
+      if (!kCStar && valid) shared_key = __ldcg(row_best);
       if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
           !tc::mbar_wait(&full_r[r.idx], r.phase, kWaitNs)) {
         fail();
@@ -324,6 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!valid) continue;
       const int colbase = (t_begin + t) * kNT + grp * 16;
+      if constexpr (kCStar) {
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (colbase + c < V) part += fminf(tc::ex2(fmaf(L[c], kt, nt)) * inv_s, qv[c]);
+        csum += part;
+        continue;
+      }
       const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -358,6 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if constexpr (kCStar) {
+      // four column groups and every split add into the row's sum
+      if (valid && !abort_flag) atomicAdd(&p.c_star[rk1], csum);
+    } else {
     // merge the four column groups through the stage buffers
     WRace* grp_state = reinterpret_cast<WRace*>(sStage);  // [3][128]
     named_bar_sync(2, kEpiWarps * 32);
@@ -372,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.i0 = rres.idx;
       p.partials[((size_t)mt * 128 + row) * nsplit + split] = w;
     }
+    }
   }
 
   // ----------------------------------------------------------- teardown --
@@ -381,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  if (kCStar) return;
   if (!last_block_arrives(p.counters + mt, (unsigned)nsplit)) return;
 
   // Last CTA of this request tile: merge the splits, four threads per request.
@@ -417,7 +436,7 @@ size_t smem_bytes(int stages) {
 
 template <typename TT, typename TL, int KC>
 cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void* U, const void* Ct,
-                         int grid, cudaStream_t stream) {
+                         int grid, bool cstar, cudaStream_t stream) {
   ResidTCParams p = base;
   CUtensorMap tm_c;
   const uint64_t cdims[3] = {(uint64_t)p.rank, (uint64_t)p.V, (uint64_t)p.gamma};
@@ -428,7 +447,7 @@ cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void*
   const size_t smem = 227 * 1024 - 4096;
   if (smem_bytes<TT, TL, KC>(2) > smem) return cudaErrorInvalidValue;
   p.smem_bytes = (int)smem;
-  auto kern = resid_tc_kernel<TT, TL, KC>;
+  auto kern = cstar ? resid_tc_kernel<TT, TL, KC, true> : resid_tc_kernel<TT, TL, KC, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, smem, stream>>>(tm_c, static_cast<const TL*>(U), static_cast<const TT*>(tgt), p);
@@ -437,12 +456,12 @@ cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void*
 
 template <typename TT, typename TL>
 cudaError_t launch_kc(const ResidTCParams& p, const void* tgt, const void* U, const void* Ct,
-                      int grid, cudaStream_t stream) {
+                      int grid, bool cstar, cudaStream_t stream) {
   switch (p.rank / 64) {
-    case 1: return launch_typed<TT, TL, 1>(p, tgt, U, Ct, grid, stream);
-    case 2: return launch_typed<TT, TL, 2>(p, tgt, U, Ct, grid, stream);
-    case 3: return launch_typed<TT, TL, 3>(p, tgt, U, Ct, grid, stream);
-    case 4: return launch_typed<TT, TL, 4>(p, tgt, U, Ct, grid, stream);
+    case 1: return launch_typed<TT, TL, 1>(p, tgt, U, Ct, grid, cstar, stream);
+    case 2: return launch_typed<TT, TL, 2>(p, tgt, U, Ct, grid, cstar, stream);
+    case 3: return launch_typed<TT, TL, 3>(p, tgt, U, Ct, grid, cstar, stream);
+    case 4: return launch_typed<TT, TL, 4>(p, tgt, U, Ct, grid, cstar, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -459,13 +478,15 @@ bool resid_tc_supported(int tgt_dtype, int logit_dtype, int fac_dtype, int rank,
 }
 
 cudaError_t launch_resid_tc(const ResidTCParams& p, int tgt_dtype, int logit_dtype, const void* tgt,
-                            const void* U, const void* Ct, int grid, cudaStream_t stream) {
+                            const void* U, const void* Ct, int grid, bool cstar,
+                            cudaStream_t stream) {
   if (tgt_dtype == SPEC_F32) {
-    if (logit_dtype == SPEC_F32) return launch_kc<float, float>(p, tgt, U, Ct, grid, stream);
-    return launch_kc<float, __nv_bfloat16>(p, tgt, U, Ct, grid, stream);
+    if (logit_dtype == SPEC_F32) return launch_kc<float, float>(p, tgt, U, Ct, grid, cstar, stream);
+    return launch_kc<float, __nv_bfloat16>(p, tgt, U, Ct, grid, cstar, stream);
   }
-  if (logit_dtype == SPEC_F32) return launch_kc<__nv_bfloat16, float>(p, tgt, U, Ct, grid, stream);
-  return launch_kc<__nv_bfloat16, __nv_bfloat16>(p, tgt, U, Ct, grid, stream);
+  if (logit_dtype == SPEC_F32)
+    return launch_kc<__nv_bfloat16, float>(p, tgt, U, Ct, grid, cstar, stream);
+  return launch_kc<__nv_bfloat16, __nv_bfloat16>(p, tgt, U, Ct, grid, cstar, stream);
 }
 
 }  // namespace spec

@@ -25,6 +25,7 @@ struct ResidTCParams {
   unsigned* row_best;       // [R] shared race bounds, zero on entry
   int32_t* out_tok;         // [R, gamma + 1]
   int* fallback;            // [R] position whose residual was zero everywhere (0: none)
+  float* c_star;            // c* mode: [R, gamma] sums of min(p, q), zero on entry
   uint32_t* status;
 };
 
@@ -34,7 +35,10 @@ inline int resid_tc_max_mtiles(int R, int gamma) { return (R + 127) / 128 + gamm
 bool resid_tc_supported(int tgt_dtype, int logit_dtype, int fac_dtype, int rank, int V,
                         const void* tgt, const void* U, const void* A, const void* Ct);
 
+// cstar = false: the residual resample of the rows in res_list.  cstar = true:
+// sum_v min(p_v, q_v) of every row in res_list, added into c_star.
 cudaError_t launch_resid_tc(const ResidTCParams& p, int tgt_dtype, int logit_dtype, const void* tgt,
-                            const void* U, const void* Ct, int grid, cudaStream_t stream);
+                            const void* U, const void* Ct, int grid, bool cstar,
+                            cudaStream_t stream);
 
 }  // namespace spec

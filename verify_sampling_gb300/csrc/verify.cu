@@ -14,6 +14,10 @@
 // the request (first rejection, outputs).
 // Kernel 2 (residual): grid (nsplit, R); only requests with a rejection work:
 // they recompute q at j* and draw the residual Gumbel-max.
+// Optional diagnostic (c_star): DSpark summary, "2.1 置信度头" -- the confidence
+// head's target c* = 1 - TV(p, q) = sum_v min(p_v, q_v) of every verified
+// draft row, from a plan of the rows per position and the tensor-core residual
+// pass in its summing form (or a generic FFMA kernel).
 #include "verify.cuh"
 
 #include "draft_tc.cuh"
@@ -691,6 +695,88 @@ __global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p
   }
 }
 
+// c* plan (one CTA): per position k, the requests with l_r >= k in request
+// order (res_list[k-1][.], res_num[k-1]), and c_star set to 0 on the verified
+// rows (the passes add into it) and NaN past l_r.
+__global__ void __launch_bounds__(kPlanThreads) cstar_plan_kernel(VerifyParams p) {
+  __shared__ int warp_sum[kPlanThreads / 32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.gamma;
+  for (int i = tid; i < p.R * G; i += kPlanThreads) {
+    int l = p.ell[i / G];
+    l = l < 0 ? 0 : (l > G ? G : l);
+    p.c_star[i] = (i % G) < l ? 0.f : __int_as_float(0x7fc00000);  // quiet NaN
+  }
+  for (int k = 1; k <= G; ++k) {
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int r0 = 0; r0 < p.R; r0 += kPlanThreads) {  // uniform trip count
+      const int r = r0 + tid;
+      int l = (r < p.R) ? p.ell[r] : 0;
+      l = l < 0 ? 0 : (l > G ? G : l);
+      const bool take = r < p.R && l >= k;
+      const unsigned bal = __ballot_sync(0xffffffffu, take);
+      if (lane == 0) warp_sum[warp] = __popc(bal);
+      __syncthreads();
+      int before = carry;
+      for (int w = 0; w < warp; ++w) before += warp_sum[w];
+      if (take) p.ws.res_list[(size_t)(k - 1) * p.R + before + __popc(bal & ((1u << lane) - 1u))] = r;
+      __syncthreads();
+      if (tid == kPlanThreads - 1) carry = before + __popc(bal);
+      __syncthreads();
+    }
+    if (tid == 0) p.ws.res_num[k - 1] = carry;
+    __syncthreads();
+  }
+}
+
+// Generic c* pass (any dtype, FFMA bias): grid (nsplit, R, gamma); block
+// (s, r, k) adds sum min(p_v, q_v) over its vocabulary slice of row (r, k),
+// k <= l_r, into c_star[r, k].
+template <typename TT, typename TL, typename TF>
+__global__ void __launch_bounds__(kVerifyThreads) cstar_kernel(VerifyParams p) {
+  __shared__ float arow[256];
+  __shared__ float red[kVerifyThreads / 32];
+  const int r = blockIdx.y, k = blockIdx.z + 1, split = blockIdx.x, nsplit = gridDim.x;
+  const int G = p.gamma, G1 = G + 1, V = p.V, rank = p.rank;
+  int l = p.ell[r];
+  l = l < 0 ? 0 : (l > G ? G : l);
+  if (k > l) return;  // uniform across the block
+  const size_t rj = (size_t)r * G1 + (k - 1);
+  const float m_t = p.ws.row_m[rj], inv_s_t = 1.0f / p.ws.row_s[rj];  // m_t in log2 units
+  const TT* L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, r, k) * (size_t)V;
+  int x_prev = (k == 1) ? p.x0[r] : p.x[(size_t)r * G + (k - 2)];
+  if (x_prev < 0 || x_prev >= V) x_prev = 0;
+  const TF* A = reinterpret_cast<const TF*>(p.A) + (size_t)(k - 1) * V * rank;
+  const TF* Ct = reinterpret_cast<const TF*>(p.Ct) + (size_t)(k - 1) * V * rank;
+  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(A, (size_t)x_prev * rank + i);
+  __syncthreads();
+  const TL* U = reinterpret_cast<const TL*>(p.U) + ((size_t)r * G + (k - 1)) * V;
+  const float inv_tq = 1.0f / p.draft_temp[k - 1];
+  const float lse_q = p.lse_q[(size_t)r * G + (k - 1)];
+  const float kt = p.inv_target_temp * fused::kLog2e;
+  const int per = (V + nsplit - 1) / nsplit;
+  const int v_begin = split * per, v_end = min(V, v_begin + per);
+  float sum = 0.f;
+  for (int v = v_begin + threadIdx.x; v < v_end; v += blockDim.x) {
+    float bias = 0.f;
+    for (int i = 0; i < rank; ++i) bias = fmaf(arow[i], ld_f(Ct, (size_t)v * rank + i), bias);
+    const float zq = (ld_f(U, (size_t)v) + bias) * inv_tq;
+    const float pv = exp2f(fmaf(ld_f(L, (size_t)v), kt, -m_t)) * inv_s_t;
+    sum += fminf(pv, expf(zq - lse_q));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_down_sync(0xffffffffu, sum, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kVerifyThreads / 32; ++w) t += red[w];
+    atomicAdd(&p.c_star[(size_t)r * G + (k - 1)], t);
+  }
+}
+
 // ------------------------------------------------------------- scratch ----
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -771,6 +857,13 @@ static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_
   const dim3 g2((unsigned)residual_nsplit(p.R, p.V), (unsigned)p.R);
   if (!p.tc_residual) {
     residual_kernel<TT, TL, TF><<<g2, kVerifyThreads, 0, stream>>>(p, p.ws.req_jstar);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || !p.c_star) return err;
+    cstar_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+    const int rows = std::max(1, p.R * p.gamma);
+    const int ns = std::max(1, std::min((p.V + 1023) / 1024, (4 * 152 * 2 + rows - 1) / rows));
+    cstar_kernel<TT, TL, TF>
+        <<<dim3((unsigned)ns, (unsigned)p.R, (unsigned)p.gamma), kVerifyThreads, 0, stream>>>(p);
     return cudaGetLastError();
   }
   ResidTCParams t{};
@@ -800,12 +893,18 @@ static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_
   t.fallback = p.ws.fallback;
   t.status = p.status;
   const int grid = std::max(p.device_sms, t.max_mtiles);
-  err = launch_resid_tc(t, tgt_dtype, logit_dtype, p.tgt, p.U, p.Ct, grid, stream);
+  err = launch_resid_tc(t, tgt_dtype, logit_dtype, p.tgt, p.U, p.Ct, grid, false, stream);
   if (err != cudaSuccess) return err;
   // requests whose residual was zero everywhere (fp32 rounding only): the
   // generic kernel redoes them, sampling from p if its residual is zero too
   residual_kernel<TT, TL, TF><<<g2, kVerifyThreads, 0, stream>>>(p, p.ws.fallback);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err != cudaSuccess || !p.c_star) return err;
+  // c*: every verified row, grouped by position (the residual lists are free now)
+  cstar_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+  t.c_star = p.c_star;
+  const int cgrid = std::max(p.device_sms, p.gamma * ((p.R + 127) / 128));
+  return launch_resid_tc(t, tgt_dtype, logit_dtype, p.tgt, p.U, p.Ct, cgrid, true, stream);
 }
 
 template <typename TT>

@@ -56,6 +56,7 @@ struct VerifyParams {
   int32_t* n_out;
   float* p_tok;
   float* lse_t;
+  float* c_star;  // [R, gamma] sum_v min(p, q) of the verified draft rows (nullable)
   uint32_t* status;
   bool tc_residual;      // residual on the fused tensor-core kernel
   bool row_ring;         // row pass: per-warp bulk-copy rings in dynamic shared memory
