@@ -8,7 +8,8 @@
 // p_v.  q_v = exp(z_v - lse_q) with z the draft logits of row k:
 //     z[m, v] = (U[m, k, v] + A_k[x_{m,k-1}, :] . C_k[:, v]) / T_k,
 // so the bias is again a rank-r GEMM: the requests of one position form the
-// M dimension (gathered, up to 128 per tile), the vocabulary the N dimension.
+// M dimension (gathered, up to kResTileRows per tile and replicated to the
+// 128 rows of the MMA), the vocabulary the N dimension.
 // p_v = 2^(L_v log2e / T_t - m_t) / s_t uses the softmax reference/sum of the target row
 // that the verify row pass stored.
 //
@@ -17,11 +18,15 @@
 // 置信度头": c* = 1 - TV(p, q), the confidence head's calibration target).
 //
 // Layout and pipelines follow the fused draft kernel (fused_tc.cuh): one CTA
-// per SM, 16 epilogue warps, a TMA producer warp and an MMA warp.  Rows are
-// gathered: the producer loads one 128-byte row box per request and operand
-// (U row and target row), which lands in the same 128-byte swizzle layout as
-// a 128-row box.  Work split: the request tiles of all positions are counted
-// on the device; CTA b takes tile b % M and vocabulary split b / M.
+// per SM, 16 epilogue warps, a TMA producer warp and an MMA warp.  Two rings:
+// the C_k tiles (one per 64-column tile, freed by the MMA) and the gathered
+// rows (U row and target row of every request of the tile, w consecutive
+// 64-column tiles per stage, one bulk copy per request and operand, freed by
+// the epilogue after its w-th tile).  w is chosen per CTA from the number of
+// gathered rows: with few rows each copy spans up to 512 columns, since the
+// cost of a gather is the number of copies, not their bytes.  Work split: the
+// request tiles of all positions are counted on the device; CTA b takes tile
+// b % M and vocabulary split b / M.
 #include "fused_tc.cuh"
 #include "draft_tc.cuh"
 #include "residual_tc.cuh"
@@ -37,19 +42,19 @@ __device__ __forceinline__ WRace wrace_merge_(const WRace& a, const WRace& b) {
   return race_beats(b.bw, b.bE, b.idx, a.bw, a.bE, a.idx) ? b : a;
 }
 
-// Gathered rows are copied linearly, one 64-column segment per request, with a
-// 16-byte pad per row so that eight consecutive rows reading the same 16-byte
-// chunk hit eight different bank groups.
+// Gathered rows are copied linearly, w 64-column segments per request, with a
+// 16-byte pad per row (pitch = w * 64 * size + 16, 16 modulo 128) so that
+// eight consecutive rows reading the same 16-byte chunk hit eight different
+// bank groups.
 template <typename T>
-struct RowTile {
-  static constexpr uint32_t kPitch = kNT * sizeof(T) + 16;
-  static constexpr uint32_t kBytes = 128 * kPitch;
-};
+__host__ __device__ constexpr uint32_t row_pitch(int w) {
+  return (uint32_t)w * kNT * sizeof(T) + 16u;
+}
 
-// 16 consecutive values of `row` from column 16*grp.
-__device__ __forceinline__ void load_row16(const unsigned char* tile, int row, int grp,
-                                           float (&v)[16], float) {
-  const unsigned char* base = tile + row * RowTile<float>::kPitch + grp * 64;
+// 16 consecutive values of `row` from column `col` of a gathered block.
+__device__ __forceinline__ void load_row16(const unsigned char* blk, uint32_t pitch, int row,
+                                           int col, float (&v)[16], float) {
+  const unsigned char* base = blk + row * pitch + col * 4;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float4 f = *reinterpret_cast<const float4*>(base + 16 * j);
@@ -59,9 +64,9 @@ __device__ __forceinline__ void load_row16(const unsigned char* tile, int row, i
     v[4 * j + 3] = f.w;
   }
 }
-__device__ __forceinline__ void load_row16(const unsigned char* tile, int row, int grp,
-                                           float (&v)[16], __nv_bfloat16) {
-  const unsigned char* base = tile + row * RowTile<__nv_bfloat16>::kPitch + grp * 32;
+__device__ __forceinline__ void load_row16(const unsigned char* blk, uint32_t pitch, int row,
+                                           int col, float (&v)[16], __nv_bfloat16) {
+  const unsigned char* base = blk + row * pitch + col * 2;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint4 q = *reinterpret_cast<const uint4*>(base + 16 * j);
@@ -74,7 +79,6 @@ __device__ __forceinline__ void load_row16(const unsigned char* tile, int row, i
   }
 }
 
-constexpr uint32_t round1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 
 }  // namespace
 
@@ -90,9 +94,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr uint32_t kCBytes = KC * kNT * 128;
   unsigned char* sA = smem;
-  unsigned char* sStage = smem + KC * 16384;
+  unsigned char* sC = smem + KC * 16384;  // C ring, then the row ring
 
-  __shared__ __align__(8) uint64_t full_c[kMaxStages], full_r[kMaxStages], empty_s[kMaxStages];
+  __shared__ __align__(8) uint64_t full_c[kMaxStages], empty_c[kMaxStages];
+  __shared__ __align__(8) uint64_t full_r[kMaxStages], empty_r[kMaxStages];
   __shared__ __align__(8) uint64_t tfull[kTmemBufs], tempty[kTmemBufs];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work assignment (identical in every CTA) -------------------------
   if (threadIdx.x == 0) {
     int M = 0;
-    for (int kk = 0; kk < G; ++kk) M += (p.res_cnt[kk] + 127) / 128;
+    for (int kk = 0; kk < G; ++kk) M += (p.res_cnt[kk] + kResTileRows - 1) / kResTileRows;
     int nsplit = M > 0 ? max(1, (int)gridDim.x / M) : 1;
     nsplit = min(min(nsplit, p.ntiles), kMaxDeviceSms);
     int mt = M > 0 ? (int)blockIdx.x % M : 0, split = M > 0 ? (int)blockIdx.x / M : 0;
@@ -114,11 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (M > 0 && split < nsplit) {
       int acc = 0;
       for (int kk = 0; kk < G; ++kk) {
-        const int n = (p.res_cnt[kk] + 127) / 128;
+        const int n = (p.res_cnt[kk] + kResTileRows - 1) / kResTileRows;
         if (mt < acc + n) {
           k = kk + 1;
-          i0 = (mt - acc) * 128;
-          rows = min(128, p.res_cnt[kk] - i0);
+          i0 = (mt - acc) * kResTileRows;
+          rows = min(kResTileRows, p.res_cnt[kk] - i0);
           break;
         }
         acc += n;
@@ -140,12 +145,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = (int)((long)(split + 1) * p.ntiles / nsplit);
   const int T = t_end - t_begin;
   const int G1 = G + 1;
-  // Stages sized for this tile's gathered rows (often far fewer than 128):
-  // C tile, then the U rows, then the target rows, each row padded.
-  const uint32_t u_bytes = (uint32_t)nrows * RowTile<TL>::kPitch;
-  const uint32_t stage_bytes = round1024(kCBytes + u_bytes + (uint32_t)nrows * RowTile<TT>::kPitch);
-  const uint32_t fit = ((uint32_t)p.smem_bytes - 1024u - KC * 16384u) / stage_bytes;
-  const int S = (int)(fit < (uint32_t)kMaxStages ? fit : (uint32_t)kMaxStages);
+  // Ring sizes for this tile's gathered rows (at most kResTileRows): the
+  // widest row stage (gw tiles) of which three fit next to three C stages,
+  // then as many C stages as leave room for three row stages (up to six), and
+  // the rest for row stages.  The host checks that two C stages and one row
+  // stage of gw = 1 always fit.
+  const uint32_t avail0 = (uint32_t)p.smem_bytes - 1024u - KC * 16384u;
+  int gw = 1;  // 64-column tiles per row stage
+  uint32_t pitch_u = row_pitch<TL>(1), pitch_t = row_pitch<TT>(1);
+  uint32_t rstage = ((uint32_t)nrows * (pitch_u + pitch_t) + 127u) & ~127u;
+  for (int cand = 8; cand > 1; cand >>= 1) {
+    const uint32_t pu = row_pitch<TL>(cand), pt = row_pitch<TT>(cand);
+    const uint32_t bytes = ((uint32_t)nrows * (pu + pt) + 127u) & ~127u;
+    if (3u * bytes + 3u * kCBytes <= avail0) {
+      gw = cand;
+      pitch_u = pu;
+      pitch_t = pt;
+      rstage = bytes;
+      break;
+    }
+  }
+  int Sc = 2;
+  while (Sc < 6 && (uint32_t)(Sc + 1) * kCBytes + 3u * rstage <= avail0) ++Sc;
+  const uint32_t fit = (avail0 - (uint32_t)Sc * kCBytes) / rstage;
+  const int Sr = (int)(fit < (uint32_t)kMaxStages ? fit : (uint32_t)kMaxStages);
+  unsigned char* sRow = sC + Sc * kCBytes;
+  const uint32_t u_block = (uint32_t)nrows * pitch_u;  // target rows follow the U rows
+  // Few rows leave most TMEM lane quadrants empty, and one warp per SM
+  // sub-partition cannot hide the epilogue's latencies.  So the rows are
+  // replicated: the A tile holds the nq quadrants of requests rho times, and
+  // replica g's quadrants take the tiles t with t % rho == g.
+  const int nq = (nrows + 31) / 32;
+  const int rho = nq == 1 ? 4 : (nq == 2 ? 2 : 1);
+  const int span = 32 * nq;  // A row i holds request slot i % span
 
   for (int i = threadIdx.x; i < 128; i += blockDim.x) {
     int r = -1, trow = 0;
@@ -157,14 +189,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_trow[i] = trow;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < Sc; ++s) {
       tc::mbar_init(&full_c[s], 1);
+      tc::mbar_init(&empty_c[s], 1);
+    }
+    for (int s = 0; s < Sr; ++s) {
       tc::mbar_init(&full_r[s], 1);
-      tc::mbar_init(&empty_s[s], 1 + kEpiWarps);
+      tc::mbar_init(&empty_r[s], kEpiWarps);
     }
     for (int b = 0; b < kTmemBufs; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], kEpiWarps);
+      tc::mbar_init(&tempty[b], 4 * nq);  // the warps of the tile's replica
     }
     abort_flag = 0;
     tc::fence_barrier_init();
@@ -183,45 +218,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == kProducerWarp) {
-    // All 32 lanes issue row loads; lane 0 also the C tile and the byte counts.
-    int issued = 0;
-    Ring r{0, 0u};
-    for (int t = 0; t < T && !abort_flag; ++t, r.next(S)) {
+    // Lane 0 loads the C tiles and arms the barriers; all 32 lanes issue the
+    // row copies of a group (one per request and operand, w tiles wide).
+    int issued_c = 0, issued_g = 0;
+    Ring rc{0, 0u}, rr{0, 0u};
+    for (int t = 0; t < T && !abort_flag; ++t, rc.next(Sc)) {
+      const int n0 = (t_begin + t) * kNT;
+      if (t % gw == 0) {
+        bool ok = true;
+        if (lane == 0) ok = tc::mbar_wait(&empty_r[rr.idx], rr.phase ^ 1u, kWaitNs);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) fail();
+          break;
+        }
+        unsigned char* st = sRow + rr.idx * rstage;
+        // columns of this group inside the split and the vocabulary (a
+        // multiple of 16 bytes in both dtypes, because V times the element
+        // size is)
+        const int seg = min(min(gw, T - t) * kNT, p.V - n0);
+        const uint32_t ub = (uint32_t)seg * sizeof(TL), tb = (uint32_t)seg * sizeof(TT);
+        if (lane == 0) tc::mbar_expect_tx(&full_r[rr.idx], (uint32_t)nrows * (ub + tb));
+        __syncwarp();
+        for (int i = lane; i < nrows; i += 32) {
+          const size_t urow = (size_t)s_req[i] * p.gamma + (k - 1);
+          tc::bulk_load(st + i * pitch_u, U + urow * p.V + n0, ub, &full_r[rr.idx]);
+          tc::bulk_load(st + u_block + i * pitch_t, tgt + (size_t)s_trow[i] * p.V + n0, tb,
+                        &full_r[rr.idx]);
+        }
+        issued_g += 1;
+        rr.next(Sr);
+      }
       bool ok = true;
-      if (lane == 0) ok = tc::mbar_wait(&empty_s[r.idx], r.phase ^ 1u, kWaitNs);
+      if (lane == 0) ok = tc::mbar_wait(&empty_c[rc.idx], rc.phase ^ 1u, kWaitNs);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) {
         if (lane == 0) fail();
         break;
       }
-      unsigned char* st = sStage + r.idx * stage_bytes;
-      const int n0 = (t_begin + t) * kNT;
-      // columns of this tile inside the vocabulary (a multiple of 16 bytes in
-      // both dtypes, because V times the element size is)
-      const int seg = min(kNT, p.V - n0);
-      const uint32_t ub = (uint32_t)seg * sizeof(TL), tb = (uint32_t)seg * sizeof(TT);
       if (lane == 0) {
-        tc::mbar_expect_tx(&full_c[r.idx], kCBytes);
+        unsigned char* st = sC + rc.idx * kCBytes;
+        tc::mbar_expect_tx(&full_c[rc.idx], kCBytes);
 #pragma unroll
         for (int kc = 0; kc < KC; ++kc)
-          tc::tma_load_3d(st + kc * 8192, &tm_c, &full_c[r.idx], kc * 64, n0, k - 1);
-        tc::mbar_expect_tx(&full_r[r.idx], (uint32_t)nrows * (ub + tb));
+          tc::tma_load_3d(st + kc * 8192, &tm_c, &full_c[rc.idx], kc * 64, n0, k - 1);
       }
       __syncwarp();
-      for (int i = lane; i < nrows; i += 32) {
-        const size_t urow = (size_t)s_req[i] * p.gamma + (k - 1);
-        tc::bulk_load(st + kCBytes + i * RowTile<TL>::kPitch, U + urow * p.V + n0, ub, &full_r[r.idx]);
-        tc::bulk_load(st + kCBytes + u_bytes + i * RowTile<TT>::kPitch,
-                      tgt + (size_t)s_trow[i] * p.V + n0, tb, &full_r[r.idx]);
-      }
-      issued = t + 1;
+      issued_c = t + 1;
     }
     if (abort_flag && lane == 0) {
-      for (int t = (issued > S ? issued - S : 0); t < issued; ++t) {
-        const uint32_t ph = (uint32_t)(t / S) & 1u;
-        tc::mbar_wait(&full_c[t % S], ph, kWaitNs);
-        tc::mbar_wait(&full_r[t % S], ph, kWaitNs);
-      }
+      // the copies still in flight must land before the CTA exits
+      for (int t = (issued_c > Sc ? issued_c - Sc : 0); t < issued_c; ++t)
+        tc::mbar_wait(&full_c[t % Sc], (uint32_t)(t / Sc) & 1u, kWaitNs);
+      for (int g = (issued_g > Sr ? issued_g - Sr : 0); g < issued_g; ++g)
+        tc::mbar_wait(&full_r[g % Sr], (uint32_t)(g / Sr) & 1u, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -231,14 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last = -1;
       Ring r{0, 0u}, rb{0, 0u};
       const uint32_t a_base = tc::smem_u32(sA);
-      for (int t = 0; t < T && !abort_flag; ++t, r.next(S), rb.next(kTmemBufs)) {
+      for (int t = 0; t < T && !abort_flag; ++t, r.next(Sc), rb.next(kTmemBufs)) {
         if (!tc::mbar_wait(&full_c[r.idx], r.phase, kWaitNs) ||
             !tc::mbar_wait(&tempty[rb.idx], rb.phase ^ 1u, kWaitNs)) {
           fail();
           break;
         }
         tc::fence_after_sync();
-        const uint32_t b_base = tc::smem_u32(sStage + r.idx * stage_bytes);
+        const uint32_t b_base = tc::smem_u32(sC + r.idx * kCBytes);
 #pragma unroll
         for (int kk = 0; kk < KC * 4; ++kk) {
           const int kc = kk >> 2, ko = (kk & 3) * 32;
@@ -246,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        tc::sw128_desc(b_base + kc * 8192 + ko), idesc, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&tfull[rb.idx]);
-        tc::mma_commit(&empty_s[r.idx]);
+        tc::mma_commit(&empty_c[r.idx]);
         last = t;
       }
       if (abort_flag && last >= 0)
@@ -257,16 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue --
     const int quad = warp & 3, grp = warp >> 2;
     const int row = quad * 32 + lane;
-    const bool valid = row < nrows;
+    const bool holder = quad < nq * rho;  // quadrant of some replica
+    const int replica = quad / nq, slot = row % span;
+    const bool valid = holder && slot < nrows;
     // the stages hold exactly nrows rows: lanes past them read row 0 (unused)
-    const int lrow = valid ? row : 0;
+    const int lrow = valid ? slot : 0;
     const int V = p.V, rank = p.rank;
     const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
     for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
       const int i = idx / (KC * 8), c = idx % (KC * 8);
       uint4 val = make_uint4(0, 0, 0, 0);
-      if (i < nrows) {
-        const int req = s_req[i];
+      if (i % span < nrows) {
+        const int req = s_req[i % span];
         int xp = (k == 1) ? p.x0[req] : p.x[(size_t)req * G + (k - 2)];
         if (xp < 0 || xp >= V) xp = 0;
         val = *reinterpret_cast<const uint4*>(Ak + (size_t)xp * rank + c * 8);
@@ -278,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(1, (kEpiWarps + 1) * 32);
 
     // Per-request constants (log2 units): q = 2^(z kq + nq), p = 2^(L kt + nt) / s_t.
-    const int req = valid ? s_req[row] : 0;
+    const int req = valid ? s_req[slot] : 0;
     const uint32_t rid = p.rid_base + (uint32_t)req;
     const size_t rk1 = (size_t)req * G + (k - 1);
     const size_t rj = (size_t)req * G1 + (k - 1);
@@ -298,35 +350,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     float c_res = CUDART_INF_F;
     uint32_t shared_key = 0;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
-    Ring r{0, 0u}, rb{0, 0u};
-    for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
+    Ring rr{0, 0u}, rb{0, 0u};
+    for (int t = 0; t < T; ++t, rb.next(kTmemBufs)) {
       if (abort_flag) break;
+      const bool group_done = (t % gw == gw - 1) || (t == T - 1);
+      // Every warp waits for each row group (so none runs a ring lap ahead)
+      // and releases it after the group's last tile; only the tile's replica
+      // waits for the accumulator and computes.
+      const bool own = holder && (t % rho == replica);
+      if ((t % gw == 0 || own) && !tc::mbar_wait(&full_r[rr.idx], rr.phase, kWaitNs)) {
+        fail();
+        break;
+      }
+      if (!own) {
+        __syncwarp();
+        if (group_done) {
+          if (lane == 0) tc::mbar_arrive(&empty_r[rr.idx]);
+          rr.next(Sr);
+        }
+        continue;
+      }
       const uint32_t shared_now = shared_key;
       if (!kCStar && valid) shared_key = __ldcg(row_best);
-      if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
-          !tc::mbar_wait(&full_r[r.idx], r.phase, kWaitNs)) {
+      if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs)) {
         fail();
         break;
       }
       tc::fence_after_sync();
+      const unsigned char* sr = sRow + rr.idx * rstage;
+      const int col = (t % gw) * kNT + grp * 16;
       // q first (frees the bias and U registers), then the target row.
       float qv[16], L[16];
       {
         uint32_t braw[16];
         float u[16];
         tc::tmem_ld16(t_lane + (uint32_t)(rb.idx * kNT), braw);
-        load_row16(sStage + r.idx * stage_bytes + kCBytes, lrow, grp, u, TL());
+        load_row16(sr, pitch_u, lrow, col, u, TL());
         tc::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 16; ++c) qv[c] = tc::ex2(fmaf(u[c] + __uint_as_float(braw[c]), kq, nq));
       }
-      load_row16(sStage + r.idx * stage_bytes + kCBytes + u_bytes, lrow, grp, L, TT());
+      load_row16(sr + u_block, pitch_t, lrow, col, L, TT());
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(&tempty[rb.idx]);
-        tc::mbar_arrive(&empty_s[r.idx]);
+        if (group_done) tc::mbar_arrive(&empty_r[rr.idx]);
       }
+      if (group_done) rr.next(Sr);
       if (!valid) continue;
       const int colbase = (t_begin + t) * kNT + grp * 16;
       if constexpr (kCStar) {
@@ -372,23 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if constexpr (kCStar) {
-      // four column groups and every split add into the row's sum
+      // column groups, replicas and splits all add into the row's sum
       if (valid && !abort_flag) atomicAdd(&p.c_star[rk1], csum);
     } else {
-    // merge the four column groups through the stage buffers
-    WRace* grp_state = reinterpret_cast<WRace*>(sStage);  // [3][128]
-    named_bar_sync(2, kEpiWarps * 32);
-    if (grp > 0) grp_state[(grp - 1) * 128 + row] = rres;
-    named_bar_sync(2, kEpiWarps * 32);
-    if (grp == 0 && valid) {
-#pragma unroll
-      for (int g = 0; g < 3; ++g) rres = wrace_merge_(rres, grp_state[g * 128 + row]);
-      Partial w{};
-      w.f0 = rres.bw;
-      w.f1 = rres.bE;
-      w.i0 = rres.idx;
-      p.partials[((size_t)mt * 128 + row) * nsplit + split] = w;
-    }
+      // merge the column groups and replicas of each request through shared
+      // memory: [4 * rho][span] states, slot (replica * 4 + grp, request slot)
+      WRace* st_all = reinterpret_cast<WRace*>(sC);
+      const int nst = 4 * rho;
+      named_bar_sync(2, kEpiWarps * 32);
+      if (valid) st_all[(replica * 4 + grp) * span + slot] = rres;
+      named_bar_sync(2, kEpiWarps * 32);
+      if (valid && replica == 0 && grp == 0) {
+        for (int g = 1; g < nst; ++g) rres = wrace_merge_(rres, st_all[g * span + slot]);
+        Partial pw{};
+        pw.f0 = rres.bw;
+        pw.f1 = rres.bE;
+        pw.i0 = rres.idx;
+        p.partials[((size_t)mt * kResTileRows + slot) * nsplit + split] = pw;
+      }
     }
   }
 
@@ -402,17 +474,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (kCStar) return;
   if (!last_block_arrives(p.counters + mt, (unsigned)nsplit)) return;
 
-  // Last CTA of this request tile: merge the splits, four threads per request.
+  static_assert(kEpiWarps * 32 / 16 >= kResTileRows, "sixteen merge threads per request");
+  // Last CTA of this request tile: merge the splits, sixteen threads per
+  // request with all their loads in flight (one round trip up to 128 splits).
   if (threadIdx.x < kEpiWarps * 32) {
-    const int row = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int row = threadIdx.x >> 4, part = threadIdx.x & 15;
     WRace a = wrace_empty();
-    if (row < nrows)
-      for (int s = part; s < nsplit; s += 4) {
-        const Partial w = load_partial(p.partials + ((size_t)mt * 128 + row) * nsplit + s);
-        a = wrace_merge_(a, WRace{w.f0, w.f1, w.i0});
+    if (row < nrows) {
+      const Partial* src = p.partials + ((size_t)mt * kResTileRows + row) * nsplit;
+      for (int s0 = part; s0 < nsplit; s0 += 16 * 8) {
+        Partial w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (s0 + 16 * q < nsplit) w[q] = load_partial(src + s0 + 16 * q);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (s0 + 16 * q < nsplit) a = wrace_merge_(a, WRace{w[q].f0, w[q].f1, w[q].i0});
       }
-    a = wrace_merge_(a, wrace_shfl_xor(a, 1));
-    a = wrace_merge_(a, wrace_shfl_xor(a, 2));
+    }
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) a = wrace_merge_(a, wrace_shfl_xor(a, off));
     if (part == 0 && row < nrows) {
       const int req = s_req[row];
       if (a.idx >= 0)
@@ -426,13 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host --
 namespace {
 
+// The kernel splits whatever shared memory it gets into rings sized for its
+// rows; two C stages and one row stage of a full tile must fit.
 template <typename TT, typename TL, int KC>
-size_t smem_bytes(int stages) {
-  return 1024 + (size_t)KC * 16384 +
-         (size_t)stages * round1024(KC * kNT * 128 + RowTile<TL>::kBytes + RowTile<TT>::kBytes);
+size_t min_smem_bytes() {
+  const size_t row1 = kResTileRows * (size_t)(row_pitch<TL>(1) + row_pitch<TT>(1));
+  return 1024 + (size_t)KC * 16384 + 2 * (size_t)KC * kNT * 128 + ((row1 + 127) & ~(size_t)127);
 }
-// The kernel splits whatever shared memory it gets into stages sized for its
-// rows; at least two stages of a full 128-row tile must fit.
 
 template <typename TT, typename TL, int KC>
 cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void* U, const void* Ct,
@@ -445,7 +526,7 @@ cudaError_t launch_typed(const ResidTCParams& base, const void* tgt, const void*
     return cudaErrorInvalidValue;
   // all of the per-CTA shared memory but 4 KB left for the static arrays
   const size_t smem = 227 * 1024 - 4096;
-  if (smem_bytes<TT, TL, KC>(2) > smem) return cudaErrorInvalidValue;
+  if (min_smem_bytes<TT, TL, KC>() > smem) return cudaErrorInvalidValue;
   p.smem_bytes = (int)smem;
   auto kern = cstar ? resid_tc_kernel<TT, TL, KC, true> : resid_tc_kernel<TT, TL, KC, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

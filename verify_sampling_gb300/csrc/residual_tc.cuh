@@ -20,7 +20,7 @@ struct ResidTCParams {
   const float* row_s;       // [R, gamma + 1] target-row softmax sum
   const int* res_cnt;       // [gamma] requests whose first rejection is at j = k
   const int* res_list;      // [gamma, R] those requests
-  Partial* partials;        // [max_mtiles, 128, nsplit]
+  Partial* partials;        // [max_mtiles, kResTileRows, nsplit]
   unsigned* counters;       // [max_mtiles], zero on entry
   unsigned* row_best;       // [R] shared race bounds, zero on entry
   int32_t* out_tok;         // [R, gamma + 1]
@@ -29,8 +29,15 @@ struct ResidTCParams {
   uint32_t* status;
 };
 
-// Request tiles the residual kernel may need: sum_k ceil(cnt_k / 128).
-inline int resid_tc_max_mtiles(int R, int gamma) { return (R + 127) / 128 + gamma; }
+// Requests per tile of the residual kernel: few enough that every row copy
+// can span several 64-column tiles and the rows replicate over all four TMEM
+// lane quadrants.
+constexpr int kResTileRows = 32;
+
+// Request tiles the residual kernel may need: sum_k ceil(cnt_k / kResTileRows).
+inline int resid_tc_max_mtiles(int R, int gamma) {
+  return (R + kResTileRows - 1) / kResTileRows + gamma;
+}
 
 bool resid_tc_supported(int tgt_dtype, int logit_dtype, int fac_dtype, int rank, int V,
                         const void* tgt, const void* U, const void* A, const void* Ct);

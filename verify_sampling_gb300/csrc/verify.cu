@@ -792,7 +792,7 @@ static size_t layout(int R, int gamma, int V, size_t off[kLayoutN]) {
   const size_t sizes[kLayoutN] = {rows * ns * sizeof(Partial), (size_t)R * nr * sizeof(Partial),
                                   rows * sizeof(float), rows * sizeof(float), rows * sizeof(int),
                                   (size_t)R * sizeof(int), (size_t)gamma * R * sizeof(int),
-                                  mt * 128 * kMaxDeviceSms * sizeof(Partial), rows * sizeof(int),
+                                  mt * kResTileRows * kMaxDeviceSms * sizeof(Partial), rows * sizeof(int),
                                   sizeof(int), sizeof(unsigned long long), rows * sizeof(unsigned), (size_t)R * sizeof(unsigned),
                                   (size_t)R * sizeof(unsigned), (size_t)gamma * sizeof(int),
                                   mt * sizeof(unsigned), (size_t)R * sizeof(unsigned),
@@ -903,7 +903,7 @@ static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_
   // c*: every verified row, grouped by position (the residual lists are free now)
   cstar_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   t.c_star = p.c_star;
-  const int cgrid = std::max(p.device_sms, p.gamma * ((p.R + 127) / 128));
+  const int cgrid = std::max(p.device_sms, p.gamma * ((p.R + kResTileRows - 1) / kResTileRows));
   return launch_resid_tc(t, tgt_dtype, logit_dtype, p.tgt, p.U, p.Ct, cgrid, true, stream);
 }
 
