@@ -426,19 +426,15 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
                           draft_temp=g["draft_temp"], h=devb["h"], W1=g["W1"], w=g["w"],
                           sts_temp=g["sts_temp"], request_id_base=rid_base)
 
+    host_out = {k: outs[k] for k in ("out_tok", "accept_len", "n_out", "stats")}
+
     def one(i):
-        for n in names:
-            devb[n].copy_(host[n], non_blocking=True)
-        res = vs.run_round(d_in, devb["tgt"].view(-1, wl.V), g["tgt_row_off"], g["sps"],
-                           g["b_lo"], g["b_step"], wl.K, 9000 + i, sched_mode=wl.sched_mode,
-                           sched_threshold=wl.sched_threshold,
-                           bufs={"draft": bufs["draft"], "ws_draft": bufs["ws_draft"],
-                                 "ws_verify": bufs["ws_verify"]})
-        v, s = res["verify"], res["sched"]
-        outs["out_tok"].copy_(v["out_tok"], non_blocking=True)
-        outs["accept_len"].copy_(v["accept_len"], non_blocking=True)
-        outs["n_out"].copy_(v["n_out"], non_blocking=True)
-        outs["stats"].copy_(s["stats"], non_blocking=True)
+        # one C-ABI call: host inputs in, host results out
+        vs.run_round_host(d_in, devb["tgt"].view(-1, wl.V), g["tgt_row_off"], g["sps"], g["b_lo"],
+                          g["b_step"], wl.K, 9000 + i, host_in=host, host_out=host_out,
+                          sched_mode=wl.sched_mode, sched_threshold=wl.sched_threshold,
+                          bufs={"draft": bufs["draft"], "ws_draft": bufs["ws_draft"],
+                                "ws_verify": bufs["ws_verify"]})
         torch.cuda.synchronize()
         return wl.R * wl.gamma + float(outs["stats"][1])
 

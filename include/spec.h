@@ -330,6 +330,48 @@ typedef struct spec_verify_args {
 
 int spec_verify(const spec_verify_args *args, uint64_t seed, spec_stream_t stream);
 
+/* --------------------------------------------------- one round, host I/O -
+ * DSpark summary, Figure 1 (one round: draft, schedule, verify) as a single
+ * call on host buffers.  The per-round inputs are copied from host memory
+ * into the device buffers the stage arguments name.  The three stages then
+ * run as spec_draft_sample, spec_schedule and spec_verify, and the per-round
+ * results are copied back.  Everything is asynchronous on `stream`, one
+ * cudaMemcpyAsync per buffer.  Page-locked host buffers keep the copies
+ * asynchronous; pageable ones make them synchronous.  The weights (A, Ct, W1,
+ * w, the temperatures, the SPS table) stay in device memory across rounds.
+ *   draft, sched, verify  as for the three calls.  draft->U, draft->h,
+ *     draft->x0 and verify->tgt are the destinations of the input copies.
+ *     The stages must be chained (checked): sched->a is draft->a;
+ *     verify->ell is sched->ell; verify->x, q_tok and lse_q are draft's x,
+ *     q_tok and lse_q; the sizes agree; and verify runs in sample mode with
+ *     verify->draft the same draft arguments.
+ *   U_host [R, gamma, V] (draft logit dtype), h_host [R, gamma, d] (confidence
+ *     dtype), x0_host [R] int32, tgt_host [tgt_rows, V] (target dtype):
+ *     per-round inputs; each is nullable, and then the device buffer is used
+ *     as it stands.
+ *   out_tok_host [R, gamma + 1], accept_len_host [R], n_out_host [R] int32
+ *     and stats_host [4] f64 (the schedule's {n, B, tau, Theta}): per-round
+ *     outputs, each nullable.
+ * Returns the first stage's error, or SPEC_ERR_CUDA when a copy fails to
+ * enqueue.
+ */
+typedef struct spec_round_host_args {
+  const spec_draft_args *draft;
+  const spec_sched_args *sched;
+  const spec_verify_args *verify;
+  const void *U_host;
+  const void *h_host;
+  const int32_t *x0_host;
+  const void *tgt_host;
+  size_t tgt_rows;
+  int32_t *out_tok_host;
+  int32_t *accept_len_host;
+  int32_t *n_out_host;
+  double *stats_host;
+} spec_round_host_args;
+
+int spec_round_host(const spec_round_host_args *args, uint64_t seed, spec_stream_t stream);
+
 /* ------------------------------------------------------------ stream ----
  * The library's random stream, as the kernels draw it (see "Randomness" above):
  * u_out[v] = uniform of vocabulary entry v at (position j, global request id

@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(spec):
     names = _declared_functions()
     assert {"spec_draft_sample", "spec_schedule", "spec_verify", "spec_workspace_bytes",
             "spec_error_string", "spec_stream_uniforms", "spec_version",
-            "spec_accept_stats", "spec_calibration"} <= set(names)
+            "spec_accept_stats", "spec_calibration", "spec_round_host"} <= set(names)
     lib = spec.lib()
     for n in names:
         assert hasattr(lib, n), n
@@ -52,12 +52,14 @@ def test_struct_layout_matches_c(spec, tmp_path):
         'printf("spec_verify_args %zu\\n", sizeof(spec_verify_args));\n'
         'printf("spec_accept_stats_args %zu\\n", sizeof(spec_accept_stats_args));\n'
         'printf("spec_calibration_args %zu\\n", sizeof(spec_calibration_args));\n'
+        'printf("spec_round_host_args %zu\\n", sizeof(spec_round_host_args));\n'
         "P(spec_draft_args, status) P(spec_draft_args, workspace_bytes) P(spec_draft_args, U)\n"
         "P(spec_sched_args, b_lo) P(spec_sched_args, stats) P(spec_sched_args, status)\n"
         "P(spec_sched_args, threshold) P(spec_accept_stats_args, beta)\n"
         "P(spec_accept_stats_args, ema) P(spec_accept_stats_args, status)\n"
         "P(spec_verify_args, c_star) P(spec_calibration_args, n_bins)\n"
         "P(spec_calibration_args, ece) P(spec_calibration_args, status)\n"
+        "P(spec_round_host_args, tgt_rows) P(spec_round_host_args, stats_host)\n"
         "P(spec_verify_args, target_temp) P(spec_verify_args, draft) P(spec_verify_args, status)\n"
         "return 0;}\n")
     exe = tmp_path / "layout"
@@ -70,6 +72,7 @@ def test_struct_layout_matches_c(spec, tmp_path):
     assert int(got["spec_verify_args"]) == ctypes.sizeof(spec.VerifyArgs)
     assert int(got["spec_accept_stats_args"]) == ctypes.sizeof(spec.AcceptStatsArgs)
     assert int(got["spec_calibration_args"]) == ctypes.sizeof(spec.CalibrationArgs)
+    assert int(got["spec_round_host_args"]) == ctypes.sizeof(spec.RoundHostArgs)
     for key, (cls, field) in {"spec_draft_args.status": (spec.DraftArgs, "status"),
                               "spec_draft_args.workspace_bytes": (spec.DraftArgs, "workspace_bytes"),
                               "spec_draft_args.U": (spec.DraftArgs, "U"),
@@ -84,6 +87,8 @@ def test_struct_layout_matches_c(spec, tmp_path):
                               "spec_calibration_args.n_bins": (spec.CalibrationArgs, "n_bins"),
                               "spec_calibration_args.ece": (spec.CalibrationArgs, "ece"),
                               "spec_calibration_args.status": (spec.CalibrationArgs, "status"),
+                              "spec_round_host_args.tgt_rows": (spec.RoundHostArgs, "tgt_rows"),
+                              "spec_round_host_args.stats_host": (spec.RoundHostArgs, "stats_host"),
                               "spec_verify_args.target_temp": (spec.VerifyArgs, "target_temp"),
                               "spec_verify_args.draft": (spec.VerifyArgs, "draft"),
                               "spec_verify_args.status": (spec.VerifyArgs, "status")}.items():
@@ -153,6 +158,16 @@ def test_host_side_rejections_launch_nothing(spec):
     assert lib.spec_calibration(ctypes.byref(ca), None) == spec.SPEC_ERR_UNSUPPORTED
     ca.n_bins, ca.sum_c = 10, ctypes.c_void_p(260)
     assert lib.spec_calibration(ctypes.byref(ca), None) == spec.SPEC_ERR_ALIGNMENT
+    # a host round whose stages are not chained through the same buffers
+    assert lib.spec_round_host(None, 0, None) == spec.SPEC_ERR_INVALID_ARG
+    da, sa, va = spec.DraftArgs(), spec.SchedArgs(), spec.VerifyArgs()
+    da.R = sa.R = va.R = 4
+    da.gamma = sa.gamma = va.gamma = 2
+    da.V = va.V = 100
+    da.a, sa.a = ctypes.c_void_p(256), ctypes.c_void_p(512)  # schedule reads another buffer
+    rh = spec.RoundHostArgs()
+    rh.draft, rh.sched, rh.verify = ctypes.pointer(da), ctypes.pointer(sa), ctypes.pointer(va)
+    assert lib.spec_round_host(ctypes.byref(rh), 0, None) == spec.SPEC_ERR_INVALID_ARG
     v = spec.VerifyArgs()
     v.mode, v.R, v.gamma, v.V = 0, 2, 2, 10
     v.tgt = v.tgt_row_off = v.ell = v.x = v.accept_len = v.out_tok = v.n_out = ctypes.c_void_p(256)

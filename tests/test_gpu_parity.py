@@ -158,6 +158,42 @@ def test_deterministic_reruns():
             assert torch.equal(x[k], y[k]), k
 
 
+@pytest.mark.parametrize("name", ["tc_c5_small", "c3_small"])
+def test_round_host_matches_device_round(name):
+    """spec_round_host: the per-round inputs come from host buffers and the
+    results go back to host buffers; the round equals the device-resident one
+    and its tokens match the oracle's round on the same inputs."""
+    wl = SMALL[name]
+    inp = synth.make_inputs(wl, "cpu")
+    g = _to_dev(inp)
+    seed = 606
+    dev_round = vs.run_round(synth.draft_inputs(g), g["tgt"].view(-1, wl.V), g["tgt_row_off"],
+                             g["sps"], g["b_lo"], g["b_step"], wl.K, seed)
+    torch.cuda.synchronize()
+    # the same round with the device inputs scrambled first: the call must refill them
+    g2 = _to_dev(inp)
+    for k in ("U", "h", "tgt"):
+        g2[k].zero_()
+    g2["x0"].fill_(1)
+    host_in = {k: inp[k].contiguous().pin_memory() for k in ("U", "h", "x0", "tgt")}
+    host_out = {"out_tok": torch.empty(wl.R, wl.gamma + 1, dtype=torch.int32).pin_memory(),
+                "accept_len": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
+                "n_out": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
+                "stats": torch.empty(4, dtype=torch.float64).pin_memory()}
+    vs.run_round_host(synth.draft_inputs(g2), g2["tgt"].view(-1, wl.V), g2["tgt_row_off"],
+                      g2["sps"], g2["b_lo"], g2["b_step"], wl.K, seed, host_in=host_in,
+                      host_out=host_out)
+    torch.cuda.synchronize()
+    v = dev_round["verify"]
+    assert torch.equal(host_out["out_tok"], v["out_tok"].cpu())
+    assert torch.equal(host_out["accept_len"], v["accept_len"].cpu())
+    assert torch.equal(host_out["n_out"], v["n_out"].cpu())
+    assert torch.equal(host_out["stats"], dev_round["sched"]["stats"].cpu())
+    rep = compare_verify(g, dev_round["draft"], dev_round["sched"]["ell"], v, seed,
+                         oracle.MODE_SAMPLE, range(wl.R))
+    assert rep.checked + rep.near_ties == wl.R
+
+
 def test_bad_inputs_set_status_without_fault():
     wl = SMALL["c2_small"]
     g = _to_dev(synth.make_inputs(wl, "cpu"))

@@ -79,6 +79,14 @@ class VerifyArgs(ctypes.Structure):
                 ("c_star", _P)]
 
 
+class RoundHostArgs(ctypes.Structure):
+    _fields_ = [("draft", ctypes.POINTER(DraftArgs)), ("sched", ctypes.POINTER(SchedArgs)),
+                ("verify", ctypes.POINTER(VerifyArgs)), ("U_host", _P), ("h_host", _P),
+                ("x0_host", _P), ("tgt_host", _P), ("tgt_rows", ctypes.c_size_t),
+                ("out_tok_host", _P), ("accept_len_host", _P), ("n_out_host", _P),
+                ("stats_host", _P)]
+
+
 class SpecError(RuntimeError):
     pass
 
@@ -99,8 +107,9 @@ def lib() -> ctypes.CDLL:
         L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.c_uint64, _P]
         L.spec_accept_stats.argtypes = [ctypes.POINTER(AcceptStatsArgs), _P]
         L.spec_calibration.argtypes = [ctypes.POINTER(CalibrationArgs), _P]
+        L.spec_round_host.argtypes = [ctypes.POINTER(RoundHostArgs), ctypes.c_uint64, _P]
         for f in (L.spec_draft_sample, L.spec_schedule, L.spec_verify, L.spec_accept_stats,
-                  L.spec_calibration):
+                  L.spec_calibration, L.spec_round_host):
             f.restype = ctypes.c_int
         L.spec_workspace_bytes.argtypes = [ctypes.c_int] * 5
         L.spec_workspace_bytes.restype = ctypes.c_size_t
@@ -240,6 +249,19 @@ def draft_sample(inp: DraftInputs, seed: int, *, want_P: bool = False, out: Opti
 
 
 # ----------------------------------------------------------------- schedule --
+def _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status) -> SchedArgs:
+    R, gamma = a.shape
+    s = SchedArgs()
+    s.R, s.gamma = R, gamma
+    s.a, s.sps, s.n_sps = _ptr(a), _ptr(sps), sps.numel()
+    s.b_lo, s.b_step, s.K, s.mode = float(b_lo), float(b_step), int(K), int(mode)
+    s.threshold = float(threshold)
+    s.ell, s.row_off, s.stats = _ptr(outs["ell"]), _ptr(outs["row_off"]), _ptr(outs["stats"])
+    s.order = _ptr(outs.get("order"))
+    s.status = _ptr(status)
+    return s
+
+
 def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: int,
              mode: int = SCHED_EARLY_STOP, *, threshold: float = 0.0, want_order: bool = False,
              out: Optional[dict] = None, status: Optional[torch.Tensor] = None,
@@ -258,19 +280,38 @@ def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: 
         "stats": torch.empty(4, dtype=torch.float64, device=dev)}
     if want_order and "order" not in outs:
         outs["order"] = torch.empty(R * gamma, dtype=torch.int32, device=dev)
-    s = SchedArgs()
-    s.R, s.gamma = R, gamma
-    s.a, s.sps, s.n_sps = _ptr(a), _ptr(sps), sps.numel()
-    s.b_lo, s.b_step, s.K, s.mode = float(b_lo), float(b_step), int(K), int(mode)
-    s.threshold = float(threshold)
-    s.ell, s.row_off, s.stats = _ptr(outs["ell"]), _ptr(outs["row_off"]), _ptr(outs["stats"])
-    s.order = _ptr(outs.get("order"))
-    s.status = _ptr(status)
+    s = _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status)
     _check(lib().spec_schedule(ctypes.byref(s), _stream_handle(stream)), "spec_schedule")
     return outs
 
 
 # ------------------------------------------------------------------- verify --
+def _verify_struct(mode, tgt, tgt_row_off, ell, x, q_tok, lse_q, target_temp, draft,
+                   request_id_base, outs, ws, status):
+    """VerifyArgs plus the DraftArgs it points to (keep it alive for the call)."""
+    R, gamma = x.shape
+    V = tgt.shape[-1]
+    v = VerifyArgs()
+    v.mode, v.R, v.gamma, v.V, v.tgt_dtype = int(mode), R, gamma, V, _dtype_code(tgt)
+    v.request_id_base = request_id_base
+    v.tgt, v.tgt_row_off, v.ell, v.x = _ptr(tgt), _ptr(_dev(tgt_row_off, "tgt_row_off")), \
+        _ptr(_dev(ell, "ell")), _ptr(x)
+    v.q_tok, v.lse_q = _ptr(q_tok), _ptr(lse_q)
+    v.target_temp = float(target_temp)
+    keep = None
+    if draft is not None:
+        keep = _draft_struct(draft, {}, None, None)
+        v.draft = ctypes.pointer(keep)
+    v.accept_len, v.out_tok, v.n_out = _ptr(outs["accept_len"]), _ptr(outs["out_tok"]), \
+        _ptr(outs["n_out"])
+    v.p_tok, v.lse_t = _ptr(outs.get("p_tok")), _ptr(outs.get("lse_t"))
+    v.c_star = _ptr(outs.get("c_star"))
+    v.workspace = _ptr(ws)
+    v.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    v.status = _ptr(status)
+    return v, keep
+
+
 def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.Tensor,
            x: torch.Tensor, seed: int, *, q_tok: Optional[torch.Tensor] = None,
            lse_q: Optional[torch.Tensor] = None, target_temp: float = 1.0,
@@ -294,24 +335,8 @@ def verify(mode: int, tgt: torch.Tensor, tgt_row_off: torch.Tensor, ell: torch.T
         outs["p_tok"] = torch.empty(R, gamma, dtype=torch.float32, device=dev)
         outs["lse_t"] = torch.empty(R, gamma + 1, dtype=torch.float32, device=dev)
     ws = _workspace(workspace_bytes(STAGE_VERIFY, R, gamma, V), dev, workspace)
-    v = VerifyArgs()
-    v.mode, v.R, v.gamma, v.V, v.tgt_dtype = int(mode), R, gamma, V, _dtype_code(tgt)
-    v.request_id_base = request_id_base
-    v.tgt, v.tgt_row_off, v.ell, v.x = _ptr(tgt), _ptr(_dev(tgt_row_off, "tgt_row_off")), \
-        _ptr(_dev(ell, "ell")), _ptr(x)
-    v.q_tok, v.lse_q = _ptr(q_tok), _ptr(lse_q)
-    v.target_temp = float(target_temp)
-    keep = None
-    if draft is not None:
-        keep = _draft_struct(draft, {}, None, None)
-        v.draft = ctypes.pointer(keep)
-    v.accept_len, v.out_tok, v.n_out = _ptr(outs["accept_len"]), _ptr(outs["out_tok"]), \
-        _ptr(outs["n_out"])
-    v.p_tok, v.lse_t = _ptr(outs.get("p_tok")), _ptr(outs.get("lse_t"))
-    v.c_star = _ptr(outs.get("c_star"))
-    v.workspace = _ptr(ws)
-    v.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    v.status = _ptr(status)
+    v, keep = _verify_struct(mode, tgt, tgt_row_off, ell, x, q_tok, lse_q, target_temp, draft,
+                             request_id_base, outs, ws, status)
     _check(lib().spec_verify(ctypes.byref(v), seed & 0xFFFFFFFFFFFFFFFF, _stream_handle(stream)),
            "spec_verify")
     del keep
@@ -398,3 +423,64 @@ def run_round(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.Tenso
                request_id_base=draft_in.request_id_base, out=bufs.get("verify"),
                workspace=bufs.get("ws_verify"), status=bufs.get("status"), stream=stream)
     return {"draft": d, "sched": s, "verify": v}
+
+
+def _host(t: Optional[torch.Tensor], like: torch.Tensor, name: str):
+    """Pointer of a host tensor that mirrors the device tensor ``like``."""
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous host tensor")
+    if t.dtype != like.dtype or t.numel() != like.numel():
+        raise ValueError(f"{name} must match its device buffer ({like.dtype}, {like.numel()} elements)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def run_round_host(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.Tensor,
+                   sps: torch.Tensor, b_lo: float, b_step: float, K: int, seed: int, *,
+                   host_in: dict, host_out: dict, sched_mode: int = SCHED_EARLY_STOP,
+                   sched_threshold: float = 0.0, target_temp: float = 1.0,
+                   bufs: Optional[dict] = None, stream=None) -> dict:
+    """spec_round_host: one round whose per-round inputs come from host tensors
+    ``host_in`` {"U", "h", "x0", "tgt"} (copied into draft_in.U / .h / .x0 and
+    ``tgt``) and whose results go to host tensors ``host_out`` {"out_tok",
+    "accept_len", "n_out", "stats"}; every key is optional.  Page-locked host
+    tensors keep the call asynchronous (synchronise before reading host_out)."""
+    bufs = {} if bufs is None else bufs
+    U = _dev(draft_in.U, "U")
+    R, gamma, V = U.shape
+    dev = U.device
+    d_outs = bufs.get("draft") or draft_outputs(R, gamma, V, dev)
+    ws_d = _workspace(workspace_bytes(STAGE_DRAFT, R, gamma, V, draft_in.A.shape[2]), dev,
+                      bufs.get("ws_draft"))
+    da = _draft_struct(draft_in, d_outs, ws_d, bufs.get("status"))
+    s_outs = bufs.get("sched") or {
+        "ell": torch.empty(R, dtype=torch.int32, device=dev),
+        "row_off": torch.empty(R + 1, dtype=torch.int32, device=dev),
+        "stats": torch.empty(4, dtype=torch.float64, device=dev)}
+    sa = _sched_struct(d_outs["a"], _dev(sps, "sps"), b_lo, b_step, K, sched_mode,
+                       sched_threshold, s_outs, bufs.get("status"))
+    tgt = _dev(tgt, "tgt")
+    v_outs = bufs.get("verify") or {
+        "accept_len": torch.empty(R, dtype=torch.int32, device=dev),
+        "out_tok": torch.empty(R, gamma + 1, dtype=torch.int32, device=dev),
+        "n_out": torch.empty(R, dtype=torch.int32, device=dev)}
+    ws_v = _workspace(workspace_bytes(STAGE_VERIFY, R, gamma, V), dev, bufs.get("ws_verify"))
+    va, keep = _verify_struct(VERIFY_SAMPLE, tgt, tgt_row_off, s_outs["ell"], d_outs["x"],
+                              d_outs["q_tok"], d_outs["lse_q"], target_temp, draft_in,
+                              draft_in.request_id_base, v_outs, ws_v, bufs.get("status"))
+    h = RoundHostArgs()
+    h.draft, h.sched, h.verify = ctypes.pointer(da), ctypes.pointer(sa), ctypes.pointer(va)
+    h.U_host = _host(host_in.get("U"), U, "host U")
+    h.h_host = _host(host_in.get("h"), draft_in.h, "host h")
+    h.x0_host = _host(host_in.get("x0"), draft_in.x0, "host x0")
+    h.tgt_host = _host(host_in.get("tgt"), tgt, "host tgt")
+    h.tgt_rows = tgt.numel() // V
+    h.out_tok_host = _host(host_out.get("out_tok"), v_outs["out_tok"], "host out_tok")
+    h.accept_len_host = _host(host_out.get("accept_len"), v_outs["accept_len"], "host accept_len")
+    h.n_out_host = _host(host_out.get("n_out"), v_outs["n_out"], "host n_out")
+    h.stats_host = _host(host_out.get("stats"), s_outs["stats"], "host stats")
+    _check(lib().spec_round_host(ctypes.byref(h), seed & 0xFFFFFFFFFFFFFFFF, _stream_handle(stream)),
+           "spec_round_host")
+    del keep
+    return {"draft": d_outs, "sched": s_outs, "verify": v_outs}

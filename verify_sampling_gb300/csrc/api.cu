@@ -384,6 +384,52 @@ int spec_calibration(const spec_calibration_args* args, spec_stream_t stream) {
              : SPEC_ERR_CUDA;
 }
 
+int spec_round_host(const spec_round_host_args* args, uint64_t seed, spec_stream_t stream) {
+  if (!args || !args->draft || !args->sched || !args->verify) return SPEC_ERR_INVALID_ARG;
+  const spec_draft_args& d = *args->draft;
+  const spec_sched_args& sc = *args->sched;
+  const spec_verify_args& v = *args->verify;
+  // the stages must be chained through the same device buffers
+  if (sc.R != d.R || sc.gamma != d.gamma || v.R != d.R || v.gamma != d.gamma || v.V != d.V ||
+      v.mode != SPEC_VERIFY_SAMPLE || sc.a != d.a || v.ell != sc.ell || v.x != d.x ||
+      v.q_tok != d.q_tok || v.lse_q != d.lse_q || !v.draft || v.draft->U != d.U ||
+      v.draft->A != d.A || v.draft->Ct != d.Ct || v.draft->x0 != d.x0)
+    return SPEC_ERR_INVALID_ARG;
+  if (!valid_dtype(d.logit_dtype) || !valid_dtype(d.conf_dtype) || !valid_dtype(v.tgt_dtype) ||
+      d.R < 1 || d.gamma < 1 || d.V < 1 || d.d < 0)
+    return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto h2d = [&](const void* dst, const void* src, size_t bytes) {
+    if (!src || bytes == 0) return true;
+    if (!dst) return false;
+    return cudaMemcpyAsync(const_cast<void*>(dst), src, bytes, cudaMemcpyHostToDevice, s) ==
+           cudaSuccess;
+  };
+  const size_t RG = (size_t)d.R * d.gamma;
+  if (!h2d(d.U, args->U_host, RG * d.V * dtype_size(d.logit_dtype)) ||
+      !h2d(d.h, args->h_host, RG * d.d * dtype_size(d.conf_dtype)) ||
+      !h2d(d.x0, args->x0_host, (size_t)d.R * sizeof(int32_t)) ||
+      !h2d(v.tgt, args->tgt_host, args->tgt_rows * d.V * dtype_size(v.tgt_dtype)))
+    return SPEC_ERR_CUDA;
+  int rc = spec_draft_sample(args->draft, seed, stream);
+  if (rc != SPEC_OK) return rc;
+  rc = spec_schedule(args->sched, stream);
+  if (rc != SPEC_OK) return rc;
+  rc = spec_verify(args->verify, seed, stream);
+  if (rc != SPEC_OK) return rc;
+  auto d2h = [&](void* dst, const void* src, size_t bytes) {
+    if (!dst) return true;
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  };
+  if (!d2h(args->out_tok_host, v.out_tok, (size_t)d.R * (d.gamma + 1) * sizeof(int32_t)) ||
+      !d2h(args->accept_len_host, v.accept_len, (size_t)d.R * sizeof(int32_t)) ||
+      !d2h(args->n_out_host, v.n_out, (size_t)d.R * sizeof(int32_t)) ||
+      !d2h(args->stats_host, sc.stats, 4 * sizeof(double)))
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
 }  // extern "C"
+
 
 
