@@ -340,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float nt = valid ? -p.row_m[rj] : 0.f;  // row_m is in log2 units
     const float inv_s = valid ? 1.0f / p.row_s[rj] : 0.f;
     unsigned* row_best = p.row_best + req;
-    const PhiloxRoundKeys rk = philox_round_keys(p.key);
+    // the row-constant parts of the first two Philox rounds, once per thread
+    const PhiloxRow prow = philox_row((uint32_t)k, rid, kPurposeResidual, p.rk);
     // Race on the residual: an element can beat a best (bw, bE) only if
     // 1 - u <= res * bE / bw (filter as in the draft kernel, with the shared
     // per-request bound).  Requests with no positive residual anywhere are
@@ -408,36 +409,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         csum += part;
         continue;
       }
+      float res[16];  // p - q of the 16 columns
+#pragma unroll
+      for (int i = 0; i < 16; ++i) res[i] = tc::ex2(fmaf(L[i], kt, nt)) * inv_s - qv[i];
       const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
+      // All four Philox blocks and the filter of the 16 columns in one
+      // straight-line block; one branch to the rare exact tests.
+      uint32_t words[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int cb = colbase + 8 * h;
-        uint32_t words[8];
+      for (int q = 0; q < 4; ++q) {
+        const uint4 bits = philox_in_row((uint32_t)((colbase >> 2) + q), prow, p.rk);
+        words[4 * q] = bits.x;
+        words[4 * q + 1] = bits.y;
+        words[4 * q + 2] = bits.z;
+        words[4 * q + 3] = bits.w;
+      }
+      uint32_t mask = 0;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint4 bits = philox((uint32_t)((cb >> 2) + q), (uint32_t)k, rid, kPurposeResidual, rk);
-          words[4 * q] = bits.x;
-          words[4 * q + 1] = bits.y;
-          words[4 * q + 2] = bits.z;
-          words[4 * q + 3] = bits.w;
-        }
-        float res[8];
+      for (int i = 0; i < 16; ++i)
+        mask |= (one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f) && res[i] > 0.f) ? (1u << i) : 0u;
+      if (mask) {  // rare: exact race tests, in index order
+        if (colbase + 16 > V) mask &= (V > colbase) ? (1u << (V - colbase)) - 1u : 0u;
+        while (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1u;
+          float ri = res[0];
+          uint32_t wi = words[0];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) res[i] = tc::ex2(fmaf(L[8 * h + i], kt, nt)) * inv_s - qv[8 * h + i];
-        bool any = false;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) any |= one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f);
-        if (any) {  // rare: exact race tests, in index order
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f) && res[i] > 0.f && cb + i < V) {
-              const float E = -logf(uniform_from_word(words[i]));
-              if (race_beats(res[i], E, cb + i, rres.bw, rres.bE, rres.idx)) {
-                rres = WRace{res[i], E, cb + i};
-                c_res = __fdividef(E, res[i]) * kFilterUp;
-                atomicMax(row_best, ordered_key(lg2(res[i]) - lg2(E) - kPublishMargin));
-              }
-            }
+          for (int j = 1; j < 16; ++j) {
+            ri = (i == j) ? res[j] : ri;
+            wi = (i == j) ? words[j] : wi;
+          }
+          const float E = -logf(uniform_from_word(wi));
+          if (race_beats(ri, E, colbase + i, rres.bw, rres.bE, rres.idx)) {
+            rres = WRace{ri, E, colbase + i};
+            c_res = __fdividef(E, ri) * kFilterUp;
+            atomicMax(row_best, ordered_key(lg2(ri) - lg2(E) - kPublishMargin));
           }
         }
       }

@@ -9,6 +9,7 @@ struct ResidTCParams {
   int R, gamma, V, rank, smem_bytes, ntiles, max_mtiles;
   uint32_t rid_base;
   PhiloxKey key;
+  PhiloxRoundKeys rk;  // round keys of `key` (kept in the parameter bank)
   float inv_target_temp;
   const int32_t* x0;
   const int32_t* x;
@@ -32,7 +33,7 @@ struct ResidTCParams {
 // Requests per tile of the residual kernel: few enough that every row copy
 // can span several 64-column tiles and the rows replicate over all four TMEM
 // lane quadrants.
-constexpr int kResTileRows = 32;
+constexpr int kResTileRows = 16;
 
 // Request tiles the residual kernel may need: sum_k ceil(cnt_k / kResTileRows).
 inline int resid_tc_max_mtiles(int R, int gamma) {

@@ -875,6 +875,7 @@ static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_
   t.max_mtiles = resid_tc_max_mtiles(p.R, p.gamma);
   t.rid_base = p.rid_base;
   t.key = p.key;
+  t.rk = p.rk;
   t.inv_target_temp = p.inv_target_temp;
   t.x0 = p.x0;
   t.x = p.x;
