@@ -112,6 +112,34 @@ __global__ void __launch_bounds__(256) draft_probs_kernel(DraftStepParams p) {
 }
 
 // ------------------------------------------------------------ confidence --
+// Lane's share of sum_i a[i] * b[i] over n entries (n a multiple of 16 bytes,
+// both rows 16-byte aligned), added to s.
+__device__ __forceinline__ float dot16(const float* a, const float* b, int n, int lane, float s) {
+  for (int i = 4 * lane; i < n; i += 128) {
+    const float4 x = *reinterpret_cast<const float4*>(a + i);
+    const float4 y = *reinterpret_cast<const float4*>(b + i);
+    s = fmaf(x.x, y.x, s);
+    s = fmaf(x.y, y.y, s);
+    s = fmaf(x.z, y.z, s);
+    s = fmaf(x.w, y.w, s);
+  }
+  return s;
+}
+__device__ __forceinline__ float dot16(const __nv_bfloat16* a, const __nv_bfloat16* b, int n, int lane,
+                                       float s) {
+  for (int i = 8 * lane; i < n; i += 256) {
+    const uint4 x = *reinterpret_cast<const uint4*>(a + i);
+    const uint4 y = *reinterpret_cast<const uint4*>(b + i);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // bf16 -> fp32 is exact: the bits shifted into place
+      s = fmaf(__uint_as_float(xs[j] << 16), __uint_as_float(ys[j] << 16), s);
+      s = fmaf(__uint_as_float(xs[j] & 0xffff0000u), __uint_as_float(ys[j] & 0xffff0000u), s);
+    }
+  }
+  return s;
+}
+
 // One CTA per request, one warp per position (looping when gamma > warps).
 template <typename TC>
 __global__ void __launch_bounds__(kConfThreads) confidence_kernel(ConfParams p) {
@@ -129,8 +157,13 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(ConfParams p) 
     const TC* h = reinterpret_cast<const TC*>(p.h) + ((size_t)r * gamma + (k - 1)) * d;
     const TC* emb = reinterpret_cast<const TC*>(p.W1) + (size_t)x_prev * e;
     float s = 0.f;
-    for (int i = lane; i < d; i += 32) s = fmaf(ld_f(w, i), ld_f(h, i), s);
-    for (int i = lane; i < e; i += 32) s = fmaf(ld_f(w, (size_t)d + i), ld_f(emb, i), s);
+    if (p.vec) {  // 16-byte loads: eight bf16 or four fp32 per lane and step
+      s = dot16(w, h, d, lane, s);
+      s = dot16(w + d, emb, e, lane, s);
+    } else {
+      for (int i = lane; i < d; i += 32) s = fmaf(ld_f(w, i), ld_f(h, i), s);
+      for (int i = lane; i < e; i += 32) s = fmaf(ld_f(w, (size_t)d + i), ld_f(emb, i), s);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_down_sync(0xffffffffu, s, off);
     if (lane == 0) cs[k - 1] = 1.0f / (1.0f + expf(-s / p.sts_temp[k - 1]));
@@ -178,7 +211,12 @@ cudaError_t launch_draft_steps(const DraftStepParams& p, int logit_dtype, int fa
   return launch_draft_typed<__nv_bfloat16, __nv_bfloat16>(p, want_probs, probs_only, stream);
 }
 
-cudaError_t launch_confidence(const ConfParams& p, int conf_dtype, cudaStream_t stream) {
+cudaError_t launch_confidence(const ConfParams& base, int conf_dtype, cudaStream_t stream) {
+  ConfParams p = base;
+  const size_t es = conf_dtype == SPEC_F32 ? 4 : 2;
+  auto al16 = [](const void* q) { return ((uintptr_t)q & 15) == 0; };
+  p.vec = al16(p.h) && al16(p.W1) && al16(p.w) && ((size_t)p.d * es) % 16 == 0 &&
+          ((size_t)p.e * es) % 16 == 0;
   const int threads = std::min(kConfThreads, 32 * std::max(1, p.gamma));
   if (conf_dtype == SPEC_F32)
     confidence_kernel<float><<<p.R, threads, 0, stream>>>(p);

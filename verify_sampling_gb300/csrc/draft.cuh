@@ -41,6 +41,7 @@ struct ConfParams {
   float* c;
   float* a;
   uint32_t* status;
+  bool vec;  // h, W1 and w rows are 16-byte aligned: 16-byte loads
 };
 
 // Number of vocabulary splits per draft row: enough CTAs to cover the GPU
