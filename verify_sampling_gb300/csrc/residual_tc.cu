@@ -51,12 +51,12 @@ __host__ __device__ constexpr uint32_t row_pitch(int w) {
   return (uint32_t)w * kNT * sizeof(T) + 16u;
 }
 
-// 16 consecutive values of `row` from column `col` of a gathered block.
-__device__ __forceinline__ void load_row16(const unsigned char* blk, uint32_t pitch, int row,
-                                           int col, float (&v)[16], float) {
+// 8 consecutive values of `row` from column `col` of a gathered block.
+__device__ __forceinline__ void load_row8(const unsigned char* blk, uint32_t pitch, int row, int col,
+                                          float (&v)[8], float) {
   const unsigned char* base = blk + row * pitch + col * 4;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 2; ++j) {
     const float4 f = *reinterpret_cast<const float4*>(base + 16 * j);
     v[4 * j] = f.x;
     v[4 * j + 1] = f.y;
@@ -64,21 +64,16 @@ __device__ __forceinline__ void load_row16(const unsigned char* blk, uint32_t pi
     v[4 * j + 3] = f.w;
   }
 }
-__device__ __forceinline__ void load_row16(const unsigned char* blk, uint32_t pitch, int row,
-                                           int col, float (&v)[16], __nv_bfloat16) {
-  const unsigned char* base = blk + row * pitch + col * 2;
+__device__ __forceinline__ void load_row8(const unsigned char* blk, uint32_t pitch, int row, int col,
+                                          float (&v)[8], __nv_bfloat16) {
+  const uint4 q = *reinterpret_cast<const uint4*>(blk + row * pitch + col * 2);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint4 q = *reinterpret_cast<const uint4*>(base + 16 * j);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      v[8 * j + 2 * h] = __uint_as_float(w[h] << 16);
-      v[8 * j + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-    }
+  for (int h = 0; h < 4; ++h) {
+    v[2 * h] = __uint_as_float(w[h] << 16);
+    v[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
   }
 }
-
 
 }  // namespace
 
@@ -171,14 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Sr = (int)(fit < (uint32_t)kMaxStages ? fit : (uint32_t)kMaxStages);
   unsigned char* sRow = sC + Sc * kCBytes;
   const uint32_t u_block = (uint32_t)nrows * pitch_u;  // target rows follow the U rows
-  // Few rows leave most TMEM lane quadrants empty, and one warp per SM
-  // sub-partition cannot hide the epilogue's latencies.  So the rows are
-  // replicated: the A tile holds the nq quadrants of requests rho times, and
-  // replica g's quadrants take the tiles t with t % rho == g.
-  const int nq = (nrows + 31) / 32;
-  const int rho = nq == 1 ? 4 : (nq == 2 ? 2 : 1);
-  const int span = 32 * nq;  // A row i holds request slot i % span
-
+  // Sixteen requests fill half of one TMEM lane quadrant, so the A tile holds
+  // them eight times (row i holds request slot i % 16).  In every quadrant,
+  // lanes 16-31 repeat the requests of lanes 0-15 and take the other half of
+  // the warp's columns, and quadrant g takes the tiles t with t % 4 == g: all
+  // 512 epilogue lanes work.
+  static_assert(kResTileRows == 16, "the replication assumes 16-request tiles");
+  constexpr int kSlots = 16;
   for (int i = threadIdx.x; i < 128; i += blockDim.x) {
     int r = -1, trow = 0;
     if (i < nrows) {
@@ -199,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kTmemBufs; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], 4 * nq);  // the warps of the tile's replica
+      tc::mbar_init(&tempty[b], 4);  // the four warps of the tile's quadrant
     }
     abort_flag = 0;
     tc::fence_barrier_init();
@@ -306,10 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue --
     const int quad = warp & 3, grp = warp >> 2;
-    const int row = quad * 32 + lane;
-    const bool holder = quad < nq * rho;  // quadrant of some replica
-    const int replica = quad / nq, slot = row % span;
-    const bool valid = holder && slot < nrows;
+    const int slot = lane & (kSlots - 1), half = lane >> 4;  // request slot, column half
+    const bool valid = slot < nrows;
     // the stages hold exactly nrows rows: lanes past them read row 0 (unused)
     const int lrow = valid ? slot : 0;
     const int V = p.V, rank = p.rank;
@@ -317,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
       const int i = idx / (KC * 8), c = idx % (KC * 8);
       uint4 val = make_uint4(0, 0, 0, 0);
-      if (i % span < nrows) {
-        const int req = s_req[i % span];
+      if (i % kSlots < nrows) {
+        const int req = s_req[i % kSlots];
         int xp = (k == 1) ? p.x0[req] : p.x[(size_t)req * G + (k - 2)];
         if (xp < 0 || xp >= V) xp = 0;
         val = *reinterpret_cast<const uint4*>(Ak + (size_t)xp * rank + c * 8);
@@ -329,13 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_proxy_async();
     named_bar_sync(1, (kEpiWarps + 1) * 32);
 
-    // Per-request constants (log2 units): q = 2^(z kq + nq), p = 2^(L kt + nt) / s_t.
+    // Per-request constants (log2 units): q = 2^(z kq + nlq), p = 2^(L kt + nt) / s_t.
     const int req = valid ? s_req[slot] : 0;
     const uint32_t rid = p.rid_base + (uint32_t)req;
     const size_t rk1 = (size_t)req * G + (k - 1);
     const size_t rj = (size_t)req * G1 + (k - 1);
     const float kq = kLog2e / p.draft_temp[k - 1];
-    const float nq = valid ? -p.lse_q[rk1] * kLog2e : 0.f;
+    const float nlq = valid ? -p.lse_q[rk1] * kLog2e : 0.f;
     const float kt = kLog2e * p.inv_target_temp;
     const float nt = valid ? -p.row_m[rj] : 0.f;  // row_m is in log2 units
     const float inv_s = valid ? 1.0f / p.row_s[rj] : 0.f;
@@ -356,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (abort_flag) break;
       const bool group_done = (t % gw == gw - 1) || (t == T - 1);
       // Every warp waits for each row group (so none runs a ring lap ahead)
-      // and releases it after the group's last tile; only the tile's replica
+      // and releases it after the group's last tile; only the tile's quadrant
       // waits for the accumulator and computes.
-      const bool own = holder && (t % rho == replica);
+      const bool own = (t & 3) == quad;
       if ((t % gw == 0 || own) && !tc::mbar_wait(&full_r[rr.idx], rr.phase, kWaitNs)) {
         fail();
         break;
@@ -379,19 +371,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       const unsigned char* sr = sRow + rr.idx * rstage;
-      const int col = (t % gw) * kNT + grp * 16;
-      // q first (frees the bias and U registers), then the target row.
-      float qv[16], L[16];
+      const int col = (t % gw) * kNT + grp * 16 + 8 * half;
+      // q first (frees the bias and U registers), then the target row: the
+      // lane's 8 columns of the warp's 16.
+      float qv[8], L[8];
       {
         uint32_t braw[16];
-        float u[16];
+        float u[8];
         tc::tmem_ld16(t_lane + (uint32_t)(rb.idx * kNT), braw);
-        load_row16(sr, pitch_u, lrow, col, u, TL());
+        load_row8(sr, pitch_u, lrow, col, u, TL());
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) qv[c] = tc::ex2(fmaf(u[c] + __uint_as_float(braw[c]), kq, nq));
+        for (int c = 0; c < 8; ++c) {
+          const float b = __uint_as_float(half ? braw[8 + c] : braw[c]);
+          qv[c] = tc::ex2(fmaf(u[c] + b, kq, nlq));
+        }
       }
-      load_row16(sr + u_block, pitch_t, lrow, col, L, TT());
+      load_row8(sr + u_block, pitch_t, lrow, col, L, TT());
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -400,24 +396,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (group_done) rr.next(Sr);
       if (!valid) continue;
-      const int colbase = (t_begin + t) * kNT + grp * 16;
+      const int colbase = (t_begin + t) * kNT + grp * 16 + 8 * half;
       if constexpr (kCStar) {
         float part = 0.f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
+        for (int c = 0; c < 8; ++c)
           if (colbase + c < V) part += fminf(tc::ex2(fmaf(L[c], kt, nt)) * inv_s, qv[c]);
         csum += part;
         continue;
       }
-      float res[16];  // p - q of the 16 columns
+      float res[8];  // p - q of the 8 columns
 #pragma unroll
-      for (int i = 0; i < 16; ++i) res[i] = tc::ex2(fmaf(L[i], kt, nt)) * inv_s - qv[i];
+      for (int i = 0; i < 8; ++i) res[i] = tc::ex2(fmaf(L[i], kt, nt)) * inv_s - qv[i];
       const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
-      // All four Philox blocks and the filter of the 16 columns in one
-      // straight-line block; one branch to the rare exact tests.
-      uint32_t words[16];
+      // Both Philox blocks and the filter of the 8 columns in one straight-line
+      // block; one branch to the rare exact tests.
+      uint32_t words[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const uint4 bits = philox_in_row((uint32_t)((colbase >> 2) + q), prow, p.rk);
         words[4 * q] = bits.x;
         words[4 * q + 1] = bits.y;
@@ -426,17 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t mask = 0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
+      for (int i = 0; i < 8; ++i)
         mask |= (one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f) && res[i] > 0.f) ? (1u << i) : 0u;
       if (mask) {  // rare: exact race tests, in index order
-        if (colbase + 16 > V) mask &= (V > colbase) ? (1u << (V - colbase)) - 1u : 0u;
+        if (colbase + 8 > V) mask &= (V > colbase) ? (1u << (V - colbase)) - 1u : 0u;
         while (mask) {
           const int i = __ffs(mask) - 1;
           mask &= mask - 1u;
           float ri = res[0];
           uint32_t wi = words[0];
 #pragma unroll
-          for (int j = 1; j < 16; ++j) {
+          for (int j = 1; j < 8; ++j) {
             ri = (i == j) ? res[j] : ri;
             wi = (i == j) ? words[j] : wi;
           }
@@ -450,18 +446,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if constexpr (kCStar) {
-      // column groups, replicas and splits all add into the row's sum
+      // quadrants, column groups, halves and splits all add into the row's sum
       if (valid && !abort_flag) atomicAdd(&p.c_star[rk1], csum);
     } else {
-      // merge the column groups and replicas of each request through shared
-      // memory: [4 * rho][span] states, slot (replica * 4 + grp, request slot)
+      // merge the 32 states of each request (quadrant, column group, column
+      // half) through shared memory: [32][16]
       WRace* st_all = reinterpret_cast<WRace*>(sC);
-      const int nst = 4 * rho;
+      constexpr int kStates = 32;
       named_bar_sync(2, kEpiWarps * 32);
-      if (valid) st_all[(replica * 4 + grp) * span + slot] = rres;
+      if (valid) st_all[((quad * 4 + grp) * 2 + half) * kSlots + slot] = rres;
       named_bar_sync(2, kEpiWarps * 32);
-      if (valid && replica == 0 && grp == 0) {
-        for (int g = 1; g < nst; ++g) rres = wrace_merge_(rres, st_all[g * span + slot]);
+      if (valid && quad == 0 && grp == 0 && half == 0) {
+        for (int g = 1; g < kStates; ++g) rres = wrace_merge_(rres, st_all[g * kSlots + slot]);
         Partial pw{};
         pw.f0 = rres.bw;
         pw.f1 = rres.bE;
