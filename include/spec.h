@@ -142,8 +142,9 @@ int spec_draft_sample(const spec_draft_args *args, uint64_t seed, spec_stream_t 
  * device memory (held by every GPU that loads the library until exit); it
  * calls no cudaMalloc or cudaFree.  Returns SPEC_ERR_UNSUPPORTED when the
  * sizes need more scratch than that (the need is about
- * 32 * R * splits + 4 * R * (1 + gamma) bytes, with at most 152 splits per
- * 128 requests on a GB300).  The first call on each device resolves the
+ * 64 * R * splits + 4 * R * (1 + gamma) bytes on the tensor-core path, two
+ * slots of split partials, with at most 152 splits per 128 requests on a
+ * GB300, and 32 * R * splits + 4 * R * (1 + gamma) on the generic one).  The first call on each device resolves the
  * array's device address (cudaGetSymbolAddress); make it before any stream
  * capture.  All calls share the array: calls that overlap on the GPU race and
  * give wrong results. */

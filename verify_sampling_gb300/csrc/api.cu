@@ -23,11 +23,15 @@ size_t dtype_size(int d) { return d == SPEC_F32 ? 4 : 2; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // Partials: the larger of the generic kernel's [R, nsplit] and the fused
-// kernel's [R, splits <= kMaxDeviceSms]; counters: one per request (generic)
-// or per 128-request tile (fused).
+// kernel's two slots of [R, splits <= kMaxDeviceSms] (positions alternate, so
+// a position's partials survive until the next position's grid has merged
+// them); counters: one per request (generic) or per 128-request tile (fused).
+size_t draft_partials_bytes(int R, int V) {
+  const size_t ns = (size_t)std::max(draft_nsplit(R, V), 2 * kMaxDeviceSms);
+  return align256((size_t)R * ns * sizeof(Partial));
+}
 size_t draft_scratch_bytes(int R, int gamma, int V) {
-  const size_t ns = (size_t)std::max(draft_nsplit(R, V), kMaxDeviceSms);
-  return align256((size_t)R * ns * sizeof(Partial)) + align256((size_t)R * (1 + gamma) * sizeof(unsigned));
+  return draft_partials_bytes(R, V) + align256((size_t)R * (1 + gamma) * sizeof(unsigned));
 }
 
 // The fused tensor-core path needs bf16 factors with r a multiple of 64, 16-byte
@@ -144,8 +148,7 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
   p.lse_q = a.lse_q;
   p.P_out = a.P_out;
   p.partials = reinterpret_cast<Partial*>(ws);
-  const size_t cnt_off =
-      align256((size_t)a.R * std::max(nsplit, kMaxDeviceSms) * sizeof(Partial));
+  const size_t cnt_off = draft_partials_bytes(a.R, a.V);  // counters follow the partials
   p.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
   p.status = a.status;
   // counters [R] and the fused kernel's shared race bounds [gamma, R], zeroed together

@@ -83,7 +83,7 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
   const int nsplit_generic = draft_nsplit(a.R, a.V);
   const int nsplit_tc = tc ? draft_tc_nsplit(a.R, a.V, sms) : 0;
   const size_t part_bytes =
-      round256((size_t)a.R * (tc ? nsplit_tc : nsplit_generic) * sizeof(Partial));
+      round256((size_t)a.R * (tc ? 2 * nsplit_tc : nsplit_generic) * sizeof(Partial));
   const size_t cnt_bytes = (size_t)a.R * (1 + a.gamma) * sizeof(unsigned);
   if (part_bytes + cnt_bytes > kStaticScratchBytes) return SPEC_ERR_UNSUPPORTED;
   char* ws = static_cast<char*>(scratch_address(dev));

@@ -44,6 +44,48 @@ namespace {
 
 using namespace fused;
 
+// The 512 epilogue threads merge the split partials of position `kpos` for
+// the tile's 128 requests, four threads per request with all of a thread's
+// loads in flight (one round trip up to 48 splits).  Writes x, q_tok and lse_q
+// of that position when `write`, and the token into s_x (nullable).
+__device__ __forceinline__ void merge_position(const DraftTCParams& p, const Partial* part, int m0,
+                                               int kpos, bool write, int* s_x) {
+  const int row = threadIdx.x >> 2, lp = threadIdx.x & 3, m = m0 + row;
+  Race acc = race_empty();
+  if (m < p.R) {
+    const Partial* src = part + (size_t)m * p.nsplit;
+    for (int s0 = lp; s0 < p.nsplit; s0 += 48) {
+      Partial w[12];
+#pragma unroll
+      for (int q = 0; q < 12; ++q)
+        if (s0 + 4 * q < p.nsplit) w[q] = load_partial(src + s0 + 4 * q);
+#pragma unroll
+      for (int q = 0; q < 12; ++q)
+        if (s0 + 4 * q < p.nsplit) acc = race_merge2(acc, Race{w[q].f0, w[q].f1, w[q].f2, w[q].f3, w[q].i0});
+    }
+  }
+  acc = race_merge2(acc, race_shfl_xor(acc, 1));
+  acc = race_merge2(acc, race_shfl_xor(acc, 2));
+  if (lp != 0) return;
+  if (s_x) s_x[row] = m < p.R ? acc.idx : -1;
+  if (write && m < p.R) {
+    const size_t o = (size_t)m * p.gamma + (kpos - 1);
+    p.x[o] = acc.idx;
+    p.q_tok[o] = acc.be / acc.s;
+    // lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s with m in log2 units;
+    // s = 2^k f with f in [1, 2): lse = (m + k) ln 2 + ln f, so only a small
+    // logarithm is taken and one fp64 multiply-add keeps m + k exact.
+    int ks;
+    const float f = 2.f * frexpf(acc.s, &ks);
+    p.lse_q[o] = (float)fma((double)acc.m + (double)(ks - 1), 0.6931471805599453, (double)logf(f));
+  }
+}
+
+// Split partials of position kpos: two slots, alternating with the position.
+__device__ __forceinline__ Partial* partial_slot(const DraftTCParams& p, int kpos) {
+  return p.partials + (size_t)(kpos & 1) * p.R * p.nsplit;
+}
+
 // Cold path: exact race test of one filtered element; on a new best, publish
 // the row's score to the CTA (and, when it raises the CTA's bound, to the
 // row's word in global memory) and return true.
@@ -89,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t tfull[kTmemBufs], tempty[kTmemBufs];
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t s_best[128];  // per tile row: best race score so far (ordered key, 0 = none)
+  __shared__ int s_x[128];          // x_{k-1} of the tile's requests, merged here
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,9 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3, grp = warp >> 2;
     const int row = quad * 32 + lane, m = m0 + row;
     const bool valid = m < p.R;
-    const int V = p.V, rank = p.rank, gamma = p.gamma;
+    const int V = p.V, rank = p.rank;
 
-    tc::grid_dep_wait();  // x_{k-1} written by the previous position's grid
+    tc::grid_dep_wait();  // the previous position's partials are written
+    // x_{k-1}: every CTA of the tile merges the previous position's split
+    // partials itself (the previous grid ends without a merge on its critical
+    // path); the CTA of split 0 also writes that position's outputs.
+    if (k > 1) {
+      merge_position(p, partial_slot(p, k - 1), m0, k - 1, split == 0, s_x);
+      named_bar_sync(2, kEpiWarps * 32);
+    }
     // Gather A_k[x_{k-1}] for the tile's 128 requests: 128 x r bf16 in 16-byte
     // chunks, 2*KC per thread, all loads in flight before the stores.
     const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
@@ -209,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int idx = threadIdx.x + j * kEpiWarps * 32, mm = m0 + idx / (KC * 8);
-        xp[j] = mm < p.R ? ((k == 1) ? p.x0[mm] : p.x[(size_t)mm * gamma + (k - 2)]) : -1;
+        xp[j] = mm < p.R ? ((k == 1) ? p.x0[mm] : s_x[idx / (KC * 8)]) : -1;
       }
       uint4 val[kPer];
 #pragma unroll
@@ -432,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.f2 = st.be;
       w.f3 = st.bE;
       w.i0 = st.idx;
-      p.partials[(size_t)m * p.nsplit + split] = w;
+      partial_slot(p, k)[(size_t)m * p.nsplit + split] = w;
     }
   }
 
@@ -443,41 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  // Positions before the last are merged by the next position's grid.
+  if (k < p.gamma) return;
   if (!last_block_arrives(p.counters + mtile, (unsigned)p.nsplit)) return;
 
-  // Last CTA of this request tile: merge the partials of every split, four
-  // threads per request.
-  if (threadIdx.x < kEpiWarps * 32) {
-    const int row = threadIdx.x >> 2, part = threadIdx.x & 3, m = m0 + row;
-    Race acc = race_empty();
-    if (m < p.R) {
-      // splits part, part + 4, ...: twelve loads in flight per round trip
-      // (one round trip for up to 48 splits)
-      const Partial* src = p.partials + (size_t)m * p.nsplit;
-      for (int s0 = part; s0 < p.nsplit; s0 += 48) {
-        Partial w[12];
-#pragma unroll
-        for (int q = 0; q < 12; ++q)
-          if (s0 + 4 * q < p.nsplit) w[q] = load_partial(src + s0 + 4 * q);
-#pragma unroll
-        for (int q = 0; q < 12; ++q)
-          if (s0 + 4 * q < p.nsplit) acc = race_merge2(acc, Race{w[q].f0, w[q].f1, w[q].f2, w[q].f3, w[q].i0});
-      }
-    }
-    acc = race_merge2(acc, race_shfl_xor(acc, 1));
-    acc = race_merge2(acc, race_shfl_xor(acc, 2));
-    if (part == 0 && m < p.R) {
-      const size_t o = (size_t)m * p.gamma + (k - 1);
-      p.x[o] = acc.idx;
-      p.q_tok[o] = acc.be / acc.s;
-      // lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s with m in log2 units;
-      // s = 2^k f with f in [1, 2): lse = (m + k) ln 2 + ln f, so only a small
-      // logarithm is taken and one fp64 multiply-add keeps m + k exact.
-      int ks;
-      const float f = 2.f * frexpf(acc.s, &ks);
-      p.lse_q[o] = (float)fma((double)acc.m + (double)(ks - 1), 0.6931471805599453, (double)logf(f));
-    }
-  }
+  // Last CTA of this request tile at the last position: merge its partials.
+  if (threadIdx.x < kEpiWarps * 32) merge_position(p, partial_slot(p, k), m0, k, true, nullptr);
 }
 
 // ------------------------------------------------------------------ host --

@@ -19,7 +19,7 @@ struct DraftTCParams {
   int32_t* x;
   float* q_tok;
   float* lse_q;
-  Partial* partials;   // [R, nsplit]
+  Partial* partials;   // [2][R, nsplit]: slot k % 2 holds position k's split partials
   unsigned* counters;  // [mtiles], zero on entry
   unsigned* row_best;  // [gamma, R] best race score per row over all CTAs (ordered keys), zero on entry
   uint32_t* status;
