@@ -390,16 +390,17 @@ def main():
         per_launch = R * (G + 1) * V * es_u
         dur_ms = ms / args.steps
         kernel = "verify_rows (greedy argmax, all R*(gamma+1) rows)"
-        launches = 1
+        launches = 2  # row plan, row pass
     else:
         # dominant kernel: the draft step, gamma launches per round; one launch
         # streams the R backbone rows of position k and the factor C_k.
         per_launch = R * V * es_u + V * wl.r * es_f
         dur_ms = stage_ms["draft"] / (args.steps * G)
         kernel = "draft_step (one launch per position k)"
-        # per round: gamma draft steps, confidence, schedule, verify rows,
-        # fused residual, residual fallback (gated, exits at once when unused)
-        launches = G + 5 + (1 if acc_tab is not None else 0) + (3 if calib is not None else 0)
+        # per round: gamma draft steps, confidence, schedule, verify row plan,
+        # verify rows, fused residual, residual fallback (gated, exits at once
+        # when unused); the EMA update; the c* plan, c* pass and diagram
+        launches = G + 6 + (1 if acc_tab is not None else 0) + (3 if calib is not None else 0)
     achieved = per_launch / (dur_ms / 1000.0) / 1e9
     traffic = None if greedy else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
