@@ -1,0 +1,27 @@
+"""The benchmark's reference arm (the oracle on the host cores) prints the one
+JSON line the harness reads, for a sampled workload and for the greedy one
+(CPU only)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("config", ["c2", "greedy"])
+def test_reference_arm_json_line(config):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", config, "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == "draft+verified positions/s"
+    assert line["value"] > 0 and line["unit"] == "positions/s" and line["higher_is_better"]
+    assert line["steps"] == 1 and line["warmup"] == 1 and line["config"]["workload"] == config
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
