@@ -71,11 +71,14 @@ def lib() -> ctypes.CDLL:
         L.orc_schedule.argtypes = [i32, i32, P, P, i32, f64, f64, i32, i32, f64, P, P, P, P, P, P]
         L.orc_schedule.restype = i32
         L.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, P, i64, P, P, i32, P, P,
-                                 u64, u32, P, P, P, P, P]
+                                 u64, u32, P, P, P, P, P, P]
         L.orc_verify.restype = i32
         L.orc_accept_stats.argtypes = [i32, i32, P, P, i32, i32, f64, i32, P, P, P, P]
         L.orc_accept_stats.restype = i32
-        L.orc_cstar.argtypes = [i32, i32, i32, P, P, P, P, f64, P, i64, P, P, i32, P, P, P]
+        L.orc_cstar.argtypes = [i32, i32, i32, P, P, P, P, f64, P, i64, P, P, i32, P, P, P, P]
+        L.orc_draft_rnn.argtypes = [i32, i32, i32, i32, P, i64, P, P, P, P, P, u64, u32, i32, P, P,
+                                    P, P, P, P, P]
+        L.orc_draft_rnn.restype = i32
         L.orc_cstar.restype = i32
         L.orc_calibration.argtypes = [i32, i32, P, P, P, i32, P, P, P, P, P]
         L.orc_calibration.restype = i32
@@ -228,7 +231,7 @@ class VerifyOut:
 
 
 def verify(mode: int, tgt, row_off, ell, x, q_tok, target_temp: float, U, A, Ct, x0, draft_temp,
-           seed: int, rid_base: int = 0) -> VerifyOut:
+           seed: int, rid_base: int = 0, S=None) -> VerifyOut:
     """tgt [rows, V]; row (r, j) = row_off[r] + j - 1.  U [R, gamma, V]; A, Ct [gamma, V, r]."""
     tgt = _f32(tgt)
     V = tgt.shape[-1]
@@ -253,7 +256,7 @@ def verify(mode: int, tgt, row_off, ell, x, q_tok, target_temp: float, U, A, Ct,
     rc = lib().orc_verify(mode, R, gamma, V, _ptr(tgt), _ptr(row_off), _ptr(ell), _ptr(x), _ptr(q),
                           target_temp, _ptr(U), gamma * V, _ptr(A), _ptr(Ct), r, _ptr(x0),
                           _ptr(temp), seed, rid_base, _ptr(acc), _ptr(out), _ptr(n_out), _ptr(mg),
-                          _ptr(js))
+                          _ptr(js), _ptr(None if S is None else _f32(S)))
     if rc != 0:
         raise ValueError(f"orc_verify failed ({rc})")
     return VerifyOut(acc, out, n_out, mg, js)
@@ -280,7 +283,7 @@ def accept_stats(ell, accept_len, ema, count, bucket: int, beta: float, min_coun
 
 
 # --------------------------------------------------- calibration diagnostics --
-def cstar(tgt, row_off, ell, x, target_temp: float, U, A, Ct, x0, draft_temp) -> np.ndarray:
+def cstar(tgt, row_off, ell, x, target_temp: float, U, A, Ct, x0, draft_temp, S=None) -> np.ndarray:
     """c* = sum_v min(p_v, q_v) for every verified draft row (r, j <= l_r);
     NaN past l_r.  Layouts as in ``verify``."""
     tgt = _f32(tgt)
@@ -292,7 +295,8 @@ def cstar(tgt, row_off, ell, x, target_temp: float, U, A, Ct, x0, draft_temp) ->
     out = np.zeros((R, gamma))
     rc = lib().orc_cstar(R, gamma, V, _ptr(tgt), _ptr(_i32(row_off)), _ptr(_i32(ell)), _ptr(x),
                          float(target_temp), _ptr(U), gamma * V, _ptr(A), _ptr(Ct), A.shape[2],
-                         _ptr(_i32(x0)), _ptr(_f32(draft_temp)), _ptr(out))
+                         _ptr(_i32(x0)), _ptr(_f32(draft_temp)), _ptr(out),
+                         _ptr(None if S is None else _f32(S)))
     if rc != 0:
         raise ValueError(f"orc_cstar failed ({rc})")
     return out
@@ -313,3 +317,35 @@ def calibration(c, ell, accept_len, count, sum_c, sum_acc):
     if rc != 0:
         raise ValueError(f"orc_calibration failed ({rc})")
     return ece.value, bad.value
+
+
+# ------------------------------------------------------------------ RNN head --
+@dataclass
+class DraftRnnOut:
+    x: np.ndarray       # [R, gamma] int32
+    q_tok: np.ndarray   # [R, gamma] f64
+    lse: np.ndarray     # [R, gamma] f64
+    gap: np.ndarray     # [R, gamma] f64
+    S: np.ndarray       # [R, gamma, r] f64 stored states
+
+
+def draft_rnn(U, A, Ct, W, x0, draft_temp, seed: int, rid_base: int = 0, bf16_state: bool = True,
+              x_cond=None, s_cond=None) -> DraftRnnOut:
+    """RNN sequential head: s_k = store(tanh(A_k[x_{k-1}] + s_{k-1} W_k)),
+    B_k = s_k C_k.  U [R, gamma, V]; A, Ct [gamma, V, r]; W [gamma, r, r]."""
+    U = _f32(U)
+    R, gamma, V = U.shape
+    A, Ct, W = _f32(A), _f32(Ct), _f32(W)
+    r = A.shape[2]
+    assert W.shape == (gamma, r, r)
+    x = np.zeros((R, gamma), np.int32)
+    q, l, g = (np.zeros((R, gamma)) for _ in range(3))
+    S = np.zeros((R, gamma, r))
+    xc = None if x_cond is None else _i32(x_cond)
+    sc = None if s_cond is None else _f32(s_cond)
+    rc = lib().orc_draft_rnn(R, gamma, V, r, _ptr(U), gamma * V, _ptr(A), _ptr(Ct), _ptr(W),
+                             _ptr(_i32(x0)), _ptr(_f32(draft_temp)), seed, rid_base, int(bf16_state),
+                             _ptr(xc), _ptr(sc), _ptr(x), _ptr(q), _ptr(l), _ptr(g), _ptr(S))
+    if rc != 0:
+        raise ValueError(f"orc_draft_rnn failed ({rc})")
+    return DraftRnnOut(x, q, l, g, S)

@@ -21,6 +21,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <limits>
 #include <vector>
 
@@ -124,16 +125,51 @@ int gumbel_argmax(const std::vector<double>& logw, const Stream& rng, uint32_t j
 // logits at position k given the previous token x_prev:
 //   z_v = (U_k[v] + B_k(x_prev)[v]) / T_k,   B_k(x)[v] = sum_i A_k[x, i] * C_k[i, v]
 // with the low-rank factors stored A_k as [V, r] and C_k transposed as [V, r].
-void draft_logits(int V, int r, const float* Uk, const float* Ak, const float* Ctk, int x_prev,
-                  double temp, std::vector<double>& z) {
+// The same with the bias taken from an explicit rank-r row: B_k[v] = row . C_k[:, v].
+void draft_logits_row(int V, int r, const float* Uk, const double* row, const float* Ctk,
+                      double temp, std::vector<double>& z) {
   z.assign((size_t)V, 0.0);
-  const float* arow = Ak + (size_t)x_prev * (size_t)r;
   for (int v = 0; v < V; ++v) {
     const float* crow = Ctk + (size_t)v * (size_t)r;
     double bias = 0.0;
-    for (int i = 0; i < r; ++i) bias += (double)arow[i] * (double)crow[i];
+    for (int i = 0; i < r; ++i) bias += row[i] * (double)crow[i];
     z[(size_t)v] = ((double)Uk[v] + bias) / temp;
   }
+}
+
+void draft_logits(int V, int r, const float* Uk, const float* Ak, const float* Ctk, int x_prev,
+                  double temp, std::vector<double>& z) {
+  const float* arow = Ak + (size_t)x_prev * (size_t)r;
+  std::vector<double> row(arow, arow + r);
+  draft_logits_row(V, r, Uk, row.data(), Ctk, temp, z);
+}
+
+// Draft logits of (req, j): the Markov row A_j[x_prev], or, when S is given
+// (the RNN head), the stored state S[req, j-1, :].
+void draft_logits_at(int V, int r, const float* Uk, const float* A, const float* Ct,
+                     const float* S, int gamma, int req, int j, int x_prev, double temp,
+                     std::vector<double>& z) {
+  const float* Ctk = Ct + (size_t)(j - 1) * V * r;
+  if (S) {
+    const float* srow = S + ((size_t)req * gamma + (j - 1)) * r;
+    std::vector<double> row(srow, srow + r);
+    draft_logits_row(V, r, Uk, row.data(), Ctk, temp, z);
+  } else {
+    draft_logits(V, r, Uk, A + (size_t)(j - 1) * V * r, Ctk, x_prev, temp, z);
+  }
+}
+
+// bf16 rounding (round to nearest, ties to even) of a value, as a double.
+double round_bf16(double v) {
+  const float f = (float)v;  // first to fp32, as a device stores its fp32 result
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  if ((b & 0x7f800000u) == 0x7f800000u) return (double)f;  // inf / nan
+  const uint32_t lsb = (b >> 16) & 1u;
+  b = (b + 0x7fffu + lsb) & 0xffff0000u;
+  float o;
+  std::memcpy(&o, &b, 4);
+  return (double)o;
 }
 
 // SPS(B) from a table sampled at B_i = b_lo + i * b_step: linear interpolation
@@ -228,6 +264,67 @@ int orc_draft(int R, int gamma, int V, int r, const float* U, int64_t U_rstride,
   }
   return 0;
 }
+
+// ------------------------------------------------------------ RNN head ---
+// [DSpark] "第二阶段：轻量顺序头": the sequential head comes in two forms, the
+// Markov head (only the previous token, low-rank) and an RNN head that keeps a
+// recurrent state for longer dependencies.  The pages give no formula for the
+// latter; this library's reading is an Elman state in the same rank-r space:
+//   s_0 = 0,  s_k = store(tanh(A_k[x_{k-1}] + s_{k-1} W_k)),  B_k = s_k C_k,
+// with W_k [r, r] per position (row i maps s_{k-1}[i] to column j) and
+// store() the state's storage precision (bf16 when `bf16_state`, else fp32).
+// Everything else is the Markov draft: z = (U_k + B_k) / T_k, Gumbel-max with
+// the purpose-0 stream.  S_out [R, gamma, r] receives the stored states.
+// x_cond (nullable) replaces the sampled tokens as in orc_draft; s_cond
+// (nullable, [R, gamma, r]) replaces the state carried to the next position
+// and used for the bias, which lets a test feed the device's states.
+int orc_draft_rnn(int R, int gamma, int V, int r, const float* U, int64_t U_rstride,
+                  const float* A, const float* Ct, const float* W, const int32_t* x0,
+                  const float* draft_temp, uint64_t seed, uint32_t rid_base, int bf16_state,
+                  const int32_t* x_cond, const float* s_cond, int32_t* x, double* q_tok,
+                  double* lse, double* gap, double* S_out) {
+  if (R < 0 || gamma <= 0 || V <= 0 || r <= 0) return -1;
+  Stream rng(seed);
+  std::vector<double> z, st((size_t)r), prev((size_t)r);
+  for (int req = 0; req < R; ++req) {
+    const uint32_t rid = rid_base + (uint32_t)req;
+    int x_prev = x0[req];
+    std::fill(prev.begin(), prev.end(), 0.0);
+    for (int k = 1; k <= gamma; ++k) {
+      if (x_prev < 0 || x_prev >= V) return -2;
+      const size_t kk = (size_t)(k - 1);
+      const float* arow = A + kk * (size_t)V * r + (size_t)x_prev * r;
+      const float* Wk = W + kk * (size_t)r * r;
+      for (int j = 0; j < r; ++j) {
+        double pre = (double)arow[j];
+        for (int i = 0; i < r; ++i) pre += prev[(size_t)i] * (double)Wk[(size_t)i * r + j];
+        const double t = std::tanh(pre);
+        st[(size_t)j] = bf16_state ? round_bf16(t) : (double)(float)t;
+      }
+      const size_t o = (size_t)req * gamma + kk;
+      for (int j = 0; j < r; ++j) S_out[o * r + j] = st[(size_t)j];
+      const double* use = st.data();
+      std::vector<double> cond;
+      if (s_cond) {
+        cond.assign(s_cond + o * r, s_cond + o * r + r);
+        use = cond.data();
+      }
+      draft_logits_row(V, r, U + (size_t)req * U_rstride + kk * V, use, Ct + kk * (size_t)V * r,
+                       (double)draft_temp[kk], z);
+      const double l = log_sum_exp(z);
+      double g;
+      const int xk = gumbel_argmax(z, rng, (uint32_t)k, rid, kDraftGumbel, &g);
+      x[o] = xk;
+      q_tok[o] = std::exp(z[(size_t)xk] - l);
+      lse[o] = l;
+      if (gap) gap[o] = g;
+      for (int j = 0; j < r; ++j) prev[(size_t)j] = use[j];
+      x_prev = x_cond ? x_cond[o] : xk;
+    }
+  }
+  return 0;
+}
+
 
 // ------------------------------------------------------------- confidence ---
 // [DSpark] "2.1 置信度头": c_k = sigmoid(w . [h_k ; W1[x_{k-1}]]), with the
@@ -360,7 +457,7 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
                const float* U, int64_t U_rstride, const float* A, const float* Ct, int r,
                const int32_t* x0, const float* draft_temp, uint64_t seed, uint32_t rid_base,
                int32_t* accept_len, int32_t* out_tok, int32_t* n_out, double* margin,
-               int32_t* jstar_out) {
+               int32_t* jstar_out, const float* S) {
   if ((mode != 0 && mode != 1) || R < 0 || gamma <= 0 || V <= 0) return -1;
   Stream rng(seed);
   std::vector<double> zt, p, zq;
@@ -428,9 +525,8 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
         const int kk = jstar - 1;
         const int x_prev = (jstar == 1) ? x0[req] : xr[jstar - 2];
         if (x_prev < 0 || x_prev >= V) return -3;
-        draft_logits(V, r, U + (size_t)req * (size_t)U_rstride + (size_t)kk * V,
-                     A + (size_t)kk * V * r, Ct + (size_t)kk * V * r, x_prev,
-                     (double)draft_temp[kk], zq);
+        draft_logits_at(V, r, U + (size_t)req * (size_t)U_rstride + (size_t)kk * V, A, Ct, S,
+                        gamma, req, jstar, x_prev, (double)draft_temp[kk], zq);
         double l_q = log_sum_exp(zq);
         std::vector<double> logres((size_t)V, kNegInf);
         bool any = false;
@@ -547,7 +643,7 @@ int orc_accept_stats(int R, int gamma, const int32_t* ell, const int32_t* accept
 int orc_cstar(int R, int gamma, int V, const float* tgt, const int32_t* row_off,
               const int32_t* ell, const int32_t* x, double target_temp, const float* U,
               int64_t U_rstride, const float* A, const float* Ct, int r, const int32_t* x0,
-              const float* draft_temp, double* c_star) {
+              const float* draft_temp, double* c_star, const float* S) {
   if (R < 0 || gamma <= 0 || V <= 0 || r <= 0 || !(target_temp > 0.0)) return -1;
   std::vector<double> zt((size_t)V), zq;
   for (int req = 0; req < R; ++req) {
@@ -562,9 +658,8 @@ int orc_cstar(int R, int gamma, int V, const float* tgt, const int32_t* row_off,
       const float* row = tgt + (size_t)(row_off[req] + j - 1) * V;
       for (int v = 0; v < V; ++v) zt[(size_t)v] = (double)row[v] / target_temp;
       const int xp = (j == 1) ? x0[req] : x[(size_t)req * gamma + (j - 2)];
-      draft_logits(V, r, U + (size_t)req * U_rstride + (size_t)(j - 1) * V,
-                   A + (size_t)(j - 1) * V * r, Ct + (size_t)(j - 1) * V * r, xp,
-                   (double)draft_temp[j - 1], zq);
+      draft_logits_at(V, r, U + (size_t)req * U_rstride + (size_t)(j - 1) * V, A, Ct, S, gamma,
+                      req, j, xp, (double)draft_temp[j - 1], zq);
       out = orc_accept_prob(V, zt.data(), zq.data());
     }
   }
