@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
         L.orc_accept_stats.restype = i32
         L.orc_cstar.argtypes = [i32, i32, i32, P, P, P, P, f64, P, i64, P, P, i32, P, P, P, P]
         L.orc_draft_rnn.argtypes = [i32, i32, i32, i32, P, i64, P, P, P, P, P, u64, u32, i32, P, P,
-                                    P, P, P, P, P]
+                                    P, P, P, P, P, P]
         L.orc_draft_rnn.restype = i32
         L.orc_cstar.restype = i32
         L.orc_calibration.argtypes = [i32, i32, P, P, P, i32, P, P, P, P, P]
@@ -327,10 +327,11 @@ class DraftRnnOut:
     lse: np.ndarray     # [R, gamma] f64
     gap: np.ndarray     # [R, gamma] f64
     S: np.ndarray       # [R, gamma, r] f64 stored states
+    P: np.ndarray | None = None  # [R, gamma, V] draft distributions (want_P)
 
 
 def draft_rnn(U, A, Ct, W, x0, draft_temp, seed: int, rid_base: int = 0, bf16_state: bool = True,
-              x_cond=None, s_cond=None) -> DraftRnnOut:
+              x_cond=None, s_cond=None, want_P: bool = False) -> DraftRnnOut:
     """RNN sequential head: s_k = store(tanh(A_k[x_{k-1}] + s_{k-1} W_k)),
     B_k = s_k C_k.  U [R, gamma, V]; A, Ct [gamma, V, r]; W [gamma, r, r]."""
     U = _f32(U)
@@ -343,9 +344,10 @@ def draft_rnn(U, A, Ct, W, x0, draft_temp, seed: int, rid_base: int = 0, bf16_st
     S = np.zeros((R, gamma, r))
     xc = None if x_cond is None else _i32(x_cond)
     sc = None if s_cond is None else _f32(s_cond)
+    P = np.zeros((R, gamma, V)) if want_P else None
     rc = lib().orc_draft_rnn(R, gamma, V, r, _ptr(U), gamma * V, _ptr(A), _ptr(Ct), _ptr(W),
                              _ptr(_i32(x0)), _ptr(_f32(draft_temp)), seed, rid_base, int(bf16_state),
-                             _ptr(xc), _ptr(sc), _ptr(x), _ptr(q), _ptr(l), _ptr(g), _ptr(S))
+                             _ptr(xc), _ptr(sc), _ptr(x), _ptr(q), _ptr(l), _ptr(g), _ptr(S), _ptr(P))
     if rc != 0:
         raise ValueError(f"orc_draft_rnn failed ({rc})")
-    return DraftRnnOut(x, q, l, g, S)
+    return DraftRnnOut(x, q, l, g, S, P)

@@ -282,7 +282,7 @@ int orc_draft_rnn(int R, int gamma, int V, int r, const float* U, int64_t U_rstr
                   const float* A, const float* Ct, const float* W, const int32_t* x0,
                   const float* draft_temp, uint64_t seed, uint32_t rid_base, int bf16_state,
                   const int32_t* x_cond, const float* s_cond, int32_t* x, double* q_tok,
-                  double* lse, double* gap, double* S_out) {
+                  double* lse, double* gap, double* S_out, double* P) {
   if (R < 0 || gamma <= 0 || V <= 0 || r <= 0) return -1;
   Stream rng(seed);
   std::vector<double> z, st((size_t)r), prev((size_t)r);
@@ -318,6 +318,8 @@ int orc_draft_rnn(int R, int gamma, int V, int r, const float* U, int64_t U_rstr
       q_tok[o] = std::exp(z[(size_t)xk] - l);
       lse[o] = l;
       if (gap) gap[o] = g;
+      if (P)
+        for (int v = 0; v < V; ++v) P[o * (size_t)V + (size_t)v] = std::exp(z[(size_t)v] - l);
       for (int j = 0; j < r; ++j) prev[(size_t)j] = use[j];
       x_prev = x_cond ? x_cond[o] : xk;
     }

@@ -52,12 +52,13 @@ def test_zero_recurrence_is_the_markov_head(bf16_state):
     W = np.zeros((gamma, r, r), np.float32)
     x0 = rng.integers(0, V, R).astype(np.int32)
     temps = np.ones(gamma, np.float32)
-    rnn = oracle.draft_rnn(U, A, Ct, W, x0, temps, seed=9, bf16_state=bf16_state)
+    rnn = oracle.draft_rnn(U, A, Ct, W, x0, temps, seed=9, bf16_state=bf16_state, want_P=True)
     tA = torch.tanh(torch.tensor(A, dtype=torch.float64)).float()
     table = (tA.to(torch.bfloat16).float() if bf16_state else tA).numpy()
-    mk = oracle.draft(U, table, Ct, x0, temps, seed=9)
+    mk = oracle.draft(U, table, Ct, x0, temps, seed=9, want_P=True)
     assert np.array_equal(rnn.x, mk.x)
     assert np.allclose(rnn.q_tok, mk.q_tok, rtol=1e-12) and np.allclose(rnn.lse, mk.lse, rtol=1e-12)
+    assert np.allclose(rnn.P, mk.P, rtol=1e-12, atol=0)
 
 
 def test_bf16_states_match_torch_rounding():
