@@ -50,6 +50,9 @@ def _args():
                    help="survival threshold of --sched-mode threshold")
     p.add_argument("--accept-stats", action="store_true",
                    help="fold every round into the per-length acceptance EMA table")
+    p.add_argument("--head", default="markov", choices=["markov", "rnn"],
+                   help="sequential draft head: the Markov head, or the RNN head with a "
+                        "recurrent state (synthetic recurrence W_k ~ N(0, 1/r))")
     p.add_argument("--calibration", action="store_true",
                    help="also compute c* = sum min(p, q) of every verified row and fold the "
                         "round into the reliability diagram (ECE)")
@@ -63,6 +66,10 @@ def _workload(args):
     if args.sched_mode != "workload":
         mode = {"early_stop": 0, "global": 1, "threshold": 2}[args.sched_mode]
         wl = dataclasses.replace(wl, sched_mode=mode, sched_threshold=args.sched_threshold)
+    if args.head != "markov":
+        if wl.mode == "greedy":
+            raise SystemExit("--head applies to workloads with a draft stage")
+        wl = dataclasses.replace(wl, head=args.head)
     return wl
 
 
@@ -71,7 +78,7 @@ def _workload(args):
 # keyed by a hash of the kernel's sources: a changed kernel reports null until
 # it is profiled again.
 DRAFT_TC_SOURCES = ["draft_tc.cu", "draft_tc.cuh", "fused_tc.cuh", "tc.cuh", "common.cuh"]
-MEASURED_TRAFFIC = {("c5", "acb4a14c5c03f6b4"): 298082048 + 3628032}
+MEASURED_TRAFFIC = {("c5", "7053e00a74b75bba"): 298082048 + 3678720}
 
 
 def _source_hash(files) -> str:
@@ -157,7 +164,13 @@ def _oracle_round(wl, inp_cpu, seed: int, n_req: int) -> tuple[int, float]:
     A, Ct = inp_cpu["A_np"], inp_cpu["Ct_np"]
     x0 = inp_cpu["x0"][:n_req].numpy()
     temps = inp_cpu["draft_temp"].numpy()
-    d = oracle.draft(U, A, Ct, x0, temps, seed)
+    S = None
+    if wl.head == "rnn":
+        d = oracle.draft_rnn(U, A, Ct, inp_cpu["Wrnn_np"], x0, temps, seed,
+                             bf16_state=inp_cpu["A"].dtype == torch_bf16())
+        S = d.S
+    else:
+        d = oracle.draft(U, A, Ct, x0, temps, seed)
     _, a = oracle.confidence(f(inp_cpu["h"][:n_req]), inp_cpu["W1_np"], inp_cpu["w_np"], x0, d.x,
                              inp_cpu["sts_temp"].numpy())
     K = max(1, round(wl.K * n_req / wl.R))
@@ -165,8 +178,13 @@ def _oracle_round(wl, inp_cpu, seed: int, n_req: int) -> tuple[int, float]:
                         wl.sched_mode, wl.sched_threshold)
     rows = f(inp_cpu["tgt"][:n_req]).reshape(-1, wl.V)
     oracle.verify(oracle.MODE_SAMPLE, rows, (np.arange(n_req) * (G + 1)).astype(np.int32), s.ell,
-                  d.x, d.q_tok, 1.0, U, A, Ct, x0, temps, seed)
+                  d.x, d.q_tok, 1.0, U, A, Ct, x0, temps, seed, S=S)
     return n_req * G + s.B, time.perf_counter() - t0
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16
 
 
 def _cpu_inputs(wl):
@@ -178,6 +196,8 @@ def _cpu_inputs(wl):
         inp["Ct_np"] = inp["Ct"].float().numpy()
         inp["W1_np"] = inp["W1"].float().numpy()
         inp["w_np"] = inp["w"].float().numpy()
+        if wl.head == "rnn":
+            inp["Wrnn_np"] = synth.rnn_weights(small, "cpu").float().numpy()
     return inp
 
 
@@ -249,7 +269,7 @@ def run_reference(args, wl):
             "ms_per_step": 1000 * tot_sec / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "R": wl.R, "gamma": wl.gamma, "V": wl.V, "r": wl.r,
-                       **_sched_config(wl)},
+                       **_sched_config(wl), **({"head": "rnn"} if wl.head == "rnn" else {})},
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
                              "sample": f"{n} of {wl.R} requests per step ({_stages(wl, n)})"},
             "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
@@ -312,6 +332,10 @@ def main():
     greedy = wl.mode == "greedy"
     din = None if greedy else synth.draft_inputs(g, request_id_base=rid_base)
     R, G, V = wl.R, wl.gamma, wl.V
+    rnn = wl.head == "rnn"
+    if rnn:  # the recurrence is a weight (resident); S is written by the draft, read by verify
+        din.Wrnn = synth.rnn_weights(wl, dev, seed=seed_in)
+        din.S = torch.empty(R, G, wl.r, dtype=wl.fac_dtype, device=dev)
     stats_hist = torch.zeros(max(1, args.steps), 4, dtype=torch.float64, device=dev)
 
     bufs = {}
@@ -415,8 +439,12 @@ def main():
         # verify rows, fused residual, residual fallback (gated, exits at once
         # when unused); the EMA update; the c* plan, c* pass and diagram
         launches = G + 6 + (1 if acc_tab is not None else 0) + (3 if calib is not None else 0)
+        if rnn:  # the state kernel before every draft step
+            launches += G
+            kernel = "draft_step (one launch per position k; RNN head, state rows gathered)"
     achieved = per_launch / (dur_ms / 1000.0) / 1e9
-    traffic = None if greedy else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
+    # measured on the Markov head's launch (the RNN head's gathers other rows)
+    traffic = None if greedy or rnn else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": traffic,
@@ -432,6 +460,7 @@ def main():
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}",
                        **_sched_config(wl),
+                       **({"head": "rnn"} if rnn else {}),
                        **({"accept_stats": True} if acc_tab is not None else {}),
                        **({"calibration": True} if calib is not None else {})},
             "stage_ms_per_step": {k: round(v / args.steps, 4) for k, v in stage_ms.items()},
@@ -469,7 +498,8 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
     d_in = vs.DraftInputs(U=devb["U"], A=g["A"], Ct=g["Ct"], x0=devb["x0"],
                           draft_temp=g["draft_temp"], h=devb["h"], W1=g["W1"], w=g["w"],
-                          sts_temp=g["sts_temp"], request_id_base=rid_base)
+                          sts_temp=g["sts_temp"], request_id_base=rid_base,
+                          Wrnn=din.Wrnn, S=din.S)
 
     host_out = {k: outs[k] for k in ("out_tok", "accept_len", "n_out", "stats")}
 

@@ -69,6 +69,7 @@ enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 };
 enum spec_verify_mode { SPEC_VERIFY_SAMPLE = 0, SPEC_VERIFY_GREEDY = 1 };
 enum spec_sched_mode { SPEC_SCHED_EARLY_STOP = 0, SPEC_SCHED_GLOBAL = 1, SPEC_SCHED_THRESHOLD = 2 };
 enum spec_stage { SPEC_STAGE_DRAFT = 0, SPEC_STAGE_SCHEDULE = 1, SPEC_STAGE_VERIFY = 2 };
+enum spec_head { SPEC_HEAD_MARKOV = 0, SPEC_HEAD_RNN = 1 };
 
 /* Bits of the device status word. */
 #define SPEC_STATUS_BAD_TOKEN 0x1u    /* a token id was outside [0, V)          */
@@ -105,6 +106,21 @@ enum spec_stage { SPEC_STAGE_DRAFT = 0, SPEC_STAGE_SCHEDULE = 1, SPEC_STAGE_VERI
  *   c, a [R, gamma]; P_out [R, gamma, V] (nullable) the full draft distributions.
  * Sizes: R >= 1, 1 <= gamma <= 64, 1 <= V < 2^30, 1 <= r <= 256, d >= 0, e >= 0,
  * R * gamma * V < 2^40.  Alignment: every pointer aligned to its element size.
+ *
+ * Sequential head.  The same passage names two heads, a Markov head and an RNN
+ * head that keeps a longer dependency, and gives no formula for the second.
+ * head = SPEC_HEAD_MARKOV (0, the default of a zeroed struct) is the bias
+ * above.  head = SPEC_HEAD_RNN keeps one state vector per request:
+ *     s_0 = 0,  s_k = store(tanh(A_k[x_{k-1}, :] + s_{k-1} W_k)),  B_k = s_k C_k,
+ * the pre-activation summed in fp32 (A_k first, then i = 0..r-1 ascending) and
+ * store() rounding to fac_dtype (bf16: round to nearest even; f32: as is).
+ *   Wrnn   [gamma, r, r]   fac_dtype     W_k[i][j] maps s_{k-1}[i] to column j
+ *   S      [R, gamma, r]   fac_dtype     out: s_k of (r, k) at S[r][k-1]; spec_verify
+ *                                        reads it back (through args->draft) for the
+ *                                        residual and c*, so keep it until then
+ * Wrnn and S are ignored (may be NULL) for the Markov head; for the RNN head
+ * both are required and aligned to the element size.  Any other head value is
+ * SPEC_ERR_INVALID_ARG.
  */
 typedef struct spec_draft_args {
   int R, gamma, V, r, d, e;
@@ -130,6 +146,9 @@ typedef struct spec_draft_args {
   void *workspace;
   size_t workspace_bytes;
   uint32_t *status; /* nullable device word */
+  int head;         /* spec_head */
+  const void *Wrnn;
+  void *S;
 } spec_draft_args;
 
 int spec_draft_sample(const spec_draft_args *args, uint64_t seed, spec_stream_t stream);

@@ -57,6 +57,7 @@ class Workload:
     seed: int
     sts_ramp: bool = False
     sched_threshold: float = 0.0  # read by the static-threshold mode only
+    head: str = "markov"          # sequential head: "markov" or "rnn" (rnn_weights)
 
     def scaled(self, **kw) -> "Workload":
         """Same recipe at other sizes (for parity cases the oracle finishes quickly).
@@ -193,6 +194,16 @@ def make_inputs(wl: Workload, device="cpu", seed: Optional[int] = None) -> dict:
         tgt = base + _randn((R, G + 1, V), g, device) * sig.view(1, G + 1, 1)
     out["tgt"] = tgt.to(wl.logit_dtype)
     return out
+
+
+def rnn_weights(wl: Workload, device="cpu", seed: Optional[int] = None) -> torch.Tensor:
+    """Recurrence matrices W_k of the RNN sequential head: [gamma, r, r], entries
+    N(0, 1/r) (unit gain on a random state), in the workload's factor dtype.
+    Drawn from their own stream (seed + 1), so the round's other inputs are the
+    same as for the Markov head."""
+    seed = wl.seed if seed is None else seed
+    g = _gen(seed + 1, device)
+    return _randn((wl.gamma, wl.r, wl.r), g, device, 1.0 / math.sqrt(wl.r)).to(wl.fac_dtype)
 
 
 def draft_inputs(inp: dict, request_id_base: int = 0):

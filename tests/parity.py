@@ -89,8 +89,49 @@ def compare_schedule(inp: dict, a_gpu: torch.Tensor, sched: dict, K: int, mode: 
     return rep
 
 
+def compare_draft_rnn(inp: dict, W: torch.Tensor, S: torch.Tensor, out: dict, seed: int, reqs,
+                      rid_base: int = 0, rep=None) -> Report:
+    """RNN head, stage-isolated per position: the oracle recomputes each state
+    from the CUDA path's previous state and token, and draws each token from
+    the CUDA path's state.  States: bf16 within one unit in the last place of
+    the stored value (the pre-activation is summed in fp32 on the device and
+    in fp64 by the oracle, so a value near a rounding boundary may round the
+    other way), with at most 1% of them off; fp32 within 1e-5."""
+    rep = rep or Report()
+    A, Ct, Wn = to_np(inp["A"]), to_np(inp["Ct"]), to_np(W)
+    bf16 = S.dtype == torch.bfloat16
+    x_gpu, S_gpu = to_np(out["x"]), to_np(S)
+    off = total = 0
+    for r in reqs:
+        od = oracle.draft_rnn(to_np(inp["U"][r:r + 1]), A, Ct, Wn, to_np(inp["x0"][r:r + 1]),
+                              to_np(inp["draft_temp"]), seed, rid_base=rid_base + r, bf16_state=bf16,
+                              x_cond=x_gpu[r:r + 1], s_cond=S_gpu[r:r + 1], want_P="P" in out)
+        diff = np.abs(od.S[0] - S_gpu[r])
+        if bf16:
+            ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(od.S[0]), 1e-30))[1] - 8)
+            assert np.all(diff <= ulp * 1.0000001), (r, diff.max())
+            off += int(np.count_nonzero(diff))
+        else:
+            assert diff.max() < 1e-5, (r, diff.max())
+        total += diff.size
+        same = od.x[0] == x_gpu[r]
+        tie = od.gap[0] < NEAR_TIE
+        assert np.all(same | tie), (r, od.x[0], x_gpu[r], od.gap[0])
+        rep.near_ties += int(np.sum(~same & tie))
+        rep.checked += len(same)
+        q, lse = to_np(out["q_tok"][r]), to_np(out["lse_q"][r])
+        assert np.all(np.abs(q - od.q_tok[0])[same] < PROB_TOL), (r, q, od.q_tok[0])
+        assert np.all((np.abs(lse - od.lse[0]) / np.maximum(1, np.abs(od.lse[0])))[same] < PROB_TOL)
+        if "P" in out:
+            assert np.abs(to_np(out["P"][r]) - od.P[0]).max() < PROB_TOL
+    assert off <= 0.01 * total, (off, total)
+    rep.notes.append(f"rnn states one ulp off: {off} of {total}")
+    return rep
+
+
 def compare_verify(inp: dict, d_out: dict, ell: torch.Tensor, v_out: dict, seed: int, mode: int,
-                   reqs, target_temp: float = 1.0, rid_base: int = 0, rep=None) -> Report:
+                   reqs, target_temp: float = 1.0, rid_base: int = 0, rep=None,
+                   S: torch.Tensor | None = None) -> Report:
     rep = rep or Report()
     tgt_all = inp["tgt"]
     V = tgt_all.shape[-1]
@@ -111,7 +152,8 @@ def compare_verify(inp: dict, d_out: dict, ell: torch.Tensor, v_out: dict, seed:
                                to_np(d_out["q_tok"][r:r + 1]).astype(np.float64), target_temp,
                                to_np(inp["U"][r:r + 1]), A, Ct,
                                to_np(inp["x0"][r:r + 1]), temps, seed,
-                               rid_base=rid_base + r)
+                               rid_base=rid_base + r,
+                               S=None if S is None else to_np(S[r:r + 1]))
         got = to_np(v_out["out_tok"][r])
         if ov.margin[0] < NEAR_TIE and not (got == ov.out_tok[0]).all():
             rep.near_ties += 1

@@ -54,6 +54,7 @@ def test_struct_layout_matches_c(spec, tmp_path):
         'printf("spec_calibration_args %zu\\n", sizeof(spec_calibration_args));\n'
         'printf("spec_round_host_args %zu\\n", sizeof(spec_round_host_args));\n'
         "P(spec_draft_args, status) P(spec_draft_args, workspace_bytes) P(spec_draft_args, U)\n"
+        "P(spec_draft_args, head) P(spec_draft_args, Wrnn) P(spec_draft_args, S)\n"
         "P(spec_sched_args, b_lo) P(spec_sched_args, stats) P(spec_sched_args, status)\n"
         "P(spec_sched_args, threshold) P(spec_accept_stats_args, beta)\n"
         "P(spec_accept_stats_args, ema) P(spec_accept_stats_args, status)\n"
@@ -76,6 +77,9 @@ def test_struct_layout_matches_c(spec, tmp_path):
     for key, (cls, field) in {"spec_draft_args.status": (spec.DraftArgs, "status"),
                               "spec_draft_args.workspace_bytes": (spec.DraftArgs, "workspace_bytes"),
                               "spec_draft_args.U": (spec.DraftArgs, "U"),
+                              "spec_draft_args.head": (spec.DraftArgs, "head"),
+                              "spec_draft_args.Wrnn": (spec.DraftArgs, "Wrnn"),
+                              "spec_draft_args.S": (spec.DraftArgs, "S"),
                               "spec_sched_args.b_lo": (spec.SchedArgs, "b_lo"),
                               "spec_sched_args.stats": (spec.SchedArgs, "stats"),
                               "spec_sched_args.status": (spec.SchedArgs, "status"),
@@ -123,6 +127,23 @@ def test_host_side_rejections_launch_nothing(spec):
     assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG  # nulls
     a.gamma = 65
     assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    # the sequential head: valid pointers reach the workspace check; a bad head
+    # value, a missing RNN buffer or a misaligned state array is refused first
+    a.gamma, a.fac_dtype = 4, spec.SPEC_BF16
+    for f in ("U", "A", "Ct", "x0", "draft_temp", "sts_temp", "x", "q_tok", "lse_q", "c", "a"):
+        setattr(a, f, ctypes.c_void_p(256))
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_WORKSPACE
+    a.head = 2
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_draft_sample_static(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    a.head, a.Wrnn = spec.HEAD_RNN, ctypes.c_void_p(256)
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG  # no S
+    assert lib.spec_draft_sample_static(ctypes.byref(a), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    a.S = ctypes.c_void_p(257)
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_ALIGNMENT
+    assert lib.spec_draft_sample_static(ctypes.byref(a), 0, None) == spec.SPEC_ERR_ALIGNMENT
+    a.S = ctypes.c_void_p(256)
+    assert lib.spec_draft_sample(ctypes.byref(a), 0, None) == spec.SPEC_ERR_WORKSPACE
     s = spec.SchedArgs()
     s.R, s.gamma, s.n_sps, s.b_step, s.K = 100, 100, 1, 1.0, 5
     s.a = s.sps = s.ell = s.row_off = s.stats = ctypes.c_void_p(256)

@@ -1,6 +1,6 @@
 """The benchmark's reference arm (the oracle on the host cores) prints the one
-JSON line the harness reads, for a sampled workload and for the greedy one
-(CPU only)."""
+JSON line the harness reads, for a sampled workload (Markov and RNN heads) and
+for the greedy one (CPU only)."""
 import json
 import os
 import subprocess
@@ -11,10 +11,10 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("config", ["c2", "greedy"])
-def test_reference_arm_json_line(config):
+@pytest.mark.parametrize("config,head", [("c2", "markov"), ("greedy", "markov"), ("c2", "rnn")])
+def test_reference_arm_json_line(config, head):
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--config", config, "--steps", "1", "--warmup", "1"],
+                          "--config", config, "--steps", "1", "--warmup", "1", "--head", head],
                          capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
@@ -25,3 +25,4 @@ def test_reference_arm_json_line(config):
     assert line["steps"] == 1 and line["warmup"] == 1 and line["config"]["workload"] == config
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"].get("head", "markov") == head

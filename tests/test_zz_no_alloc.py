@@ -64,3 +64,25 @@ def test_static_scratch_rejects_oversized_batches():
                                             ctypes.c_void_p]
     lib.spec_draft_sample_static.restype = ctypes.c_int
     assert lib.spec_draft_sample_static(ctypes.byref(a), 1, None) == vs.SPEC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["fused_fp32", "generic_fp32"])
+def test_static_scratch_rnn_head(name):
+    """The RNN head through the static entry point: same tokens and states."""
+    wl = CASES[name]
+    g = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v)
+         for k, v in synth.make_inputs(wl, "cpu").items()}
+    din = synth.draft_inputs(g)
+    din.Wrnn = synth.rnn_weights(wl, "cuda")
+    din.S = torch.zeros(wl.R, wl.gamma, wl.r, dtype=wl.fac_dtype, device="cuda")
+    ref = vs.draft_sample(din, 5)
+    torch.cuda.synchronize()
+    S_ref = din.S.clone()
+    din.S.fill_(float("nan"))
+    got = vs.draft_outputs(wl.R, wl.gamma, wl.V, "cuda")
+    _static_call(din, got, 5)
+    torch.cuda.synchronize()
+    assert torch.equal(got["x"], ref["x"])
+    assert torch.equal(din.S, S_ref)
+    for key in ("q_tok", "lse_q"):
+        assert torch.allclose(got[key], ref[key], rtol=0, atol=1e-5), key

@@ -30,6 +30,7 @@ SPEC_F32, SPEC_BF16 = 0, 1
 VERIFY_SAMPLE, VERIFY_GREEDY = 0, 1
 SCHED_EARLY_STOP, SCHED_GLOBAL, SCHED_THRESHOLD = 0, 1, 2
 STAGE_DRAFT, STAGE_SCHEDULE, STAGE_VERIFY = 0, 1, 2
+HEAD_MARKOV, HEAD_RNN = 0, 1
 STATUS_BAD_TOKEN, STATUS_BAD_ELL, STATUS_BAD_SURVIVAL, STATUS_BAD_ROW = 0x1, 0x2, 0x4, 0x8
 
 _P = ctypes.c_void_p
@@ -43,7 +44,8 @@ class DraftArgs(ctypes.Structure):
                 ("U", _P), ("A", _P), ("Ct", _P), ("x0", _P), ("draft_temp", _P), ("h", _P),
                 ("W1", _P), ("w", _P), ("sts_temp", _P), ("x", _P), ("q_tok", _P), ("lse_q", _P),
                 ("c", _P), ("a", _P), ("P_out", _P), ("workspace", _P),
-                ("workspace_bytes", ctypes.c_size_t), ("status", _P)]
+                ("workspace_bytes", ctypes.c_size_t), ("status", _P),
+                ("head", ctypes.c_int), ("Wrnn", _P), ("S", _P)]
 
 
 class SchedArgs(ctypes.Structure):
@@ -191,6 +193,10 @@ class DraftInputs:
     w: torch.Tensor            # [d + e]
     sts_temp: torch.Tensor     # [gamma] f32
     request_id_base: int = 0
+    # RNN sequential head (both or neither; factor dtype): the recurrence W_k and
+    # the state array the draft writes and the verifier reads back
+    Wrnn: Optional[torch.Tensor] = None   # [gamma, r, r]
+    S: Optional[torch.Tensor] = None      # [R, gamma, r]
 
 
 def _draft_struct(inp: DraftInputs, outs: dict, ws: Optional[torch.Tensor], status) -> DraftArgs:
@@ -215,6 +221,13 @@ def _draft_struct(inp: DraftInputs, outs: dict, ws: Optional[torch.Tensor], stat
     a.request_id_base = inp.request_id_base
     a.U, a.A, a.Ct, a.x0, a.draft_temp = _ptr(U), _ptr(A), _ptr(Ct), _ptr(inp.x0), _ptr(inp.draft_temp)
     a.h, a.W1, a.w, a.sts_temp = _ptr(h), _ptr(W1), _ptr(w), _ptr(inp.sts_temp)
+    if (inp.Wrnn is None) != (inp.S is None):
+        raise ValueError("the RNN head needs both Wrnn and S")
+    if inp.Wrnn is not None:
+        Wr, S = _dev(inp.Wrnn, "Wrnn"), _dev(inp.S, "S")
+        if Wr.shape != (gamma, r, r) or S.shape != (R, gamma, r) or not (Wr.dtype == S.dtype == A.dtype):
+            raise ValueError("Wrnn must be [gamma, r, r] and S [R, gamma, r], in the dtype of A")
+        a.head, a.Wrnn, a.S = HEAD_RNN, _ptr(Wr), _ptr(S)
     if outs:
         a.x, a.q_tok, a.lse_q = _ptr(outs["x"]), _ptr(outs["q_tok"]), _ptr(outs["lse_q"])
         a.c, a.a, a.P_out = _ptr(outs["c"]), _ptr(outs["a"]), _ptr(outs.get("P"))

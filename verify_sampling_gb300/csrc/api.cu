@@ -40,6 +40,7 @@ bool draft_tc_ok(const spec_draft_args& a, int* sms) {
   if (a.fac_dtype != SPEC_BF16 || a.r % 64 != 0 || a.r > 256) return false;
   if (((size_t)a.V * dtype_size(a.logit_dtype)) % 16 != 0) return false;
   if (!aligned(a.U, 16) || !aligned(a.A, 16) || !aligned(a.Ct, 16)) return false;
+  if (a.head == SPEC_HEAD_RNN && !aligned(a.S, 16)) return false;
   int dev = 0, major = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -68,6 +69,8 @@ int check_draft_args(const spec_draft_args* a) {
   if (!a->U || !a->A || !a->Ct || !a->x0 || !a->draft_temp || !a->x || !a->q_tok || !a->lse_q)
     return SPEC_ERR_INVALID_ARG;
   if (!a->sts_temp || !a->c || !a->a) return SPEC_ERR_INVALID_ARG;
+  if (a->head != SPEC_HEAD_MARKOV && a->head != SPEC_HEAD_RNN) return SPEC_ERR_INVALID_ARG;
+  if (a->head == SPEC_HEAD_RNN && (!a->Wrnn || !a->S)) return SPEC_ERR_INVALID_ARG;
   if ((a->d > 0 && !a->h) || (a->e > 0 && !a->W1) || (a->d + a->e > 0 && !a->w))
     return SPEC_ERR_INVALID_ARG;
   const size_t ls = dtype_size(a->logit_dtype), fs = dtype_size(a->fac_dtype),
@@ -77,6 +80,8 @@ int check_draft_args(const spec_draft_args* a) {
       !aligned(a->lse_q, 4) || !aligned(a->sts_temp, 4) || !aligned(a->c, 4) ||
       !aligned(a->a, 4) || !aligned(a->P_out, 4) || !aligned(a->h, cs) || !aligned(a->W1, cs) ||
       !aligned(a->w, cs) || !aligned(a->status, 4))
+    return SPEC_ERR_ALIGNMENT;
+  if (a->head == SPEC_HEAD_RNN && (!aligned(a->Wrnn, fs) || !aligned(a->S, fs)))
     return SPEC_ERR_ALIGNMENT;
   return SPEC_OK;
 }
@@ -141,6 +146,10 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
   p.U = a.U;
   p.A = a.A;
   p.Ct = a.Ct;
+  if (a.head == SPEC_HEAD_RNN) {
+    p.W = a.Wrnn;
+    p.S = a.S;
+  }
   p.x0 = a.x0;
   p.draft_temp = a.draft_temp;
   p.x = a.x;
@@ -169,6 +178,8 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
     t.x0 = a.x0;
     t.draft_temp = a.draft_temp;
     t.A = a.A;
+    t.W = p.W;
+    t.S = p.S;
     t.x = a.x;
     t.q_tok = a.q_tok;
     t.lse_q = a.lse_q;
@@ -258,12 +269,15 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
         !d.x0 || !d.draft_temp)
       return SPEC_ERR_INVALID_ARG;
     if (d.request_id_base != a.request_id_base) return SPEC_ERR_INVALID_ARG;
+    if (d.head != SPEC_HEAD_MARKOV && d.head != SPEC_HEAD_RNN) return SPEC_ERR_INVALID_ARG;
+    if (d.head == SPEC_HEAD_RNN && !d.S) return SPEC_ERR_INVALID_ARG;
     fac_dtype = d.fac_dtype;
     logit_dtype = d.logit_dtype;
     rank = d.r;
     if (!aligned(d.U, dtype_size(logit_dtype)) || !aligned(d.A, dtype_size(fac_dtype)) ||
         !aligned(d.Ct, dtype_size(fac_dtype)) || !aligned(d.x0, 4) || !aligned(d.draft_temp, 4) ||
-        !aligned(a.q_tok, 4) || !aligned(a.lse_q, 4))
+        !aligned(a.q_tok, 4) || !aligned(a.lse_q, 4) ||
+        (d.head == SPEC_HEAD_RNN && !aligned(d.S, dtype_size(fac_dtype))))
       return SPEC_ERR_ALIGNMENT;
   }
   if (!aligned(a.tgt, dtype_size(a.tgt_dtype)) || !aligned(a.tgt_row_off, 4) || !aligned(a.ell, 4) ||
@@ -296,6 +310,7 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
     p.U = a.draft->U;
     p.A = a.draft->A;
     p.Ct = a.draft->Ct;
+    if (a.draft->head == SPEC_HEAD_RNN) p.S = a.draft->S;
     p.x0 = a.draft->x0;
     p.draft_temp = a.draft->draft_temp;
   }
@@ -314,7 +329,8 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
     if (!dev_ok) return SPEC_ERR_CUDA;
     p.tc_residual = sample && major == 10 && sms >= 1 && sms <= kMaxDeviceSms &&
-                    resid_tc_supported(a.tgt_dtype, logit_dtype, fac_dtype, rank, a.V, a.tgt, p.U, p.A, p.Ct);
+                    resid_tc_supported(a.tgt_dtype, logit_dtype, fac_dtype, rank, a.V, a.tgt, p.U, p.A, p.Ct) &&
+                    aligned(p.S, 16);
     p.device_sms = sms;
   }
   size_t cnt_off = 0, cnt_bytes = 0;
@@ -396,7 +412,8 @@ int spec_round_host(const spec_round_host_args* args, uint64_t seed, spec_stream
   if (sc.R != d.R || sc.gamma != d.gamma || v.R != d.R || v.gamma != d.gamma || v.V != d.V ||
       v.mode != SPEC_VERIFY_SAMPLE || sc.a != d.a || v.ell != sc.ell || v.x != d.x ||
       v.q_tok != d.q_tok || v.lse_q != d.lse_q || !v.draft || v.draft->U != d.U ||
-      v.draft->A != d.A || v.draft->Ct != d.Ct || v.draft->x0 != d.x0)
+      v.draft->A != d.A || v.draft->Ct != d.Ct || v.draft->x0 != d.x0 ||
+      v.draft->head != d.head || (d.head == SPEC_HEAD_RNN && v.draft->S != d.S))
     return SPEC_ERR_INVALID_ARG;
   if (!valid_dtype(d.logit_dtype) || !valid_dtype(d.conf_dtype) || !valid_dtype(v.tgt_dtype) ||
       d.R < 1 || d.gamma < 1 || d.V < 1 || d.d < 0)

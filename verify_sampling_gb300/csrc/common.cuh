@@ -295,6 +295,16 @@ __device__ __forceinline__ float ld_f(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
 }
 
+// Row of the bias factor for position k (1-based) of request r: the Markov
+// head's A_k[x_prev] or, when the RNN head's state array S [R, gamma, rank] is
+// given, the stored state s_k = S[r][k - 1].
+template <typename TF>
+__device__ __forceinline__ const TF* bias_row(const void* A, const void* S, int V, int rank, int gamma,
+                                              int k, int r, int x_prev) {
+  if (S) return reinterpret_cast<const TF*>(S) + ((size_t)r * gamma + (k - 1)) * rank;
+  return reinterpret_cast<const TF*>(A) + ((size_t)(k - 1) * V + x_prev) * rank;
+}
+
 // ---------------------------------------------------------- block helpers --
 // Block-wide merge of per-thread states; the result is valid in thread 0.
 template <typename S, typename ShflFn, typename MergeFn>

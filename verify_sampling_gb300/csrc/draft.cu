@@ -1,11 +1,14 @@
-// Draft stage kernels: Markov-head sampling step, full-distribution output and
-// the confidence head with survival products.
+// Draft stage kernels: sequential-head sampling step, full-distribution output
+// and the confidence head with survival products.
 //
 // DSpark summary, "第二阶段：轻量顺序头": P_k = softmax((U_k + B_k(x_{k-1})) / T_k)
 // with the low-rank bias B_k(x) = A_k[x, :] C_k (history article, "杀招一");
 // DSpark summary, "2.1 置信度头": c_k = sigmoid(w . [h_k ; W1[x_{k-1}]] / tau_k);
 // history article, "杀招二": a_j = prod_{i<=j} c_i.
+#include <type_traits>
+
 #include "draft.cuh"
+#include "rnn.cuh"
 
 namespace spec {
 
@@ -14,6 +17,8 @@ namespace spec {
 // blocks [vb_begin, vb_end) of row (r, k), 4 entries per Philox block, keeps a
 // Gumbel race + online softmax per thread, reduces it over the CTA and publishes
 // a partial; the last CTA of the row merges the partials into x_k, q_tok, lse.
+// The bias row is A_k[x_{k-1}] (Markov head) or the state s_k (RNN head, written
+// by the state kernel launched just before).
 template <typename TL, typename TF>
 __global__ void __launch_bounds__(kDraftThreads)
     draft_step_kernel(DraftStepParams p) {
@@ -29,9 +34,9 @@ __global__ void __launch_bounds__(kDraftThreads)
     if (threadIdx.x == 0) set_status(p.status, SPEC_STATUS_BAD_TOKEN);
     x_prev = 0;
   }
-  const TF* A = reinterpret_cast<const TF*>(p.A) + (size_t)(k - 1) * V * rank;
+  const TF* brow = bias_row<TF>(p.A, p.S, V, rank, gamma, k, r, x_prev);
   const TF* Ct = reinterpret_cast<const TF*>(p.Ct) + (size_t)(k - 1) * V * rank;
-  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(A, (size_t)x_prev * rank + i);
+  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(brow, (size_t)i);
   __syncthreads();
 
   const TL* U = reinterpret_cast<const TL*>(p.U) + ((size_t)r * gamma + (k - 1)) * V;
@@ -95,9 +100,9 @@ __global__ void __launch_bounds__(256) draft_probs_kernel(DraftStepParams p) {
   const int V = p.V, rank = p.rank, gamma = p.gamma;
   int x_prev = (k == 1) ? p.x0[r] : p.x[(size_t)r * gamma + (k - 2)];
   if (x_prev < 0 || x_prev >= V) x_prev = 0;
-  const TF* A = reinterpret_cast<const TF*>(p.A) + (size_t)(k - 1) * V * rank;
+  const TF* brow = bias_row<TF>(p.A, p.S, V, rank, gamma, k, r, x_prev);
   const TF* Ct = reinterpret_cast<const TF*>(p.Ct) + (size_t)(k - 1) * V * rank;
-  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(A, (size_t)x_prev * rank + i);
+  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(brow, (size_t)i);
   __syncthreads();
   const size_t o = (size_t)r * gamma + (k - 1);
   const TL* U = reinterpret_cast<const TL*>(p.U) + o * V;
@@ -180,6 +185,22 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(ConfParams p) 
 }
 
 // ------------------------------------------------------------- launchers --
+static RnnStateParams rnn_params(const DraftStepParams& p, int k) {
+  RnnStateParams q{};
+  q.R = p.R;
+  q.gamma = p.gamma;
+  q.V = p.V;
+  q.rank = p.rank;
+  q.k = k;
+  q.x0 = p.x0;
+  q.x = p.x;
+  q.A = p.A;
+  q.W = p.W;
+  q.S = p.S;
+  q.status = p.status;
+  return q;
+}
+
 template <typename TL, typename TF>
 static cudaError_t launch_draft_typed(const DraftStepParams& base, bool want_probs,
                                       bool probs_only, cudaStream_t stream) {
@@ -187,6 +208,10 @@ static cudaError_t launch_draft_typed(const DraftStepParams& base, bool want_pro
   const dim3 grid((unsigned)p.nsplit, (unsigned)p.R);
   for (int k = 1; k <= p.gamma && !probs_only; ++k) {
     p.k = k;
+    if (p.S) {  // RNN head: s_k from x_{k-1} (final: the previous step merged it)
+      cudaError_t err = launch_rnn_state(rnn_params(p, k), std::is_same<TF, float>::value, false, stream);
+      if (err != cudaSuccess) return err;
+    }
     draft_step_kernel<TL, TF><<<grid, kDraftThreads, 0, stream>>>(p);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;

@@ -19,6 +19,8 @@ struct DraftStepParams {
   const void* U;
   const void* A;
   const void* Ct;
+  const void* W;  // RNN head: recurrence [gamma, rank, rank] (null: Markov head)
+  void* S;        // RNN head: states [R, gamma, rank] (null: Markov head)
   const int32_t* x0;
   const float* draft_temp;
   int32_t* x;

@@ -60,13 +60,15 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
   if (!a.U || !a.A || !a.Ct || !a.x0 || !a.draft_temp || !a.x || !a.q_tok || !a.lse_q || !a.sts_temp ||
       !a.c || !a.a || (a.d > 0 && !a.h) || (a.e > 0 && !a.W1) || (a.d + a.e > 0 && !a.w))
     return SPEC_ERR_INVALID_ARG;
+  const bool rnn = a.head == SPEC_HEAD_RNN;
+  if ((a.head != SPEC_HEAD_MARKOV && !rnn) || (rnn && (!a.Wrnn || !a.S))) return SPEC_ERR_INVALID_ARG;
   auto al = [](const void* q, size_t n) { return ((uintptr_t)q % n) == 0; };
   const size_t ls = a.logit_dtype == SPEC_F32 ? 4 : 2, fs = a.fac_dtype == SPEC_F32 ? 4 : 2,
                cs = a.conf_dtype == SPEC_F32 ? 4 : 2;
   if (!al(a.U, ls) || !al(a.A, fs) || !al(a.Ct, fs) || !al(a.x0, 4) || !al(a.draft_temp, 4) ||
       !al(a.x, 4) || !al(a.q_tok, 4) || !al(a.lse_q, 4) || !al(a.sts_temp, 4) || !al(a.c, 4) ||
       !al(a.a, 4) || !al(a.P_out, 4) || !al(a.h, cs) || !al(a.W1, cs) || !al(a.w, cs) ||
-      !al(a.status, 4))
+      !al(a.status, 4) || (rnn && (!al(a.Wrnn, fs) || !al(a.S, fs))))
     return SPEC_ERR_ALIGNMENT;
 
   int dev = 0, major = 0, sms = 0;
@@ -75,7 +77,7 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SPEC_ERR_CUDA;
   const bool tc = a.fac_dtype == SPEC_BF16 && a.r % 64 == 0 && ((size_t)a.V * ls) % 16 == 0 &&
-                  al(a.U, 16) && al(a.A, 16) && al(a.Ct, 16) && major == 10 && sms >= 1 &&
+                  al(a.U, 16) && al(a.A, 16) && al(a.Ct, 16) && (!rnn || al(a.S, 16)) && major == 10 && sms >= 1 &&
                   sms <= kMaxDeviceSms;
 
   // Exact scratch for the path taken: partials [R, splits], then counters [R]
@@ -101,6 +103,10 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
   p.U = a.U;
   p.A = a.A;
   p.Ct = a.Ct;
+  if (rnn) {
+    p.W = a.Wrnn;
+    p.S = a.S;
+  }
   p.x0 = a.x0;
   p.draft_temp = a.draft_temp;
   p.x = a.x;
@@ -125,6 +131,8 @@ extern "C" int spec_draft_sample_static(const spec_draft_args* args, uint64_t se
     t.x0 = a.x0;
     t.draft_temp = a.draft_temp;
     t.A = a.A;
+    t.W = p.W;
+    t.S = p.S;
     t.x = a.x;
     t.q_tok = a.q_tok;
     t.lse_q = a.lse_q;

@@ -36,6 +36,7 @@
 #include "draft.cuh"
 #include "draft_tc.cuh"
 #include "fused_tc.cuh"
+#include "rnn.cuh"
 #include "tc.cuh"
 
 namespace spec {
@@ -68,17 +69,7 @@ __device__ __forceinline__ void merge_position(const DraftTCParams& p, const Par
   acc = race_merge2(acc, race_shfl_xor(acc, 2));
   if (lp != 0) return;
   if (s_x) s_x[row] = m < p.R ? acc.idx : -1;
-  if (write && m < p.R) {
-    const size_t o = (size_t)m * p.gamma + (kpos - 1);
-    p.x[o] = acc.idx;
-    p.q_tok[o] = acc.be / acc.s;
-    // lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s with m in log2 units;
-    // s = 2^k f with f in [1, 2): lse = (m + k) ln 2 + ln f, so only a small
-    // logarithm is taken and one fp64 multiply-add keeps m + k exact.
-    int ks;
-    const float f = 2.f * frexpf(acc.s, &ks);
-    p.lse_q[o] = (float)fma((double)acc.m + (double)(ks - 1), 0.6931471805599453, (double)logf(f));
-  }
+  if (write && m < p.R) store_race(p.x, p.q_tok, p.lse_q, (size_t)m * p.gamma + (kpos - 1), acc);
 }
 
 // Split partials of position kpos: two slots, alternating with the position.
@@ -242,18 +233,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = m < p.R;
     const int V = p.V, rank = p.rank;
 
-    tc::grid_dep_wait();  // the previous position's partials are written
+    tc::grid_dep_wait();  // the previous position's partials (or states) are written
     // x_{k-1}: every CTA of the tile merges the previous position's split
     // partials itself (the previous grid ends without a merge on its critical
-    // path); the CTA of split 0 also writes that position's outputs.
-    if (k > 1) {
+    // path); the CTA of split 0 also writes that position's outputs.  With the
+    // RNN head the state kernel between the two grids has merged them.
+    const bool rnn = p.S != nullptr;
+    if (k > 1 && !rnn) {
       merge_position(p, partial_slot(p, k - 1), m0, k - 1, split == 0, s_x);
       named_bar_sync(2, kEpiWarps * 32);
     }
-    // Gather A_k[x_{k-1}] for the tile's 128 requests: 128 x r bf16 in 16-byte
-    // chunks, 2*KC per thread, all loads in flight before the stores.
+    // Gather the bias rows of the tile's 128 requests -- A_k[x_{k-1}], or the
+    // RNN head's states s_k -- 128 x r bf16 in 16-byte chunks, 2*KC per thread,
+    // all loads in flight before the stores.
     const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
-    {
+    const __nv_bfloat16* Sk = reinterpret_cast<const __nv_bfloat16*>(p.S) + (size_t)(k - 1) * rank;
+    if (rnn) {
+      constexpr int kPer = 128 * KC * 8 / (kEpiWarps * 32);
+      uint4 val[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = threadIdx.x + j * kEpiWarps * 32, c = idx % (KC * 8), mm = m0 + idx / (KC * 8);
+        val[j] = mm < p.R ? *reinterpret_cast<const uint4*>(Sk + (size_t)mm * p.gamma * rank + c * 8)
+                          : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = threadIdx.x + j * kEpiWarps * 32, i = idx / (KC * 8), c = idx % (KC * 8);
+        const int kc = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(sA + kc * 16384 + i * 128 + ((cc ^ (i & 7)) << 4)) = val[j];
+      }
+    } else {
       constexpr int kPer = 128 * KC * 8 / (kEpiWarps * 32);
       int xp[kPer];
 #pragma unroll
@@ -547,8 +557,30 @@ cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* C
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  RnnStateParams q{};
+  if (p.S) {
+    q.R = p.R;
+    q.gamma = p.gamma;
+    q.V = p.V;
+    q.rank = p.rank;
+    q.x0 = p.x0;
+    q.x = p.x;
+    q.q_tok = p.q_tok;
+    q.lse_q = p.lse_q;
+    q.A = p.A;
+    q.W = p.W;
+    q.S = p.S;
+    q.status = p.status;
+  }
   for (int k = 1; k <= p.gamma; ++k) {
     p.k = k;
+    if (p.S) {  // RNN head: merge position k-1, then s_k, before the grid of position k
+      q.k = k;
+      q.nsplit = k > 1 ? p.nsplit : 0;
+      q.part = p.partials + (size_t)((k - 1) & 1) * p.R * p.nsplit;
+      err = launch_rnn_state(q, /*fac_f32=*/false, /*pdl=*/true, stream);
+      if (err != cudaSuccess) return err;
+    }
     err = cudaLaunchKernelEx(&cfg, kern, tm_u, tm_c, p);
     if (err != cudaSuccess) return err;
   }

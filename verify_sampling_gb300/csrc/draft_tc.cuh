@@ -16,6 +16,8 @@ struct DraftTCParams {
   const int32_t* x0;
   const float* draft_temp;
   const void* A;  // bf16 [gamma, V, rank]
+  const void* W;  // RNN head: bf16 [gamma, rank, rank] (null: Markov head)
+  void* S;        // RNN head: bf16 states [R, gamma, rank], 16-byte aligned (null: Markov head)
   int32_t* x;
   float* q_tok;
   float* lse_q;
@@ -28,7 +30,8 @@ struct DraftTCParams {
 // Vocabulary splits per 128-request tile for a device with `device_sms` SMs.
 int draft_tc_nsplit(int R, int V, int device_sms);
 
-// gamma dependent launches (one per position) of the fused kernel.
+// gamma dependent launches (one per position) of the fused kernel; with the RNN
+// head each is preceded by the state kernel of its position.
 cudaError_t launch_draft_tc(const DraftTCParams& p, int logit_dtype, const void* U, const void* Ct,
                             cudaStream_t stream);
 

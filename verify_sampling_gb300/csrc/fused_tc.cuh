@@ -67,6 +67,19 @@ __device__ __forceinline__ Race race_merge2(const Race& a, const Race& b) {
   return o;
 }
 
+// Writes the outputs of a merged race (reference m in log2 units) at index o:
+// the token, q = e_best / s and lse = ln(sum_v exp(z_v / T)) = m ln 2 + ln s.
+// With s = 2^k f, f in [1, 2), lse = (m + k) ln 2 + ln f: only a small
+// logarithm is taken and one fp64 multiply-add keeps m + k exact.
+__device__ __forceinline__ void store_race(int32_t* x, float* q_tok, float* lse_q, size_t o,
+                                           const Race& acc) {
+  x[o] = acc.idx;
+  q_tok[o] = acc.be / acc.s;
+  int ks;
+  const float f = 2.f * frexpf(acc.s, &ks);
+  lse_q[o] = (float)fma((double)acc.m + (double)(ks - 1), 0.6931471805599453, (double)logf(f));
+}
+
 __device__ __forceinline__ Race race_shfl_xor(const Race& st, int mask) {
   Race o;
   o.m = __shfl_xor_sync(0xffffffffu, st.m, mask);

@@ -305,7 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the stages hold exactly nrows rows: lanes past them read row 0 (unused)
     const int lrow = valid ? slot : 0;
     const int V = p.V, rank = p.rank;
-    const __nv_bfloat16* Ak = reinterpret_cast<const __nv_bfloat16*>(p.A) + (size_t)(k - 1) * V * rank;
     for (int idx = threadIdx.x; idx < 128 * KC * 8; idx += kEpiWarps * 32) {
       const int i = idx / (KC * 8), c = idx % (KC * 8);
       uint4 val = make_uint4(0, 0, 0, 0);
@@ -313,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int req = s_req[i % kSlots];
         int xp = (k == 1) ? p.x0[req] : p.x[(size_t)req * G + (k - 2)];
         if (xp < 0 || xp >= V) xp = 0;
-        val = *reinterpret_cast<const uint4*>(Ak + (size_t)xp * rank + c * 8);
+        val = *reinterpret_cast<const uint4*>(bias_row<__nv_bfloat16>(p.A, p.S, V, rank, G, k, req, xp) +
+                                              c * 8);
       }
       const int kc = c >> 3, cc = c & 7;
       *reinterpret_cast<uint4*>(sA + kc * 16384 + i * 128 + ((cc ^ (i & 7)) << 4)) = val;

@@ -15,6 +15,7 @@ struct ResidTCParams {
   const int32_t* x;
   const float* draft_temp;
   const void* A;  // bf16 [gamma, V, rank]
+  const void* S;  // RNN head: bf16 states [R, gamma, rank], 16-byte aligned (null: Markov head)
   const float* lse_q;
   const int32_t* tgt_row_off;
   const float* row_m;       // [R, gamma + 1] target-row softmax reference (log2 units)

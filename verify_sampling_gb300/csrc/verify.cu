@@ -632,9 +632,9 @@ __global__ void __launch_bounds__(kVerifyThreads) residual_kernel(VerifyParams p
   const int k = jstar;
   int x_prev = (k == 1) ? p.x0[r] : p.x[(size_t)r * p.gamma + (k - 2)];
   if (x_prev < 0 || x_prev >= V) x_prev = 0;
-  const TF* A = reinterpret_cast<const TF*>(p.A) + (size_t)(k - 1) * V * rank;
+  const TF* brow = bias_row<TF>(p.A, p.S, V, rank, p.gamma, k, r, x_prev);
   const TF* Ct = reinterpret_cast<const TF*>(p.Ct) + (size_t)(k - 1) * V * rank;
-  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(A, (size_t)x_prev * rank + i);
+  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(brow, (size_t)i);
   __syncthreads();
   const TL* U = reinterpret_cast<const TL*>(p.U) + ((size_t)r * p.gamma + (k - 1)) * V;
   const float inv_tq = 1.0f / p.draft_temp[k - 1];
@@ -748,9 +748,9 @@ __global__ void __launch_bounds__(kVerifyThreads) cstar_kernel(VerifyParams p) {
   const TT* L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, r, k) * (size_t)V;
   int x_prev = (k == 1) ? p.x0[r] : p.x[(size_t)r * G + (k - 2)];
   if (x_prev < 0 || x_prev >= V) x_prev = 0;
-  const TF* A = reinterpret_cast<const TF*>(p.A) + (size_t)(k - 1) * V * rank;
+  const TF* brow = bias_row<TF>(p.A, p.S, V, rank, p.gamma, k, r, x_prev);
   const TF* Ct = reinterpret_cast<const TF*>(p.Ct) + (size_t)(k - 1) * V * rank;
-  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(A, (size_t)x_prev * rank + i);
+  for (int i = threadIdx.x; i < rank; i += blockDim.x) arow[i] = ld_f(brow, (size_t)i);
   __syncthreads();
   const TL* U = reinterpret_cast<const TL*>(p.U) + ((size_t)r * G + (k - 1)) * V;
   const float inv_tq = 1.0f / p.draft_temp[k - 1];
@@ -881,6 +881,7 @@ static cudaError_t launch_typed(const VerifyParams& p, int tgt_dtype, int logit_
   t.x = p.x;
   t.draft_temp = p.draft_temp;
   t.A = p.A;
+  t.S = p.S;
   t.lse_q = p.lse_q;
   t.tgt_row_off = p.tgt_row_off;
   t.row_m = p.ws.row_m;

@@ -49,6 +49,7 @@ struct VerifyParams {
   const void* U;
   const void* A;
   const void* Ct;
+  const void* S;  // RNN head: states [R, gamma, rank] in the factor dtype (null: Markov head)
   const int32_t* x0;
   const float* draft_temp;
   int32_t* accept_len;
