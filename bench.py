@@ -53,6 +53,9 @@ def _args():
     p.add_argument("--head", default="markov", choices=["markov", "rnn"],
                    help="sequential draft head: the Markov head, or the RNN head with a "
                         "recurrent state (synthetic recurrence W_k ~ N(0, 1/r))")
+    p.add_argument("--async-cap", action="store_true",
+                   help="cap each round's admissions by the uncapped count of the round two "
+                        "earlier, kept on the device (the first two rounds use K)")
     p.add_argument("--calibration", action="store_true",
                    help="also compute c* = sum min(p, q) of every verified row and fold the "
                         "round into the reliability diagram (ECE)")
@@ -70,6 +73,10 @@ def _workload(args):
         if wl.mode == "greedy":
             raise SystemExit("--head applies to workloads with a draft stage")
         wl = dataclasses.replace(wl, head=args.head)
+    if args.async_cap:
+        if wl.mode == "greedy":
+            raise SystemExit("--async-cap applies to workloads with a schedule")
+        wl = dataclasses.replace(wl, async_cap=True)
     return wl
 
 
@@ -144,10 +151,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- reference ----
-def _oracle_round(wl, inp_cpu, seed: int, n_req: int) -> tuple[int, float]:
+def _oracle_round(wl, inp_cpu, seed: int, n_req: int, chain=None) -> tuple[int, float]:
     """The oracle as it stands on a sub-batch of n_req requests of the workload:
     draft, confidence, schedule over the sub-batch, verify.  Returns
-    (positions, seconds)."""
+    (positions, seconds).  With the asynchronous cap, `chain` (a list kept by
+    the caller) holds the uncapped counts of the earlier rounds."""
     import numpy as np
     import oracle
     t0 = time.perf_counter()
@@ -174,6 +182,11 @@ def _oracle_round(wl, inp_cpu, seed: int, n_req: int) -> tuple[int, float]:
     _, a = oracle.confidence(f(inp_cpu["h"][:n_req]), inp_cpu["W1_np"], inp_cpu["w_np"], x0, d.x,
                              inp_cpu["sts_temp"].numpy())
     K = max(1, round(wl.K * n_req / wl.R))
+    if wl.async_cap and chain is not None:
+        if len(chain) >= 2:
+            K = min(K, chain[-2])
+        chain.append(oracle.schedule(a, inp_cpu["sps"].numpy(), inp_cpu["b_lo"], inp_cpu["b_step"],
+                                     n_req * G, wl.sched_mode, wl.sched_threshold).n)
     s = oracle.schedule(a, inp_cpu["sps"].numpy(), inp_cpu["b_lo"], inp_cpu["b_step"], K,
                         wl.sched_mode, wl.sched_threshold)
     rows = f(inp_cpu["tgt"][:n_req]).reshape(-1, wl.V)
@@ -212,8 +225,9 @@ def cpu_baseline(wl, budget_s: float = 15.0) -> dict:
     inp = _cpu_inputs(wl)
     n = min(wl.R, 8)
     pos_tot, sec_tot, rounds = 0, 0.0, 0
+    chain = []
     while sec_tot < budget_s and rounds < 1000:
-        pos, sec = _oracle_round(wl, inp, 100 + rounds, n)
+        pos, sec = _oracle_round(wl, inp, 100 + rounds, n, chain)
         pos_tot, sec_tot, rounds = pos_tot + pos, sec_tot + sec, rounds + 1
     return {"value": pos_tot / sec_tot, "unit": "positions/s", "cores": 1, "kind": "oracle",
             "sample": f"{rounds} rounds of {n} of the {wl.R} requests of the same workload "
@@ -228,8 +242,9 @@ def _cpu_worker(args):
     inp = _cpu_inputs(wl)
     n = min(wl.R, 8)
     pos_tot, sec_tot, rounds = 0, 0.0, 0
+    chain = []
     while sec_tot < budget_s and rounds < 1000:
-        pos, sec = _oracle_round(wl, inp, 100000 * (wid + 1) + rounds, n)
+        pos, sec = _oracle_round(wl, inp, 100000 * (wid + 1) + rounds, n, chain)
         pos_tot, sec_tot, rounds = pos_tot + pos, sec_tot + sec, rounds + 1
     return pos_tot, sec_tot, rounds
 
@@ -259,8 +274,9 @@ def run_reference(args, wl):
     for i in range(args.warmup):
         _oracle_round(wl, inp, 100 + i, 1)
     tot_pos, tot_sec = 0, 0.0
+    chain = []
     for i in range(args.steps):
-        p, s = _oracle_round(wl, inp, 1000 + i, n)
+        p, s = _oracle_round(wl, inp, 1000 + i, n, chain)
         tot_pos += p
         tot_sec += s
     value = tot_pos / tot_sec
@@ -304,6 +320,8 @@ def _sched_config(wl) -> dict:
     out = {"sched_mode": names[wl.sched_mode]}
     if wl.sched_mode == 2:
         out["sched_threshold"] = wl.sched_threshold
+    if wl.async_cap:
+        out["async_cap"] = "K_t = uncapped n of round t-2"
     return out
 
 
@@ -351,6 +369,8 @@ def main():
                    "count": torch.zeros(1, G, dtype=torch.int64, device=dev),
                    "estimate": torch.zeros(G, dtype=torch.float64, device=dev)}
     calib = vs.calibration_tables(10, dev) if args.calibration and not greedy else None
+    # asynchronous cap: word t % 2 holds the uncapped count of round t - 2
+    cap_words = torch.full((2,), wl.K, dtype=torch.int32, device=dev) if wl.async_cap else None
     stream = torch.cuda.current_stream()
     nev = max(1, args.steps)
     ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
@@ -368,8 +388,10 @@ def main():
         d = vs.draft_sample(din, seed, out=bufs["draft"], workspace=bufs["ws_draft"])
         if timed:
             ev["d1"][i].record(stream)
+        word = cap_words[i % 2: i % 2 + 1] if cap_words is not None else None
         s = vs.schedule(d["a"], g["sps"], g["b_lo"], g["b_step"], wl.K, wl.sched_mode,
-                        threshold=wl.sched_threshold, out=bufs.get("sched"))
+                        threshold=wl.sched_threshold, K_dev=word, n_free=word,
+                        out=bufs.get("sched"))
         bufs["sched"] = s
         if timed:
             ev["s1"][i].record(stream)

@@ -196,6 +196,20 @@ int spec_draft_sample_static(const spec_draft_args *args, uint64_t seed, spec_st
  * + 1 + l_r (the packed verify layout); stats [4] f64 = {n, B, tau, Theta};
  * order [R * gamma] int32 (nullable) = candidate ids r * gamma + j - 1 in
  * sorted order.  Sizes: R * gamma <= 8192 (one thread block).
+ *
+ * Asynchronous cap (DSpark summary, "挑战2"): the verification capacity of a
+ * round is capped from the confidences of two rounds earlier, while the
+ * candidates themselves are ranked by the newest survivals; the history
+ * article, "杀招三", adds that the scheduler uses the previous batch's estimate
+ * so the GPU never waits for the host.  Reading: K_t = the number the same
+ * rule admits on round t-2's survivals with no cap.  Both ends stay on the
+ * device:
+ *   n_free  (nullable) receives that uncapped number for this round's a;
+ *   K_dev   (nullable) is read on the device: the cap becomes
+ *           min(K, max(K_dev[0], 0)).
+ * A caller keeps two int32 words, passes word t % 2 as both K_dev and n_free
+ * in round t (the kernel reads K_dev before it writes n_free), and fills both
+ * with K before the first round.  With both NULL the call is as above.
  */
 typedef struct spec_sched_args {
   int R, gamma;
@@ -213,6 +227,8 @@ typedef struct spec_sched_args {
   size_t workspace_bytes;
   uint32_t *status;
   double threshold;
+  const int32_t *K_dev; /* nullable device word: cap = min(K, max(K_dev[0], 0)) */
+  int32_t *n_free;      /* nullable device word: n the same rule admits with no cap */
 } spec_sched_args;
 
 int spec_schedule(const spec_sched_args *args, spec_stream_t stream);

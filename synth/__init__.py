@@ -58,6 +58,7 @@ class Workload:
     sts_ramp: bool = False
     sched_threshold: float = 0.0  # read by the static-threshold mode only
     head: str = "markov"          # sequential head: "markov" or "rnn" (rnn_weights)
+    async_cap: bool = False       # cap round t by the uncapped count of round t - 2
 
     def scaled(self, **kw) -> "Workload":
         """Same recipe at other sizes (for parity cases the oracle finishes quickly).

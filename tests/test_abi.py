@@ -56,7 +56,8 @@ def test_struct_layout_matches_c(spec, tmp_path):
         "P(spec_draft_args, status) P(spec_draft_args, workspace_bytes) P(spec_draft_args, U)\n"
         "P(spec_draft_args, head) P(spec_draft_args, Wrnn) P(spec_draft_args, S)\n"
         "P(spec_sched_args, b_lo) P(spec_sched_args, stats) P(spec_sched_args, status)\n"
-        "P(spec_sched_args, threshold) P(spec_accept_stats_args, beta)\n"
+        "P(spec_sched_args, threshold) P(spec_sched_args, K_dev) P(spec_sched_args, n_free)\n"
+        "P(spec_accept_stats_args, beta)\n"
         "P(spec_accept_stats_args, ema) P(spec_accept_stats_args, status)\n"
         "P(spec_verify_args, c_star) P(spec_calibration_args, n_bins)\n"
         "P(spec_calibration_args, ece) P(spec_calibration_args, status)\n"
@@ -84,6 +85,8 @@ def test_struct_layout_matches_c(spec, tmp_path):
                               "spec_sched_args.stats": (spec.SchedArgs, "stats"),
                               "spec_sched_args.status": (spec.SchedArgs, "status"),
                               "spec_sched_args.threshold": (spec.SchedArgs, "threshold"),
+                              "spec_sched_args.K_dev": (spec.SchedArgs, "K_dev"),
+                              "spec_sched_args.n_free": (spec.SchedArgs, "n_free"),
                               "spec_accept_stats_args.beta": (spec.AcceptStatsArgs, "beta"),
                               "spec_accept_stats_args.ema": (spec.AcceptStatsArgs, "ema"),
                               "spec_accept_stats_args.status": (spec.AcceptStatsArgs, "status"),
@@ -154,6 +157,11 @@ def test_host_side_rejections_launch_nothing(spec):
     s.stats = ctypes.c_void_p(260)  # not 8-byte aligned
     assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_ALIGNMENT
     s.stats = ctypes.c_void_p(256)
+    s.n_free = ctypes.c_void_p(258)  # not 4-byte aligned
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_ALIGNMENT
+    s.n_free, s.K_dev = None, ctypes.c_void_p(257)
+    assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_ALIGNMENT
+    s.K_dev = None
     s.mode, s.threshold = spec.SCHED_THRESHOLD, float("nan")
     assert lib.spec_schedule(ctypes.byref(s), None) == spec.SPEC_ERR_INVALID_ARG
     s.mode = 3

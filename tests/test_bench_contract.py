@@ -11,10 +11,12 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("config,head", [("c2", "markov"), ("greedy", "markov"), ("c2", "rnn")])
-def test_reference_arm_json_line(config, head):
+@pytest.mark.parametrize("config,head,extra", [("c2", "markov", []), ("greedy", "markov", []),
+                                               ("c2", "rnn", []), ("c5", "markov", ["--async-cap"])])
+def test_reference_arm_json_line(config, head, extra):
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--config", config, "--steps", "1", "--warmup", "1", "--head", head],
+                          "--config", config, "--steps", "3", "--warmup", "1", "--head", head,
+                          *extra],
                          capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
@@ -22,7 +24,8 @@ def test_reference_arm_json_line(config, head):
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["metric"] == "draft+verified positions/s"
     assert line["value"] > 0 and line["unit"] == "positions/s" and line["higher_is_better"]
-    assert line["steps"] == 1 and line["warmup"] == 1 and line["config"]["workload"] == config
+    assert line["steps"] == 3 and line["warmup"] == 1 and line["config"]["workload"] == config
+    assert ("async_cap" in line["config"]) == bool(extra)
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"].get("head", "markov") == head

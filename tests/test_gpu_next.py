@@ -243,3 +243,43 @@ def test_calibration_bad_entries_and_empty():
                    torch.zeros(0, dtype=torch.int32, device=DEV), empty)
     torch.cuda.synchronize()
     assert np.isnan(float(empty["ece"].item()))
+
+
+def _level_survivals(rng, R, gamma, lo):
+    c = rng.uniform(lo, 1.0, (R, gamma)).astype(np.float32)
+    return np.cumprod(c, axis=1, dtype=np.float32)
+
+
+@pytest.mark.parametrize("mode", [oracle.SCHED_EARLY_STOP, oracle.SCHED_GLOBAL,
+                                  oracle.SCHED_THRESHOLD])
+def test_async_cap_chain(mode):
+    """DSpark summary, "挑战2": round t is capped by the uncapped count of
+    round t - 2, through one device word per parity of t (read, then written,
+    by the same launch).  Every round's decision and its uncapped count equal
+    the oracle's, run with the cap the oracle's own chain gives."""
+    R, gamma, K = 512, 11, 2048
+    N = R * gamma
+    rng = np.random.default_rng(90 + mode)
+    # confidence levels that make the two-rounds-back cap bind (a low round
+    # followed, two rounds later, by a high one)
+    levels = [0.05, 0.1, 0.9, 0.95, 0.2, 0.6]
+    sps = _sps(R, gamma).to(DEV)
+    sps_np = to_np(sps).astype(np.float64)
+    thr = 0.3
+    cap = torch.full((2,), K, dtype=torch.int32, device=DEV)
+    free_seen, bound = [], 0
+    for t, lo in enumerate(levels):
+        a_np = _level_survivals(rng, R, gamma, lo)
+        a = torch.tensor(a_np, device=DEV)
+        word = cap[t % 2: t % 2 + 1]
+        s = vs.schedule(a, sps, 1.0, 1.0, K, mode, threshold=thr, K_dev=word, n_free=word)
+        torch.cuda.synchronize()
+        k_t = K if t < 2 else min(K, free_seen[t - 2])
+        inp = {"sps": sps, "b_lo": 1.0, "b_step": 1.0}
+        rep = compare_schedule(inp, a, s, k_t, mode, threshold=thr)
+        of = oracle.schedule(a_np.astype(np.float64), sps_np, 1.0, 1.0, N, mode, thr)
+        if of.margin >= 1e-6 and rep.near_ties == 0:
+            assert int(word.item()) == of.n, (t, int(word.item()), of.n)
+        free_seen.append(int(word.item()))
+        bound += int(int(to_np(s["stats"])[0]) < min(K, of.n))
+    assert bound >= 1  # the lagged cap took effect at least once

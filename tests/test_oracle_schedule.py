@@ -229,3 +229,41 @@ def test_threshold_sweep_raises_acceptance_rate():
         assert sim == pytest.approx(out.tau / out.n, abs=0.01)
     assert all(x <= y for x, y in zip(rates, rates[1:]))
     assert rates[-1] > rates[0] + 0.1
+
+
+@pytest.mark.parametrize("mode", [oracle.SCHED_EARLY_STOP, oracle.SCHED_THRESHOLD])
+def test_cap_truncates_the_uncapped_decision(mode):
+    """DSpark summary, "挑战2": the asynchronous cap only limits how many of
+    the newest-ranked candidates are admitted.  For the rules that stop at the
+    first failing candidate, the capped count is min(uncapped count, K) and
+    the admitted set is the first n of the same sorted order -- what the
+    device kernel uses to take both decisions from one scan."""
+    rng = np.random.default_rng(11 + mode)
+    R, gamma = 40, 6
+    B = np.arange(1, R * (gamma + 1) + 1, dtype=np.float64)
+    sps = 1.0 / (0.01 + 5e-4 * B)
+    for trial in range(20):
+        c = rng.uniform(0.05 * (trial % 10), 1.0, (R, gamma))
+        a = np.cumprod(c, axis=1)
+        free = oracle.schedule(a, sps, 1.0, 1.0, R * gamma, mode, 0.3)
+        for K in (0, 1, free.n // 2, free.n, free.n + 3, R * gamma):
+            got = oracle.schedule(a, sps, 1.0, 1.0, K, mode, 0.3)
+            assert got.n == min(free.n, K)
+            assert np.array_equal(got.order[:got.n], free.order[:got.n])
+
+
+def test_global_cap_is_the_argmax_below_the_cap():
+    """Global search under a cap: the smallest argmax of Theta over n <= K,
+    which may differ from the uncapped argmax truncated to K."""
+    rng = np.random.default_rng(5)
+    R, gamma = 30, 5
+    B = np.arange(1, R * (gamma + 1) + 1, dtype=np.float64)
+    sps = (1.0 + 0.3 * ((B % 20) / 20.0)) / (0.01 + 5e-4 * B)  # sawtooth
+    for _ in range(10):
+        a = np.cumprod(rng.uniform(0.2, 1.0, (R, gamma)), axis=1)
+        full = oracle.schedule(a, sps, 1.0, 1.0, R * gamma, oracle.SCHED_GLOBAL)
+        th = full.theta_seq
+        for K in (1, 7, full.n // 2, full.n, R * gamma):
+            got = oracle.schedule(a, sps, 1.0, 1.0, K, oracle.SCHED_GLOBAL)
+            want = int(np.argmax(th[: min(K, R * gamma) + 1]))
+            assert got.n == want

@@ -54,7 +54,7 @@ class SchedArgs(ctypes.Structure):
                 ("K", ctypes.c_int), ("mode", ctypes.c_int), ("ell", _P), ("row_off", _P),
                 ("stats", _P), ("order", _P), ("workspace", _P),
                 ("workspace_bytes", ctypes.c_size_t), ("status", _P),
-                ("threshold", ctypes.c_double)]
+                ("threshold", ctypes.c_double), ("K_dev", _P), ("n_free", _P)]
 
 
 class AcceptStatsArgs(ctypes.Structure):
@@ -262,7 +262,8 @@ def draft_sample(inp: DraftInputs, seed: int, *, want_P: bool = False, out: Opti
 
 
 # ----------------------------------------------------------------- schedule --
-def _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status) -> SchedArgs:
+def _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status, K_dev=None,
+                  n_free=None) -> SchedArgs:
     R, gamma = a.shape
     s = SchedArgs()
     s.R, s.gamma = R, gamma
@@ -272,15 +273,22 @@ def _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status) -> Sch
     s.ell, s.row_off, s.stats = _ptr(outs["ell"]), _ptr(outs["row_off"]), _ptr(outs["stats"])
     s.order = _ptr(outs.get("order"))
     s.status = _ptr(status)
+    for name, t in (("K_dev", K_dev), ("n_free", n_free)):
+        if t is not None and (_dev(t, name).dtype != torch.int32 or t.numel() < 1):
+            raise TypeError(f"{name} must be an int32 device tensor")
+    s.K_dev, s.n_free = _ptr(K_dev), _ptr(n_free)
     return s
 
 
 def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: int,
              mode: int = SCHED_EARLY_STOP, *, threshold: float = 0.0, want_order: bool = False,
+             K_dev: Optional[torch.Tensor] = None, n_free: Optional[torch.Tensor] = None,
              out: Optional[dict] = None, status: Optional[torch.Tensor] = None,
              stream=None) -> dict:
     """spec_schedule: l_r, packed row offsets and {n, B, tau, Theta} on the device.
-    ``threshold`` is read by SCHED_THRESHOLD only (admit survivals >= threshold)."""
+    ``threshold`` is read by SCHED_THRESHOLD only (admit survivals >= threshold).
+    Asynchronous cap: ``K_dev`` (int32 device word, may alias ``n_free``) lowers
+    the cap to min(K, K_dev[0]); ``n_free`` receives the uncapped n."""
     a = _dev(a, "a")
     sps = _dev(sps, "sps")
     if a.dtype != torch.float32 or sps.dtype != torch.float32:
@@ -293,7 +301,7 @@ def schedule(a: torch.Tensor, sps: torch.Tensor, b_lo: float, b_step: float, K: 
         "stats": torch.empty(4, dtype=torch.float64, device=dev)}
     if want_order and "order" not in outs:
         outs["order"] = torch.empty(R * gamma, dtype=torch.int32, device=dev)
-    s = _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status)
+    s = _sched_struct(a, sps, b_lo, b_step, K, mode, threshold, outs, status, K_dev, n_free)
     _check(lib().spec_schedule(ctypes.byref(s), _stream_handle(stream)), "spec_schedule")
     return outs
 

@@ -227,7 +227,8 @@ int spec_schedule(const spec_sched_args* args, spec_stream_t stream) {
   if (!a.a || !a.sps || !a.ell || !a.row_off || !a.stats) return SPEC_ERR_INVALID_ARG;
   if ((long)a.R * a.gamma > kSchedMaxCandidates) return SPEC_ERR_UNSUPPORTED;
   if (!aligned(a.a, 4) || !aligned(a.sps, 4) || !aligned(a.ell, 4) || !aligned(a.row_off, 4) ||
-      !aligned(a.stats, 8) || !aligned(a.order, 4) || !aligned(a.status, 4))
+      !aligned(a.stats, 8) || !aligned(a.order, 4) || !aligned(a.status, 4) ||
+      !aligned(a.K_dev, 4) || !aligned(a.n_free, 4))
     return SPEC_ERR_ALIGNMENT;
   SchedParams p{};
   p.R = a.R;
@@ -244,6 +245,8 @@ int spec_schedule(const spec_sched_args* args, spec_stream_t stream) {
   p.row_off = a.row_off;
   p.stats = a.stats;
   p.order = a.order;
+  p.K_dev = a.K_dev;
+  p.n_free = a.n_free;
   p.status = a.status;
   return launch_schedule(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK
                                                                                     : SPEC_ERR_CUDA;

@@ -176,9 +176,14 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
 
   // 3. zero the per-request counts; SPS(R + n) for every admissible n, in
   // parallel (theta[n] holds it until step 4 multiplies in tau_n).
-  const int nmax = min(p.K, N);
+  // The cap: K, lowered by the device word K_dev when given (asynchronous cap).
+  // With n_free requested, Theta is formed for every n so that the uncapped
+  // decision can be taken too.
+  const int kcap = p.K_dev ? min(p.K, max(*p.K_dev, 0)) : p.K;
+  const int nmax = min(kcap, N);
+  const int ntheta = p.n_free ? N : nmax;
   for (int i = tid; i < p.R; i += kThreads) ell_s[i] = 0;
-  for (int n = tid; n <= nmax; n += kThreads) {
+  for (int n = tid; n <= ntheta; n += kThreads) {
     double v = 0.0;
     if (n > 0) {
       if (p.unit_grid) {
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
       if (i < cnt) {
         run += qv[i];
         const int n = lo + i + 1;
-        if (n <= nmax) theta[n] = __dmul_rn(__dmul_rn((double)run, unit), theta[n]);
+        if (n <= ntheta) theta[n] = __dmul_rn(__dmul_rn((double)run, unit), theta[n]);
       }
     seg_q[tid] = warp_q[warp] + incl - local;
   }
@@ -257,9 +262,10 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
   // 5. choose n*.
   if (p.mode != SPEC_SCHED_GLOBAL) {
     // first sorted position that stops the admission
+    // The first stop over all of [0, ntheta); the capped n* is min(first, nmax).
     const bool thr = p.mode == SPEC_SCHED_THRESHOLD;
-    int first = nmax;
-    for (int n = tid; n < nmax; n += kThreads) {
+    int first = ntheta;
+    for (int n = tid; n < ntheta; n += kThreads) {
       const bool stop = thr ? !((double)__uint_as_float(~keyA[n]) >= p.threshold)
                             : !(theta[n + 1] > theta[n]);
       if (stop) first = min(first, n);
@@ -269,41 +275,52 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(SchedParams p) {
     if (lane == 0) bestn_s[warp] = first;
     __syncthreads();
     if (tid == 0) {
-      int f = nmax;
+      int f = ntheta;
       for (int w = 0; w < kThreads / 32; ++w) f = min(f, bestn_s[w]);
-      nstar_s = f;
+      nstar_s = min(f, nmax);
+      if (p.n_free) *p.n_free = f;
     }
   } else {
-    double best = -1.0;
-    int bn = 0;
-    for (int n = tid; n <= nmax; n += kThreads)
-      if (theta[n] > best) {
-        best = theta[n];
-        bn = n;
-      }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const double ob = __shfl_down_sync(0xffffffffu, best, off);
-      const int on = __shfl_down_sync(0xffffffffu, bn, off);
-      if (ob > best || (ob == best && on < bn)) {
-        best = ob;
-        bn = on;
-      }
-    }
-    if (lane == 0) {
-      best_s[warp] = best;
-      bestn_s[warp] = bn;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      double b = -1.0;
-      int n = 0;
-      for (int w = 0; w < kThreads / 32; ++w)
-        if (best_s[w] > b || (best_s[w] == b && bestn_s[w] < n)) {
-          b = best_s[w];
-          n = bestn_s[w];
+    // smallest argmax of Theta over n <= lim, block-wide (result in thread 0)
+    auto argmax_upto = [&](int lim) -> int {
+      double best = -1.0;
+      int bn = 0;
+      for (int n = tid; n <= lim; n += kThreads)
+        if (theta[n] > best) {
+          best = theta[n];
+          bn = n;
         }
-      nstar_s = n;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const double ob = __shfl_down_sync(0xffffffffu, best, off);
+        const int on = __shfl_down_sync(0xffffffffu, bn, off);
+        if (ob > best || (ob == best && on < bn)) {
+          best = ob;
+          bn = on;
+        }
+      }
+      if (lane == 0) {
+        best_s[warp] = best;
+        bestn_s[warp] = bn;
+      }
+      __syncthreads();
+      int n = 0;
+      if (tid == 0) {
+        double b = -1.0;
+        for (int w = 0; w < kThreads / 32; ++w)
+          if (best_s[w] > b || (best_s[w] == b && bestn_s[w] < n)) {
+            b = best_s[w];
+            n = bestn_s[w];
+          }
+      }
+      __syncthreads();  // best_s may be reused by the next call
+      return n;
+    };
+    const int n_cap = argmax_upto(nmax);
+    if (tid == 0) nstar_s = n_cap;
+    if (p.n_free) {
+      const int n_all = argmax_upto(ntheta);
+      if (tid == 0) *p.n_free = n_all;
     }
   }
   __syncthreads();

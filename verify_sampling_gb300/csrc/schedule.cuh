@@ -19,6 +19,8 @@ struct SchedParams {
   int32_t* row_off;
   double* stats;
   int32_t* order;
+  const int32_t* K_dev;  // nullable: cap = min(K, max(*K_dev, 0)), read on the device
+  int32_t* n_free;       // nullable: the rule's n with no cap
   uint32_t* status;
 };
 
