@@ -35,6 +35,10 @@ CASES = {
     # W_k too large to stage in shared memory (read from global memory instead)
     "tc_c5_r256": synth.WORKLOADS["c5"].scaled(R=6, gamma=3, V=2048, d=16, r=256),
     "fp32_r160": synth.WORKLOADS["tiny"].scaled(R=5, gamma=3, V=777, r=160),
+    # degenerate sizes: one token, one position, one request
+    "v1": synth.WORKLOADS["tiny"].scaled(R=2, gamma=1, V=1, r=1, d=3, e=1),
+    "r1_gamma1": synth.WORKLOADS["c2"].scaled(R=1, gamma=1, V=4097, d=64, e=16, r=16),
+    "tc_gamma1": synth.WORKLOADS["c5"].scaled(R=3, gamma=1, V=2048, d=16, r=64),
 }
 SAMPLED = {"tc_c3_small_R130": [0, 1, 2, 64, 127, 128, 129]}
 
