@@ -493,7 +493,8 @@ def main():
 
     # ----------------------------------------------------- e2e (rank 0) ----
     if rank == 0 and not args.no_e2e and not greedy:
-        line["e2e"] = _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 5))
+        line["e2e"] = _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 5),
+                           cap_words=cap_words)
     if rank == 0 and not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl)
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(wl)
@@ -504,11 +505,14 @@ def main():
         dist.destroy_process_group()
 
 
-def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
-    """Same round through the public API with the per-step inputs (U, h, x0,
-    target logits) copied from pinned host memory each step and the results
+def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None) -> dict:
+    """Same round through the public API (one spec_round_host call per step)
+    with the per-step inputs taken from pinned host memory and the results
     (tokens, lengths, stats) copied back; the model weights (A, Ct, W1, w) stay
-    resident."""
+    resident.  U, h and x0 are copied whole.  Of the target logits, held on the
+    host for every candidate row [R, gamma + 1, V], only the B rows the
+    schedule admits are read -- the rows a target model computes for the
+    round -- by the library's gather from the mapped host buffer."""
     names = ["U", "h", "x0", "tgt"]
     host = {n: g[n].cpu().pin_memory() for n in names}
     devb = {n: torch.empty_like(g[n]) for n in names}
@@ -516,7 +520,8 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
             "accept_len": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
             "n_out": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
             "stats": torch.empty(4, dtype=torch.float64).pin_memory()}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    whole = sum(host[n].numel() * host[n].element_size() for n in ("U", "h", "x0"))
+    row_bytes = wl.V * host["tgt"].element_size()
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
     d_in = vs.DraftInputs(U=devb["U"], A=g["A"], Ct=g["Ct"], x0=devb["x0"],
                           draft_temp=g["draft_temp"], h=devb["h"], W1=g["W1"], w=g["w"],
@@ -530,17 +535,26 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int) -> dict:
         vs.run_round_host(d_in, devb["tgt"].view(-1, wl.V), g["tgt_row_off"], g["sps"], g["b_lo"],
                           g["b_step"], wl.K, 9000 + i, host_in=host, host_out=host_out,
                           sched_mode=wl.sched_mode, sched_threshold=wl.sched_threshold,
+                          tgt_scheduled_only=True,
+                          K_dev=None if cap_words is None else cap_words[i % 2: i % 2 + 1],
+                          n_free=None if cap_words is None else cap_words[i % 2: i % 2 + 1],
                           bufs={"draft": bufs["draft"], "ws_draft": bufs["ws_draft"],
                                 "ws_verify": bufs["ws_verify"]})
         torch.cuda.synchronize()
-        return wl.R * wl.gamma + float(outs["stats"][1])
+        B = float(outs["stats"][1])
+        return wl.R * wl.gamma + B, B
 
     one(-1)
     t0 = time.perf_counter()
-    pos = sum(one(i) for i in range(steps))
+    res = [one(i) for i in range(steps)]
     sec = time.perf_counter() - t0
-    return {"value": pos / sec, "unit": "positions/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+    pos = sum(p for p, _ in res)
+    B_mean = sum(b for _, b in res) / steps
+    return {"value": pos / sec, "unit": "positions/s",
+            "h2d_bytes_per_step": int(whole + B_mean * row_bytes),
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "target_rows": "the B scheduled rows of each step (mean %.1f), read from the "
+                           "pinned [R, gamma+1, V] host array" % B_mean}
 
 
 if __name__ == "__main__":

@@ -388,6 +388,17 @@ int spec_verify(const spec_verify_args *args, uint64_t seed, spec_stream_t strea
  *   out_tok_host [R, gamma + 1], accept_len_host [R], n_out_host [R] int32
  *     and stats_host [4] f64 (the schedule's {n, B, tau, Theta}): per-round
  *     outputs, each nullable.
+ *   tgt_scheduled_only  nonzero: tgt_host holds every candidate row of every
+ *     request, padded [R, gamma + 1, V], and only the rows the schedule
+ *     admits -- rows 1 .. l_r + 1 of request r, B in all, the rows a target
+ *     model computes for the round -- cross the link: after the schedule a
+ *     kernel reads them through the device's mapping of tgt_host and writes
+ *     them to verify->tgt in the packed layout of sched->row_off, with no
+ *     host synchronisation.  Then verify->tgt_row_off must be sched->row_off,
+ *     verify->tgt must hold R * (gamma + 1) rows, tgt_rows is ignored, and
+ *     tgt_host must be page-locked memory the device can address
+ *     (cudaHostAlloc, cudaHostRegister): SPEC_ERR_UNSUPPORTED otherwise.
+ *     Zero: tgt_host's tgt_rows rows are copied as they are, before the draft.
  * Returns the first stage's error, or SPEC_ERR_CUDA when a copy fails to
  * enqueue.
  */
@@ -404,6 +415,7 @@ typedef struct spec_round_host_args {
   int32_t *accept_len_host;
   int32_t *n_out_host;
   double *stats_host;
+  int tgt_scheduled_only;
 } spec_round_host_args;
 
 int spec_round_host(const spec_round_host_args *args, uint64_t seed, spec_stream_t stream);

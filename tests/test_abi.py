@@ -62,6 +62,7 @@ def test_struct_layout_matches_c(spec, tmp_path):
         "P(spec_verify_args, c_star) P(spec_calibration_args, n_bins)\n"
         "P(spec_calibration_args, ece) P(spec_calibration_args, status)\n"
         "P(spec_round_host_args, tgt_rows) P(spec_round_host_args, stats_host)\n"
+        "P(spec_round_host_args, tgt_scheduled_only)\n"
         "P(spec_verify_args, target_temp) P(spec_verify_args, draft) P(spec_verify_args, status)\n"
         "return 0;}\n")
     exe = tmp_path / "layout"
@@ -96,6 +97,8 @@ def test_struct_layout_matches_c(spec, tmp_path):
                               "spec_calibration_args.status": (spec.CalibrationArgs, "status"),
                               "spec_round_host_args.tgt_rows": (spec.RoundHostArgs, "tgt_rows"),
                               "spec_round_host_args.stats_host": (spec.RoundHostArgs, "stats_host"),
+                              "spec_round_host_args.tgt_scheduled_only":
+                                  (spec.RoundHostArgs, "tgt_scheduled_only"),
                               "spec_verify_args.target_temp": (spec.VerifyArgs, "target_temp"),
                               "spec_verify_args.draft": (spec.VerifyArgs, "draft"),
                               "spec_verify_args.status": (spec.VerifyArgs, "status")}.items():

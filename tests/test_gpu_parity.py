@@ -158,11 +158,13 @@ def test_deterministic_reruns():
             assert torch.equal(x[k], y[k]), k
 
 
+@pytest.mark.parametrize("packed", [False, True])
 @pytest.mark.parametrize("name", ["tc_c5_small", "c3_small"])
-def test_round_host_matches_device_round(name):
+def test_round_host_matches_device_round(name, packed):
     """spec_round_host: the per-round inputs come from host buffers and the
     results go back to host buffers; the round equals the device-resident one
-    and its tokens match the oracle's round on the same inputs."""
+    and its tokens match the oracle's round on the same inputs.  packed: only
+    the scheduled target rows are read from the host, into the packed layout."""
     wl = SMALL[name]
     inp = synth.make_inputs(wl, "cpu")
     g = _to_dev(inp)
@@ -180,10 +182,18 @@ def test_round_host_matches_device_round(name):
                 "accept_len": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
                 "n_out": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
                 "stats": torch.empty(4, dtype=torch.float64).pin_memory()}
-    vs.run_round_host(synth.draft_inputs(g2), g2["tgt"].view(-1, wl.V), g2["tgt_row_off"],
-                      g2["sps"], g2["b_lo"], g2["b_step"], wl.K, seed, host_in=host_in,
-                      host_out=host_out)
+    g2["tgt"].fill_(float("nan"))  # rows the packed gather does not write stay NaN
+    res = vs.run_round_host(synth.draft_inputs(g2), g2["tgt"].view(-1, wl.V), g2["tgt_row_off"],
+                            g2["sps"], g2["b_lo"], g2["b_step"], wl.K, seed, host_in=host_in,
+                            host_out=host_out, tgt_scheduled_only=packed)
     torch.cuda.synchronize()
+    if packed:  # the device buffer holds exactly the B scheduled rows, packed
+        ro, ell = res["sched"]["row_off"].cpu(), res["sched"]["ell"].cpu()
+        rows = g2["tgt"].view(-1, wl.V)
+        for r in range(wl.R):
+            for j in range(int(ell[r]) + 1):
+                assert torch.equal(rows[int(ro[r]) + j].cpu(), inp["tgt"][r, j])
+        assert torch.isnan(rows[int(ro[wl.R]):].float()).all()
     v = dev_round["verify"]
     assert torch.equal(host_out["out_tok"], v["out_tok"].cpu())
     assert torch.equal(host_out["accept_len"], v["accept_len"].cpu())

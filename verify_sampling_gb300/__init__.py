@@ -86,7 +86,7 @@ class RoundHostArgs(ctypes.Structure):
                 ("verify", ctypes.POINTER(VerifyArgs)), ("U_host", _P), ("h_host", _P),
                 ("x0_host", _P), ("tgt_host", _P), ("tgt_rows", ctypes.c_size_t),
                 ("out_tok_host", _P), ("accept_len_host", _P), ("n_out_host", _P),
-                ("stats_host", _P)]
+                ("stats_host", _P), ("tgt_scheduled_only", ctypes.c_int)]
 
 
 class SpecError(RuntimeError):
@@ -461,12 +461,19 @@ def run_round_host(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.
                    sps: torch.Tensor, b_lo: float, b_step: float, K: int, seed: int, *,
                    host_in: dict, host_out: dict, sched_mode: int = SCHED_EARLY_STOP,
                    sched_threshold: float = 0.0, target_temp: float = 1.0,
+                   tgt_scheduled_only: bool = False, K_dev: Optional[torch.Tensor] = None,
+                   n_free: Optional[torch.Tensor] = None,
                    bufs: Optional[dict] = None, stream=None) -> dict:
     """spec_round_host: one round whose per-round inputs come from host tensors
     ``host_in`` {"U", "h", "x0", "tgt"} (copied into draft_in.U / .h / .x0 and
     ``tgt``) and whose results go to host tensors ``host_out`` {"out_tok",
     "accept_len", "n_out", "stats"}; every key is optional.  Page-locked host
-    tensors keep the call asynchronous (synchronise before reading host_out)."""
+    tensors keep the call asynchronous (synchronise before reading host_out).
+    ``tgt_scheduled_only``: host_in["tgt"] is the padded [R, gamma + 1, V]
+    page-locked array and only the scheduled rows are read from it, into
+    ``tgt`` (room for R * (gamma + 1) rows) in the schedule's packed layout;
+    ``tgt_row_off`` is then ignored.  ``K_dev`` / ``n_free``: the scheduler's
+    asynchronous cap words, as for schedule()."""
     bufs = {} if bufs is None else bufs
     U = _dev(draft_in.U, "U")
     R, gamma, V = U.shape
@@ -480,8 +487,15 @@ def run_round_host(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.
         "row_off": torch.empty(R + 1, dtype=torch.int32, device=dev),
         "stats": torch.empty(4, dtype=torch.float64, device=dev)}
     sa = _sched_struct(d_outs["a"], _dev(sps, "sps"), b_lo, b_step, K, sched_mode,
-                       sched_threshold, s_outs, bufs.get("status"))
+                       sched_threshold, s_outs, bufs.get("status"), K_dev, n_free)
     tgt = _dev(tgt, "tgt")
+    if tgt_scheduled_only:
+        ht = host_in.get("tgt")
+        if ht is None or not ht.is_pinned() or ht.numel() != R * (gamma + 1) * V:
+            raise ValueError("tgt_scheduled_only needs a pinned host tgt of R*(gamma+1)*V entries")
+        if tgt.numel() < R * (gamma + 1) * V:
+            raise ValueError("tgt must hold R*(gamma+1) rows")
+        tgt_row_off = s_outs["row_off"]
     v_outs = bufs.get("verify") or {
         "accept_len": torch.empty(R, dtype=torch.int32, device=dev),
         "out_tok": torch.empty(R, gamma + 1, dtype=torch.int32, device=dev),
@@ -501,6 +515,7 @@ def run_round_host(draft_in: DraftInputs, tgt: torch.Tensor, tgt_row_off: torch.
     h.accept_len_host = _host(host_out.get("accept_len"), v_outs["accept_len"], "host accept_len")
     h.n_out_host = _host(host_out.get("n_out"), v_outs["n_out"], "host n_out")
     h.stats_host = _host(host_out.get("stats"), s_outs["stats"], "host stats")
+    h.tgt_scheduled_only = int(bool(tgt_scheduled_only))
     _check(lib().spec_round_host(ctypes.byref(h), seed & 0xFFFFFFFFFFFFFFFF, _stream_handle(stream)),
            "spec_round_host")
     del keep

@@ -5,6 +5,7 @@
 
 #include "draft.cuh"
 #include "draft_tc.cuh"
+#include "host_rows.cuh"
 #include "schedule.cuh"
 #include "accept_stats.cuh"
 #include "residual_tc.cuh"
@@ -421,6 +422,18 @@ int spec_round_host(const spec_round_host_args* args, uint64_t seed, spec_stream
   if (!valid_dtype(d.logit_dtype) || !valid_dtype(d.conf_dtype) || !valid_dtype(v.tgt_dtype) ||
       d.R < 1 || d.gamma < 1 || d.V < 1 || d.d < 0)
     return SPEC_ERR_INVALID_ARG;
+  const bool packed = args->tgt_scheduled_only != 0;
+  const void* tgt_dev_view = nullptr;  // the device's address of tgt_host (packed mode)
+  if (packed) {
+    if (!args->tgt_host || v.tgt_row_off != sc.row_off || !v.tgt) return SPEC_ERR_INVALID_ARG;
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, args->tgt_host) != cudaSuccess) {
+      cudaGetLastError();  // clear this (non-sticky) error so later launch checks do not see it
+      return SPEC_ERR_UNSUPPORTED;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return SPEC_ERR_UNSUPPORTED;
+    tgt_dev_view = attr.devicePointer;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   auto h2d = [&](const void* dst, const void* src, size_t bytes) {
     if (!src || bytes == 0) return true;
@@ -432,12 +445,23 @@ int spec_round_host(const spec_round_host_args* args, uint64_t seed, spec_stream
   if (!h2d(d.U, args->U_host, RG * d.V * dtype_size(d.logit_dtype)) ||
       !h2d(d.h, args->h_host, RG * d.d * dtype_size(d.conf_dtype)) ||
       !h2d(d.x0, args->x0_host, (size_t)d.R * sizeof(int32_t)) ||
-      !h2d(v.tgt, args->tgt_host, args->tgt_rows * d.V * dtype_size(v.tgt_dtype)))
+      (!packed && !h2d(v.tgt, args->tgt_host, args->tgt_rows * d.V * dtype_size(v.tgt_dtype))))
     return SPEC_ERR_CUDA;
   int rc = spec_draft_sample(args->draft, seed, stream);
   if (rc != SPEC_OK) return rc;
   rc = spec_schedule(args->sched, stream);
   if (rc != SPEC_OK) return rc;
+  if (packed) {
+    GatherRowsParams g{};
+    g.R = d.R;
+    g.G1 = d.gamma + 1;
+    g.row_bytes = (size_t)d.V * dtype_size(v.tgt_dtype);
+    g.src = static_cast<const unsigned char*>(tgt_dev_view);
+    g.dst = static_cast<unsigned char*>(const_cast<void*>(v.tgt));
+    g.row_off = sc.row_off;
+    g.status = v.status;
+    if (launch_gather_rows(g, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
   rc = spec_verify(args->verify, seed, stream);
   if (rc != SPEC_OK) return rc;
   auto d2h = [&](void* dst, const void* src, size_t bytes) {
