@@ -4,9 +4,9 @@
  * One speculative round for R concurrent requests and a draft block of gamma
  * positions over a vocabulary of V tokens, in three stages:
  *
- *   spec_draft_sample  semi-autoregressive Markov draft head, sampling,
- *                      confidence head with sequential temperature scaling and
- *                      survival products
+ *   spec_draft_sample  semi-autoregressive draft head (Markov, or RNN with a
+ *                      recurrent state), sampling, confidence head with
+ *                      sequential temperature scaling and survival products
  *   spec_schedule      hardware-aware prefix scheduler (sorted survivals,
  *                      greedy admission while tau * SPS(B) rises, top-K cap)
  *   spec_verify        lossless rejection-sampling verification (residual
