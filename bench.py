@@ -2,8 +2,9 @@
 
 A step is one full round over one batch: draft (gamma sampling steps of the
 Markov head, or of the RNN head with --head rnn, + confidence head), prefix
-schedule, verification (rejection sampling, residual, bonus).  Default workload: R=512 requests, gamma=11, V=129280, r=128,
-fp32 logits, bf16 factors, top-K cap 2048 (the largest configuration).
+schedule, verification (rejection sampling, residual, bonus).  Default
+workload: R=512 requests, gamma=11, V=129280, r=128, fp32 logits, bf16
+factors, top-K cap 2048 (the largest configuration).
 Inputs are synthetic and seeded (synth/), resident in HBM, larger than L2.
 
 Metric: draft+verified positions per second = (R * gamma + B) / step time,
