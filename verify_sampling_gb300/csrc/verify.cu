@@ -835,7 +835,7 @@ VerifyScratch verify_scratch_carve(void* base, int R, int gamma, int V, size_t* 
   s.fallback = reinterpret_cast<int*>(b + off[kFallback]);
   s.unit_cnt = reinterpret_cast<unsigned long long*>(b + off[kUnitCnt]);
   *counters_offset = off[kUnitCnt];
-  *counters_bytes = total - off[kRowCnt];
+  *counters_bytes = total - off[kUnitCnt];  // the counter block, to the end
   return s;
 }
 
