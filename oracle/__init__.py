@@ -14,6 +14,9 @@ Each wrapper cites the passage of the pages it follows (see ``oracle.cpp``):
   * schedule, threshold mode -- DSpark summary, comparison table (SpecDec++) and Figure 5
   * accept_stats -- LightSpec article, "无需额外训练，基于运行时统计的动态调度"
   * cstar, calibration -- DSpark summary, "2.1 置信度头" and Figure 6
+  * draft_rnn  -- DSpark summary, "第二阶段：轻量顺序头" (the RNN head; no formula is
+                  given there: s_k = store(tanh(A_k[x_{k-1}] + s_{k-1} W_k)) is this
+                  library's reading, pinned by its reduction to the Markov head)
 """
 from __future__ import annotations
 

@@ -16,7 +16,9 @@
 //
 // Parity status: Philox, softmax, Gumbel-max sampling, the scheduler and the
 // verifier are pinned by the tests under tests/ (curand host generator,
-// closed forms, chi-square, brute force, hand-built fixtures).
+// closed forms, chi-square, brute force, hand-built fixtures).  The RNN head
+// follows a reading of its own (the pages give no formula); it is pinned by a
+// hand-computed case, its reduction to the Markov head and losslessness.
 
 #include <algorithm>
 #include <cmath>
