@@ -200,6 +200,23 @@ def test_host_side_rejections_launch_nothing(spec):
     rh = spec.RoundHostArgs()
     rh.draft, rh.sched, rh.verify = ctypes.pointer(da), ctypes.pointer(sa), ctypes.pointer(va)
     assert lib.spec_round_host(ctypes.byref(rh), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    # the scheduled-rows mode: a verify that does not read the schedule's row
+    # offsets is refused, and so is host memory the device cannot address
+    # (checked before anything is copied or launched)
+    sa.a = da.a
+    va.ell = sa.ell = ctypes.c_void_p(1024)
+    va.x, va.q_tok, va.lse_q = (ctypes.c_void_p(2048), ctypes.c_void_p(3072), ctypes.c_void_p(4096))
+    da.x, da.q_tok, da.lse_q = va.x, va.q_tok, va.lse_q
+    da.U = da.A = da.Ct = da.x0 = ctypes.c_void_p(8192)
+    va.draft = ctypes.pointer(da)
+    va.tgt = ctypes.c_void_p(16384)
+    da.logit_dtype = da.conf_dtype = va.tgt_dtype = spec.SPEC_F32
+    host_tgt = (ctypes.c_float * 16)()
+    rh.tgt_host, rh.tgt_scheduled_only = ctypes.cast(host_tgt, ctypes.c_void_p), 1
+    sa.row_off, va.tgt_row_off = ctypes.c_void_p(5120), ctypes.c_void_p(6144)
+    assert lib.spec_round_host(ctypes.byref(rh), 0, None) == spec.SPEC_ERR_INVALID_ARG
+    va.tgt_row_off = sa.row_off
+    assert lib.spec_round_host(ctypes.byref(rh), 0, None) == spec.SPEC_ERR_UNSUPPORTED
     v = spec.VerifyArgs()
     v.mode, v.R, v.gamma, v.V = 0, 2, 2, 10
     v.tgt = v.tgt_row_off = v.ell = v.x = v.accept_len = v.out_tok = v.n_out = ctypes.c_void_p(256)
