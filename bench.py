@@ -110,10 +110,10 @@ def _peaks():
 class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_bench_", suffix=".csv")
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_QUERY}", "--format=csv",
                  "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -132,6 +132,10 @@ class ClockSampler:
         sm, mx, reasons = [], [], set()
         with open(self.path) as f:
             lines = f.read().strip().splitlines()[1:]
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         for ln in lines:
             c = [x.strip() for x in ln.split(",")]
             if len(c) < 9:

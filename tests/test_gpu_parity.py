@@ -283,7 +283,7 @@ def _gpu_round(U, A, Ct, x0, tgt_rows_fn, ell, seed, rid_base):
 
 
 def test_gpu_lossless_gamma2_pairs_chisquare():
-    """north_star check (a) through the CUDA path: 10^6 rounds, V = 6, gamma = 2;
+    """The lossless property through the CUDA path: 10^6 rounds, V = 6, gamma = 2;
     the first two emitted tokens follow p1(a) p2(b|a)."""
     from scipy import stats
     from scipy.special import softmax

@@ -101,7 +101,7 @@ def test_confidence_closed_forms():
 
 
 def test_survival_non_increasing():
-    """The benchmark spec check (c): a_{r,j} is non-increasing along j."""
+    """Survival check: a_{r,j} = prod_{i<=j} c_{r,i} is non-increasing along j."""
     rng = np.random.default_rng(2)
     R, gamma, d, e, V = 8, 16, 32, 8, 50
     h = rng.normal(size=(R, gamma, d))

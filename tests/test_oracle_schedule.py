@@ -1,7 +1,7 @@
 """Pins for the oracle's prefix scheduler (CPU only).
 
 * a hand-computed walk-through of the history article's "杀招三" (golden fixture);
-* brute force over every l-vector (the benchmark spec check (d)): because a_{r,j} is
+* brute force over every l-vector: because a_{r,j} is
   non-increasing in j, the best admitted set of any size n is the top-n of the
   sorted list, so the global search must equal the brute-force optimum, and the
   early-stop result can only be lower (its ratio is reported);
@@ -98,7 +98,7 @@ def test_early_stop_equals_global_when_theta_unimodal():
 
 
 def test_admission_is_prefix_closed_and_sorted():
-    """The benchmark spec check (c): the admitted set is a prefix per request."""
+    """Prefix closure: the admitted set is a prefix of each request."""
     rng = np.random.default_rng(5)
     for _ in range(20):
         R, gamma = int(rng.integers(1, 9)), int(rng.integers(1, 17))

@@ -1,6 +1,6 @@
 """Pins for the oracle's verifier (CPU only).
 
-* the benchmark spec check (a), the lossless property of the history article's
+* the lossless property of the history article's
   "数学上的美感": over 10^6 seeded rounds on a tiny vocabulary the emitted first
   token (gamma = 1) and the first two tokens (gamma = 2, completed by a second
   round when the first round emits one token) follow the target p, by
@@ -8,7 +8,7 @@
   closed form the DSpark summary ("2.1") gives as 1 - TV;
 * the lossy reading (regenerate from p instead of the residual) must fail the
   same chi-square -- the test has the power to see the difference;
-* the benchmark spec check (b): greedy accept length = longest prefix with
+* greedy: accept length = longest prefix with
   x_j == argmax L_j (numpy argmax, lowest index on ties), brute force;
 * DSpark Figure 1 as a scripted round (golden fixture).
 """
@@ -157,7 +157,7 @@ def test_target_temperature():
 
 
 def test_greedy_brute_force():
-    """The benchmark spec check (b)."""
+    """Greedy accept length: the longest prefix with x_j == argmax L_j."""
     rng = np.random.default_rng(15)
     R, gamma, V = 300, 6, 40
     # bf16-like coarse values so that exact ties occur
