@@ -498,7 +498,7 @@ def main():
 
     # ----------------------------------------------------- e2e (rank 0) ----
     if rank == 0 and not args.no_e2e and not greedy:
-        line["e2e"] = _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 5),
+        line["e2e"] = _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 8),
                            cap_words=cap_words)
     if rank == 0 and not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl)
@@ -517,47 +517,75 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None)
     resident.  U, h and x0 are copied whole.  Of the target logits, held on the
     host for every candidate row [R, gamma + 1, V], only the B rows the
     schedule admits are read -- the rows a target model computes for the
-    round -- by the library's gather from the mapped host buffer."""
+    round -- by the library's gather from the mapped host buffer.
+
+    Two rounds are in flight, on two streams with their own device buffers:
+    while one round computes, the next one's inputs cross the link.  Step i's
+    results are read on the host before step i + 2 reuses its buffers."""
     names = ["U", "h", "x0", "tgt"]
     host = {n: g[n].cpu().pin_memory() for n in names}
-    devb = {n: torch.empty_like(g[n]) for n in names}
-    outs = {"out_tok": torch.empty(wl.R, wl.gamma + 1, dtype=torch.int32).pin_memory(),
-            "accept_len": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
-            "n_out": torch.empty(wl.R, dtype=torch.int32).pin_memory(),
-            "stats": torch.empty(4, dtype=torch.float64).pin_memory()}
     whole = sum(host[n].numel() * host[n].element_size() for n in ("U", "h", "x0"))
     row_bytes = wl.V * host["tgt"].element_size()
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
-    d_in = vs.DraftInputs(U=devb["U"], A=g["A"], Ct=g["Ct"], x0=devb["x0"],
-                          draft_temp=g["draft_temp"], h=devb["h"], W1=g["W1"], w=g["w"],
-                          sts_temp=g["sts_temp"], request_id_base=rid_base,
-                          Wrnn=din.Wrnn, S=din.S)
+    R, G, V = wl.R, wl.gamma, wl.V
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    sets = []
+    for _ in range(2):
+        devb = {n: torch.empty_like(g[n]) for n in names}
+        outs = {"out_tok": torch.empty(R, G + 1, dtype=torch.int32).pin_memory(),
+                "accept_len": torch.empty(R, dtype=torch.int32).pin_memory(),
+                "n_out": torch.empty(R, dtype=torch.int32).pin_memory(),
+                "stats": torch.empty(4, dtype=torch.float64).pin_memory()}
+        d_in = vs.DraftInputs(U=devb["U"], A=g["A"], Ct=g["Ct"], x0=devb["x0"],
+                              draft_temp=g["draft_temp"], h=devb["h"], W1=g["W1"], w=g["w"],
+                              sts_temp=g["sts_temp"], request_id_base=rid_base, Wrnn=din.Wrnn,
+                              S=None if din.S is None else torch.empty_like(din.S))
+        b = {"draft": vs.draft_outputs(R, G, V, dev),
+             "ws_draft": torch.empty_like(bufs["ws_draft"]),
+             "ws_verify": torch.empty_like(bufs["ws_verify"]),
+             "sched": {"ell": torch.empty(R, dtype=torch.int32, device=dev),
+                       "row_off": torch.empty(R + 1, dtype=torch.int32, device=dev),
+                       "stats": torch.empty(4, dtype=torch.float64, device=dev)},
+             "verify": {"accept_len": torch.empty(R, dtype=torch.int32, device=dev),
+                        "out_tok": torch.empty(R, G + 1, dtype=torch.int32, device=dev),
+                        "n_out": torch.empty(R, dtype=torch.int32, device=dev)}}
+        sets.append((devb, outs, d_in, b))
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][1].values())
+    torch.cuda.synchronize()
 
-    host_out = {k: outs[k] for k in ("out_tok", "accept_len", "n_out", "stats")}
-
-    def one(i):
-        # one C-ABI call: host inputs in, host results out
-        vs.run_round_host(d_in, devb["tgt"].view(-1, wl.V), g["tgt_row_off"], g["sps"], g["b_lo"],
-                          g["b_step"], wl.K, 9000 + i, host_in=host, host_out=host_out,
+    def issue(i):
+        # one C-ABI call: host inputs in, host results out (asynchronous)
+        devb, outs, d_in, b = sets[i % 2]
+        vs.run_round_host(d_in, devb["tgt"].view(-1, V), g["tgt_row_off"], g["sps"], g["b_lo"],
+                          g["b_step"], wl.K, 9000 + i, host_in=host, host_out=outs,
                           sched_mode=wl.sched_mode, sched_threshold=wl.sched_threshold,
                           tgt_scheduled_only=True,
                           K_dev=None if cap_words is None else cap_words[i % 2: i % 2 + 1],
                           n_free=None if cap_words is None else cap_words[i % 2: i % 2 + 1],
-                          bufs={"draft": bufs["draft"], "ws_draft": bufs["ws_draft"],
-                                "ws_verify": bufs["ws_verify"]})
-        torch.cuda.synchronize()
-        B = float(outs["stats"][1])
-        return wl.R * wl.gamma + B, B
+                          bufs=b, stream=streams[i % 2])
 
-    one(-1)
+    def collect(i):
+        streams[i % 2].synchronize()
+        B = float(sets[i % 2][1]["stats"][1])
+        return R * G + B, B
+
+    issue(0)
+    issue(1)
+    collect(0)
+    collect(1)  # warm-up
     t0 = time.perf_counter()
-    res = [one(i) for i in range(steps)]
+    res = []
+    for i in range(steps):
+        if i >= 2:
+            res.append(collect(i - 2))
+        issue(i)
+    for i in range(max(0, steps - 2), steps):
+        res.append(collect(i))
     sec = time.perf_counter() - t0
     pos = sum(p for p, _ in res)
     B_mean = sum(b for _, b in res) / steps
     return {"value": pos / sec, "unit": "positions/s",
             "h2d_bytes_per_step": int(whole + B_mean * row_bytes),
-            "d2h_bytes_per_step": d2h, "steps": steps,
+            "d2h_bytes_per_step": d2h, "steps": steps, "rounds_in_flight": 2,
             "target_rows": "the B scheduled rows of each step (mean %.1f), read from the "
                            "pinned [R, gamma+1, V] host array" % B_mean}
 
