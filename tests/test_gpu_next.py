@@ -283,3 +283,21 @@ def test_async_cap_chain(mode):
         free_seen.append(int(word.item()))
         bound += int(int(to_np(s["stats"])[0]) < min(K, of.n))
     assert bound >= 1  # the lagged cap took effect at least once
+
+
+@pytest.mark.parametrize("R,gamma", [(512, 11), (128, 64), (3, 7), (1, 40)])
+def test_schedule_unordered_survivals(R, gamma):
+    """Survivals that rise along j (not products of confidences): the sort
+    orders every run itself before merging.  Order, l_r and stats equal the
+    oracle's in all three modes."""
+    rng = np.random.default_rng(R + gamma)
+    a_np = rng.uniform(0.0, 1.0, (R, gamma)).astype(np.float32)
+    a_np[rng.random((R, gamma)) < 0.05] = np.float32(0.5)  # ties across requests
+    a = torch.tensor(a_np, device=DEV)
+    inp = {"sps": _sps(R, gamma).to(DEV), "b_lo": 1.0, "b_step": 1.0}
+    for mode in (oracle.SCHED_EARLY_STOP, oracle.SCHED_GLOBAL, oracle.SCHED_THRESHOLD):
+        K = max(1, (R * gamma) // 2)
+        s = vs.schedule(a, inp["sps"], 1.0, 1.0, K, mode, threshold=0.4, want_order=True)
+        torch.cuda.synchronize()
+        rep = compare_schedule(inp, a, s, K, mode, threshold=0.4)
+        assert rep.checked + rep.near_ties == 1
