@@ -123,3 +123,24 @@ def test_rnn_full_size_c5_sampled():
     order = np.argsort(-ell, kind="stable")
     reqs = sorted({0, 1, 255, wl.R - 1, int(order[0]), int(order[1])})
     _check(g, wl, W, seed, S, d, s, v, reqs)
+
+
+def test_rnn_request_sharding_is_invariant():
+    """The state is per request and the stream is keyed by the global request
+    id: drafting the last requests alone, with request_id_base = their first
+    global id, gives the same tokens and states (one and two request tiles)."""
+    wl = CASES["tc_c3_small_R130"]
+    g = {k: (t.to(DEV) if isinstance(t, torch.Tensor) else t)
+         for k, t in synth.make_inputs(wl, "cpu").items()}
+    W = synth.rnn_weights(wl, DEV)
+    S_all, d_all, _, _ = _round(g, wl, W, 5, want_P=False)
+    lo = 70
+    half = {k: (v[lo:] if isinstance(v, torch.Tensor) and k in ("U", "x0", "h") else v)
+            for k, v in g.items()}
+    din = synth.draft_inputs(half, request_id_base=lo)
+    din.Wrnn = W
+    din.S = torch.zeros(wl.R - lo, wl.gamma, wl.r, dtype=wl.fac_dtype, device=DEV)
+    d_half = vs.draft_sample(din, 5)
+    torch.cuda.synchronize()
+    assert torch.equal(d_half["x"], d_all["x"][lo:])
+    assert torch.equal(din.S, S_all[lo:])
