@@ -475,7 +475,10 @@ def main():
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": traffic,
-                "algorithmic_bytes_per_launch": per_launch}
+                "algorithmic_bytes_per_launch": per_launch,
+                # DRAM bytes the profiler counted per launch over the same
+                # event-timed duration (null with traffic)
+                "achieved_dram": None if traffic is None else round(traffic / (dur_ms / 1000.0) / 1e9, 1)}
 
     line = {"metric": "draft+verified positions/s", "value": value, "unit": "positions/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
