@@ -112,13 +112,15 @@ class ClockSampler:
         self.proc = None
         import tempfile
         fd, self.path = tempfile.mkstemp(prefix="clocks_bench_", suffix=".csv")
+        self.f = os.fdopen(fd, "w")
         try:
-            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_QUERY}", "--format=csv",
                  "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            self.f.close()
+            os.remove(self.path)
 
     def stop(self):
         if self.proc is None:
