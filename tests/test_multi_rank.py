@@ -43,15 +43,21 @@ def _init(rank: int, port: int):
     dist.init_process_group("gloo", rank=rank, world_size=WORLD)
 
 
-def _round(inp, wl, lo, hi, rid_base, seed, a_all=None):
+def _round(inp, wl, lo, hi, rid_base, seed, a_all=None, W=None):
     """Oracle draft + confidence on requests [lo, hi); schedule over a_all (or
-    the shard's own survivals); verify the shard."""
+    the shard's own survivals); verify the shard.  W: the RNN head's
+    recurrence (None: the Markov head)."""
     f = lambda t: t.float().numpy()
     U = f(inp["U"][lo:hi])
     A, Ct = f(inp["A"]), f(inp["Ct"])
     x0 = inp["x0"][lo:hi].numpy()
     temps = inp["draft_temp"].numpy()
-    d = oracle.draft(U, A, Ct, x0, temps, seed, rid_base=rid_base)
+    S = None
+    if W is None:
+        d = oracle.draft(U, A, Ct, x0, temps, seed, rid_base=rid_base)
+    else:
+        d = oracle.draft_rnn(U, A, Ct, W, x0, temps, seed, rid_base=rid_base, bf16_state=False)
+        S = d.S
     _, a = oracle.confidence(f(inp["h"][lo:hi]), f(inp["W1"]), f(inp["w"]), x0, d.x,
                              inp["sts_temp"].numpy())
     s = oracle.schedule(a if a_all is None else a_all, inp["sps"].numpy(), inp["b_lo"],
@@ -60,7 +66,7 @@ def _round(inp, wl, lo, hi, rid_base, seed, a_all=None):
     ell = s.ell[lo:hi] if a_all is not None else s.ell
     rows = f(inp["tgt"][lo:hi]).reshape(-1, V)
     v = oracle.verify(oracle.MODE_SAMPLE, rows, (np.arange(hi - lo) * (G + 1)).astype(np.int32),
-                      ell, d.x, d.q_tok, 1.0, U, A, Ct, x0, temps, seed, rid_base=rid_base)
+                      ell, d.x, d.q_tok, 1.0, U, A, Ct, x0, temps, seed, rid_base=rid_base, S=S)
     return d, a, s, v
 
 
@@ -73,21 +79,27 @@ def _worker_combine(rank, port, q):
         dist.destroy_process_group()
 
 
-def _worker_shard(rank, port, q):
+def _shard_inputs(rnn: bool):
+    wl = synth.WORKLOADS["tiny"].scaled(R=6, V=300)
+    inp = synth.make_inputs(wl, "cpu")
+    W = synth.rnn_weights(wl, "cpu").numpy() if rnn else None
+    return wl, inp, W
+
+
+def _worker_shard(rank, port, q, rnn=False):
     _init(rank, port)
     try:
-        wl = synth.WORKLOADS["tiny"].scaled(R=6, V=300)
-        inp = synth.make_inputs(wl, "cpu")
+        wl, inp, W = _shard_inputs(rnn)
         per = wl.R // WORLD
         lo, hi = rank * per, (rank + 1) * per
         seed = 77
         # stage 1: draft + confidence on the shard, all-gather the survivals
-        d, a, _, _ = _round(inp, wl, lo, hi, lo, seed)
+        d, a, _, _ = _round(inp, wl, lo, hi, lo, seed, W=W)
         parts = [torch.zeros(per, wl.gamma, dtype=torch.float64) for _ in range(WORLD)]
         dist.all_gather(parts, torch.from_numpy(np.ascontiguousarray(a)))
         a_all = torch.cat(parts).numpy()
         # stage 2: identical schedule on every rank, verify the shard
-        _, _, s, v = _round(inp, wl, lo, hi, lo, seed, a_all=a_all)
+        _, _, s, v = _round(inp, wl, lo, hi, lo, seed, a_all=a_all, W=W)
         got = {k: torch.from_numpy(np.ascontiguousarray(t)) for k, t in
                (("x", d.x), ("acc", v.accept_len), ("out", v.out_tok), ("n", v.n_out))}
         gathered = {}
@@ -98,6 +110,10 @@ def _worker_shard(rank, port, q):
         q.put((rank, gathered, s.ell.copy(), s.B))
     finally:
         dist.destroy_process_group()
+
+
+def _worker_shard_rnn(rank, port, q):
+    _worker_shard(rank, port, q, rnn=True)
 
 
 def _spawn(fn):
@@ -131,11 +147,13 @@ def test_combine_over_ranks_gloo():
     assert bench.combine_over_ranks(3.0, 100.0, "cpu", 1) == (3.0, 100.0)
 
 
-def test_request_sharded_round_equals_whole_batch_gloo():
-    out = _spawn(_worker_shard)
-    wl = synth.WORKLOADS["tiny"].scaled(R=6, V=300)
-    inp = synth.make_inputs(wl, "cpu")
-    d, _, s, v = _round(inp, wl, 0, wl.R, 0, 77)
+@pytest.mark.parametrize("rnn", [False, True])
+def test_request_sharded_round_equals_whole_batch_gloo(rnn):
+    """Markov head, and the RNN head (its state is per request, so the shards
+    carry no state of one another)."""
+    out = _spawn(_worker_shard_rnn if rnn else _worker_shard)
+    wl, inp, W = _shard_inputs(rnn)
+    d, _, s, v = _round(inp, wl, 0, wl.R, 0, 77, W=W)
     for _, g, ell, B in out:
         np.testing.assert_array_equal(g["x"], d.x)
         np.testing.assert_array_equal(ell, s.ell)
