@@ -12,7 +12,8 @@
 // CTA takes kRnnRows requests, one warp each for the per-request part: on the
 // fused tensor-core path the warp first merges the split partials of position
 // k-1 (that path's draft grid leaves them unmerged) and writes x, q_tok and
-// lse_q there; then it stages s_{k-1} in shared memory.  The r x r product
+// lse_q there; it stages s_{k-1} (loaded before the merge) and the row
+// A_k[x_{k-1}] in shared memory.  The r x r product
 // runs with one thread per output column j for all the CTA's requests, so each
 // W_k[i][j] is loaded once per CTA (coalesced over j) and used kRnnRows times.
 #include "draft.cuh"
@@ -38,7 +39,7 @@ __device__ __forceinline__ void store_state(__nv_bfloat16* p, float v) { *p = __
 template <typename TF, bool kStaged>
 __global__ void __launch_bounds__(kRnnThreads) rnn_state_kernel(RnnStateParams p) {
   __shared__ float s_prev[kRnnRows][kMaxRank];
-  __shared__ int s_xp[kRnnRows];
+  __shared__ float s_arow[kRnnRows][kMaxRank];  // A_k[x_{k-1}] of each request
   extern __shared__ uint4 s_w[];  // kStaged: W_k [rank, rank]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * kRnnRows, k = p.k, rank = p.rank, G = p.gamma, V = p.V;
@@ -56,6 +57,14 @@ __global__ void __launch_bounds__(kRnnThreads) rnn_state_kernel(RnnStateParams p
   tc::grid_dep_wait();
   tc::grid_dep_launch();
   if (m < p.R) {
+    // s_{k-1} is loaded before the merge, so the two round trips overlap
+    constexpr int kPerLane = kMaxRank / 32;
+    float sv[kPerLane];
+    if (k > 1) {
+      const TF* prev = S + ((size_t)m * G + (k - 2)) * rank;
+#pragma unroll
+      for (int q = 0; q < kPerLane; ++q) sv[q] = lane + 32 * q < rank ? ld_f(prev, (size_t)(lane + 32 * q)) : 0.f;
+    }
     int xp;
     if (k == 1) {
       xp = p.x0[m];
@@ -77,21 +86,22 @@ __global__ void __launch_bounds__(kRnnThreads) rnn_state_kernel(RnnStateParams p
       if (lane == 0) set_status(p.status, SPEC_STATUS_BAD_TOKEN);
       xp = 0;
     }
-    if (lane == 0) s_xp[warp] = xp;
+    const TF* arow = reinterpret_cast<const TF*>(p.A) + ((size_t)(k - 1) * V + xp) * rank;
+    for (int i = lane; i < rank; i += 32) s_arow[warp][i] = ld_f(arow, (size_t)i);
     if (k > 1) {
-      const TF* prev = S + ((size_t)m * G + (k - 2)) * rank;
-      for (int i = lane; i < rank; i += 32) s_prev[warp][i] = ld_f(prev, (size_t)i);
+#pragma unroll
+      for (int q = 0; q < kPerLane; ++q)
+        if (lane + 32 * q < rank) s_prev[warp][lane + 32 * q] = sv[q];
     }
   }
   __syncthreads();
   const int nrows = min(kRnnRows, p.R - r0);
-  const TF* Ak = reinterpret_cast<const TF*>(p.A) + (size_t)(k - 1) * V * rank;
   const TF* sW = reinterpret_cast<const TF*>(s_w);
   TF* out = reinterpret_cast<TF*>(p.S);
   for (int j = threadIdx.x; j < rank; j += kRnnThreads) {
     float acc[kRnnRows];
 #pragma unroll
-    for (int w = 0; w < kRnnRows; ++w) acc[w] = w < nrows ? ld_f(Ak, (size_t)s_xp[w] * rank + j) : 0.f;
+    for (int w = 0; w < kRnnRows; ++w) acc[w] = w < nrows ? s_arow[w][j] : 0.f;
     if (kStaged && k > 1) {  // s_0 = 0: the product vanishes at k = 1
       for (int i = 0; i < rank; ++i) {
         const float wij = ld_f(sW, (size_t)i * rank + j);
