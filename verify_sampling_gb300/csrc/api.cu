@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include "draft.cuh"
+#include "draft_run.cuh"
 #include "draft_tc.cuh"
 #include "host_rows.cuh"
 #include "schedule.cuh"
@@ -35,6 +36,30 @@ size_t draft_scratch_bytes(int R, int gamma, int V) {
   return draft_partials_bytes(R, V) + align256((size_t)R * (1 + gamma) * sizeof(unsigned));
 }
 
+bool draft_sizes_ok(int R, int gamma, int V, int r) {
+  return R >= 1 && R <= kMaxGridY && gamma >= 1 && gamma <= kMaxGamma && V >= 1 &&
+         V < (1 << 30) && r >= 1 && r <= kMaxRank &&
+         (double)R * gamma * V < 1099511627776.0;  // 2^40
+}
+
+bool verify_sizes_ok(int R, int gamma, int V) {
+  return R >= 1 && R <= kMaxGridY && gamma >= 1 && gamma + 1 <= kMaxGridY && V >= 1 &&
+         V < (1 << 30) && (double)R * (gamma + 1) * V < 1099511627776.0;
+}
+
+int check_workspace(void* ws, size_t have, size_t need) {
+  if (need == 0) return SPEC_OK;
+  if (!ws || have < need) return SPEC_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return SPEC_ERR_ALIGNMENT;
+  return SPEC_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------- shared by the two draft
+// entry points (spec_draft_sample and spec_draft_sample_static)
+namespace spec {
+
 // The fused tensor-core path needs bf16 factors with r a multiple of 64, 16-byte
 // aligned rows of U (V * element size a multiple of 16) and an sm_100-family GPU.
 bool draft_tc_ok(const spec_draft_args& a, int* sms) {
@@ -48,17 +73,6 @@ bool draft_tc_ok(const spec_draft_args& a, int* sms) {
       cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return false;
   return major == 10 && *sms >= 1 && *sms <= kMaxDeviceSms;
-}
-
-bool draft_sizes_ok(int R, int gamma, int V, int r) {
-  return R >= 1 && R <= kMaxGridY && gamma >= 1 && gamma <= kMaxGamma && V >= 1 &&
-         V < (1 << 30) && r >= 1 && r <= kMaxRank &&
-         (double)R * gamma * V < 1099511627776.0;  // 2^40
-}
-
-bool verify_sizes_ok(int R, int gamma, int V) {
-  return R >= 1 && R <= kMaxGridY && gamma >= 1 && gamma + 1 <= kMaxGridY && V >= 1 &&
-         V < (1 << 30) && (double)R * (gamma + 1) * V < 1099511627776.0;
 }
 
 int check_draft_args(const spec_draft_args* a) {
@@ -87,14 +101,85 @@ int check_draft_args(const spec_draft_args* a) {
   return SPEC_OK;
 }
 
-int check_workspace(void* ws, size_t have, size_t need) {
-  if (need == 0) return SPEC_OK;
-  if (!ws || have < need) return SPEC_ERR_WORKSPACE;
-  if (!aligned(ws, 256)) return SPEC_ERR_ALIGNMENT;
-  return SPEC_OK;
+int run_draft(const spec_draft_args& a, uint64_t seed, Partial* partials, unsigned* counters,
+              int tc_sms, cudaStream_t s) {
+  DraftStepParams p{};
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.V = a.V;
+  p.rank = a.r;
+  p.nsplit = draft_nsplit(a.R, a.V);
+  p.rid_base = a.request_id_base;
+  p.key = philox_key(seed);
+  p.U = a.U;
+  p.A = a.A;
+  p.Ct = a.Ct;
+  if (a.head == SPEC_HEAD_RNN) {
+    p.W = a.Wrnn;
+    p.S = a.S;
+  }
+  p.x0 = a.x0;
+  p.draft_temp = a.draft_temp;
+  p.x = a.x;
+  p.q_tok = a.q_tok;
+  p.lse_q = a.lse_q;
+  p.P_out = a.P_out;
+  p.partials = partials;
+  p.counters = counters;
+  p.status = a.status;
+  // counters [R] and the fused kernel's shared race bounds [gamma, R], zeroed together
+  if (cudaMemsetAsync(p.counters, 0, (size_t)a.R * (1 + a.gamma) * sizeof(unsigned), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (tc_sms > 0) {
+    DraftTCParams t{};
+    t.R = a.R;
+    t.gamma = a.gamma;
+    t.V = a.V;
+    t.rank = a.r;
+    t.mtiles = (a.R + 127) / 128;
+    t.ntiles = (a.V + 63) / 64;
+    t.nsplit = draft_tc_nsplit(a.R, a.V, tc_sms);
+    t.rid_base = a.request_id_base;
+    t.key = p.key;
+    t.x0 = a.x0;
+    t.draft_temp = a.draft_temp;
+    t.A = a.A;
+    t.W = p.W;
+    t.S = p.S;
+    t.x = a.x;
+    t.q_tok = a.q_tok;
+    t.lse_q = a.lse_q;
+    t.partials = p.partials;
+    t.counters = p.counters;
+    t.row_best = p.counters + a.R;
+    t.status = a.status;
+    if (launch_draft_tc(t, a.logit_dtype, a.U, a.Ct, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (a.P_out && launch_draft_steps(p, a.logit_dtype, a.fac_dtype, true, s, /*probs_only=*/true) !=
+                       cudaSuccess)
+      return SPEC_ERR_CUDA;
+  } else if (launch_draft_steps(p, a.logit_dtype, a.fac_dtype, a.P_out != nullptr, s) !=
+             cudaSuccess) {
+    return SPEC_ERR_CUDA;
+  }
+  ConfParams c{};
+  c.R = a.R;
+  c.gamma = a.gamma;
+  c.V = a.V;
+  c.d = a.d;
+  c.e = a.e;
+  c.x0 = a.x0;
+  c.x = a.x;
+  c.h = a.h;
+  c.W1 = a.W1;
+  c.w = a.w;
+  c.sts_temp = a.sts_temp;
+  c.c = a.c;
+  c.a = a.a;
+  c.status = a.status;
+  return launch_confidence(c, a.conf_dtype, s) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-}  // namespace
+}  // namespace spec
 
 extern "C" {
 
@@ -132,88 +217,13 @@ int spec_draft_sample(const spec_draft_args* args, uint64_t seed, spec_stream_t 
   const size_t need = draft_scratch_bytes(a.R, a.gamma, a.V);
   rc = check_workspace(a.workspace, a.workspace_bytes, need);
   if (rc != SPEC_OK) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-  const int nsplit = draft_nsplit(a.R, a.V);
   char* ws = static_cast<char*>(a.workspace);
-  DraftStepParams p{};
-  p.R = a.R;
-  p.gamma = a.gamma;
-  p.V = a.V;
-  p.rank = a.r;
-  p.nsplit = nsplit;
-  p.rid_base = a.request_id_base;
-  p.key = philox_key(seed);
-  p.U = a.U;
-  p.A = a.A;
-  p.Ct = a.Ct;
-  if (a.head == SPEC_HEAD_RNN) {
-    p.W = a.Wrnn;
-    p.S = a.S;
-  }
-  p.x0 = a.x0;
-  p.draft_temp = a.draft_temp;
-  p.x = a.x;
-  p.q_tok = a.q_tok;
-  p.lse_q = a.lse_q;
-  p.P_out = a.P_out;
-  p.partials = reinterpret_cast<Partial*>(ws);
-  const size_t cnt_off = draft_partials_bytes(a.R, a.V);  // counters follow the partials
-  p.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
-  p.status = a.status;
-  // counters [R] and the fused kernel's shared race bounds [gamma, R], zeroed together
-  if (cudaMemsetAsync(p.counters, 0, (size_t)a.R * (1 + a.gamma) * sizeof(unsigned), s) != cudaSuccess)
-    return SPEC_ERR_CUDA;
   int sms = 0;
-  if (draft_tc_ok(a, &sms)) {
-    DraftTCParams t{};
-    t.R = a.R;
-    t.gamma = a.gamma;
-    t.V = a.V;
-    t.rank = a.r;
-    t.mtiles = (a.R + 127) / 128;
-    t.ntiles = (a.V + 63) / 64;
-    t.nsplit = draft_tc_nsplit(a.R, a.V, sms);
-    t.rid_base = a.request_id_base;
-    t.key = p.key;
-    t.x0 = a.x0;
-    t.draft_temp = a.draft_temp;
-    t.A = a.A;
-    t.W = p.W;
-    t.S = p.S;
-    t.x = a.x;
-    t.q_tok = a.q_tok;
-    t.lse_q = a.lse_q;
-    t.partials = p.partials;
-    t.counters = p.counters;
-    t.row_best = p.counters + a.R;
-    t.status = a.status;
-    if (launch_draft_tc(t, a.logit_dtype, a.U, a.Ct, s) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (a.P_out && launch_draft_steps(p, a.logit_dtype, a.fac_dtype, true, s, /*probs_only=*/true) !=
-                       cudaSuccess)
-      return SPEC_ERR_CUDA;
-  } else if (launch_draft_steps(p, a.logit_dtype, a.fac_dtype, a.P_out != nullptr, s) !=
-             cudaSuccess) {
-    return SPEC_ERR_CUDA;
-  }
-
-  ConfParams c{};
-  c.R = a.R;
-  c.gamma = a.gamma;
-  c.V = a.V;
-  c.d = a.d;
-  c.e = a.e;
-  c.x0 = a.x0;
-  c.x = a.x;
-  c.h = a.h;
-  c.W1 = a.W1;
-  c.w = a.w;
-  c.sts_temp = a.sts_temp;
-  c.c = a.c;
-  c.a = a.a;
-  c.status = a.status;
-  if (launch_confidence(c, a.conf_dtype, s) != cudaSuccess) return SPEC_ERR_CUDA;
-  return SPEC_OK;
+  const int tc_sms = draft_tc_ok(a, &sms) ? sms : 0;
+  // partials first, the counters after the larger of the two paths' partials
+  return run_draft(a, seed, reinterpret_cast<Partial*>(ws),
+                   reinterpret_cast<unsigned*>(ws + draft_partials_bytes(a.R, a.V)), tc_sms,
+                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 int spec_schedule(const spec_sched_args* args, spec_stream_t stream) {
