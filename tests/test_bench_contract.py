@@ -29,3 +29,28 @@ def test_reference_arm_json_line(config, head, extra):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"].get("head", "markov") == head
+
+
+def test_workload_options():
+    """--head and --async-cap reach the workload and the reported config; the
+    verify-only greedy workload refuses both (it has no draft or schedule)."""
+    import argparse
+    import sys as _sys
+    _sys.path.insert(0, ROOT)
+    import bench
+
+    def args(**kw):
+        base = dict(config="c5", sched_mode="workload", sched_threshold=0.3, head="markov",
+                    async_cap=False)
+        base.update(kw)
+        return argparse.Namespace(**base)
+
+    wl = bench._workload(args(head="rnn", async_cap=True))
+    assert wl.head == "rnn" and wl.async_cap and wl.name == "c5"
+    cfg = bench._sched_config(wl)
+    assert cfg["sched_mode"] == "early_stop" and "async_cap" in cfg
+    wl = bench._workload(args(sched_mode="threshold", sched_threshold=0.25))
+    assert bench._sched_config(wl) == {"sched_mode": "threshold", "sched_threshold": 0.25}
+    for kw in (dict(head="rnn"), dict(async_cap=True)):
+        with pytest.raises(SystemExit):
+            bench._workload(args(config="greedy", **kw))
