@@ -430,6 +430,16 @@ int spec_round_host(const spec_round_host_args *args, uint64_t seed, spec_stream
 int spec_stream_uniforms(uint64_t seed, uint32_t j, uint32_t rid, uint32_t purpose, int V,
                          float *u_out, float *e_out, spec_stream_t stream);
 
+/* ------------------------------------------------------- wait self-test -
+ * Exercises the bounded wait that every pipeline wait of the tensor-core
+ * kernels uses (an mbarrier try-wait that gives up after a time limit): one
+ * thread waits on a barrier that nothing will ever complete, gives up after
+ * limit_ns nanoseconds (measured on the GPU's global timer), sets
+ * SPEC_STATUS_TIMEOUT in *status (device word, required) and returns.  No
+ * copy or tensor-memory operation is in flight, so the context stays usable.
+ * 1 <= limit_ns <= 2e9 (SPEC_ERR_INVALID_ARG otherwise). */
+int spec_wait_selftest(uint64_t limit_ns, uint32_t *status, spec_stream_t stream);
+
 /* Workspace bytes a stage needs for these sizes (0 if the sizes are invalid).
  * `stage` is a spec_stage; r is ignored by SCHEDULE and VERIFY-greedy. */
 size_t spec_workspace_bytes(int stage, int R, int gamma, int V, int r);

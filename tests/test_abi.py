@@ -227,6 +227,11 @@ def test_host_side_rejections_launch_nothing(spec):
     v.mode, v.c_star = 1, ctypes.c_void_p(256)  # c* needs sample mode
     assert lib.spec_verify(ctypes.byref(v), 0, None) == spec.SPEC_ERR_INVALID_ARG
     assert lib.spec_stream_uniforms(0, 1, 0, 0, 0, None, None, None) == spec.SPEC_ERR_INVALID_ARG
+    # the wait self-test: limits outside [1 ns, 2 s], no status word, a misaligned one
+    assert lib.spec_wait_selftest(0, ctypes.c_void_p(256), None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_wait_selftest(3_000_000_000, ctypes.c_void_p(256), None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_wait_selftest(1000, None, None) == spec.SPEC_ERR_INVALID_ARG
+    assert lib.spec_wait_selftest(1000, ctypes.c_void_p(258), None) == spec.SPEC_ERR_ALIGNMENT
 
 
 def test_missing_library_fails_loudly(spec, monkeypatch):

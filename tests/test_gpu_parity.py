@@ -343,3 +343,23 @@ def test_gpu_matches_oracle_on_tiny_vocab_rounds():
                        1.0, Ub, A, Ct, to_np(x0), np.ones(G), 31)
     same = (ov.out_tok == to_np(v["out_tok"])).all(axis=1)
     assert np.all(same | (ov.margin < NEAR_TIE)), np.flatnonzero(~same)[:10]
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """The pipeline waits of the tensor-core kernels are bounded: a wait that
+    nothing completes gives up after its limit, flags SPEC_STATUS_TIMEOUT and
+    returns (no fault, no hang); the next calls run normally."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    vs.wait_selftest(50_000_000, status)  # 50 ms
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(status.item()) == vs.STATUS_TIMEOUT
+    assert 0.045 < waited < 5.0
+    wl = SMALL["tc_c5_temp"]
+    g = _to_dev(synth.make_inputs(wl, "cpu"))
+    d, s, v = _run(g, wl, 3)
+    rep = compare_draft(g, d, 3, range(wl.R))
+    assert rep.checked > 0

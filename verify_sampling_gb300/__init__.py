@@ -32,6 +32,7 @@ SCHED_EARLY_STOP, SCHED_GLOBAL, SCHED_THRESHOLD = 0, 1, 2
 STAGE_DRAFT, STAGE_SCHEDULE, STAGE_VERIFY = 0, 1, 2
 HEAD_MARKOV, HEAD_RNN = 0, 1
 STATUS_BAD_TOKEN, STATUS_BAD_ELL, STATUS_BAD_SURVIVAL, STATUS_BAD_ROW = 0x1, 0x2, 0x4, 0x8
+STATUS_TIMEOUT = 0x10
 
 _P = ctypes.c_void_p
 
@@ -118,6 +119,8 @@ def lib() -> ctypes.CDLL:
         L.spec_error_string.argtypes = [ctypes.c_int]
         L.spec_error_string.restype = ctypes.c_char_p
         L.spec_version.restype = ctypes.c_int
+        L.spec_wait_selftest.argtypes = [ctypes.c_uint64, _P, _P]
+        L.spec_wait_selftest.restype = ctypes.c_int
         L.spec_stream_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                            ctypes.c_uint32, ctypes.c_int, _P, _P, _P]
         L.spec_stream_uniforms.restype = ctypes.c_int
@@ -177,6 +180,14 @@ def stream_uniforms(seed: int, j: int, rid: int, purpose: int, V: int, device="c
     _check(lib().spec_stream_uniforms(seed & 0xFFFFFFFFFFFFFFFF, j, rid, purpose, V, _ptr(u),
                                       _ptr(e), _stream_handle(stream)), "spec_stream_uniforms")
     return u, e
+
+
+def wait_selftest(limit_ns: int, status: torch.Tensor, stream=None) -> None:
+    """spec_wait_selftest: a bounded wait that nothing completes gives up after
+    limit_ns and sets STATUS_TIMEOUT in ``status`` (int32 device word)."""
+    status = _dev(status, "status")
+    _check(lib().spec_wait_selftest(int(limit_ns), _ptr(status), _stream_handle(stream)),
+           "spec_wait_selftest")
 
 
 # -------------------------------------------------------------------- draft --
