@@ -74,7 +74,7 @@ def lib() -> ctypes.CDLL:
         L.orc_schedule.argtypes = [i32, i32, P, P, i32, f64, f64, i32, i32, f64, P, P, P, P, P, P]
         L.orc_schedule.restype = i32
         L.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, P, i64, P, P, i32, P, P,
-                                 u64, u32, P, P, P, P, P, P]
+                                 u64, u32, P, P, P, P, P, P, P, P]
         L.orc_verify.restype = i32
         L.orc_accept_stats.argtypes = [i32, i32, P, P, i32, i32, f64, i32, P, P, P, P]
         L.orc_accept_stats.restype = i32
@@ -231,6 +231,8 @@ class VerifyOut:
     n_out: np.ndarray
     margin: np.ndarray
     jstar: np.ndarray
+    margin_acc: np.ndarray  # smallest |u - p/q| of the accept tests (+inf: none made)
+    margin_gap: np.ndarray  # Gumbel top-2 gap of the emitted sample (+inf in greedy mode)
 
 
 def verify(mode: int, tgt, row_off, ell, x, q_tok, target_temp: float, U, A, Ct, x0, draft_temp,
@@ -255,14 +257,16 @@ def verify(mode: int, tgt, row_off, ell, x, q_tok, target_temp: float, U, A, Ct,
     out = np.zeros((R, gamma + 1), np.int32)
     n_out = np.zeros(R, np.int32)
     mg = np.zeros(R)
+    mg_acc = np.zeros(R)
+    mg_gap = np.zeros(R)
     js = np.zeros(R, np.int32)
     rc = lib().orc_verify(mode, R, gamma, V, _ptr(tgt), _ptr(row_off), _ptr(ell), _ptr(x), _ptr(q),
                           target_temp, _ptr(U), gamma * V, _ptr(A), _ptr(Ct), r, _ptr(x0),
                           _ptr(temp), seed, rid_base, _ptr(acc), _ptr(out), _ptr(n_out), _ptr(mg),
-                          _ptr(js), _ptr(None if S is None else _f32(S)))
+                          _ptr(js), _ptr(None if S is None else _f32(S)), _ptr(mg_acc), _ptr(mg_gap))
     if rc != 0:
         raise ValueError(f"orc_verify failed ({rc})")
-    return VerifyOut(acc, out, n_out, mg, js)
+    return VerifyOut(acc, out, n_out, mg, js, mg_acc, mg_gap)
 
 
 # ----------------------------------------------------- acceptance statistics --

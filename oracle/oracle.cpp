@@ -456,12 +456,15 @@ int orc_schedule(int R, int gamma, const double* a, const double* sps, int n_sps
 // n_out, margin (smallest decision margin: |u - p/q| of every accept test made
 // and the Gumbel top-2 gap of the emitted sample; +inf in greedy mode, whose
 // decisions are exact comparisons), jstar (first rejected position, 0 if none).
+// margin_acc and margin_gap (nullable) split margin by kind: the smallest
+// |u - p/q| of the accept tests, and the Gumbel gap of the emitted residual or
+// bonus sample (+inf where the request made no such decision).
 int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_t* row_off,
                const int32_t* ell, const int32_t* x, const double* q_tok, double target_temp,
                const float* U, int64_t U_rstride, const float* A, const float* Ct, int r,
                const int32_t* x0, const float* draft_temp, uint64_t seed, uint32_t rid_base,
                int32_t* accept_len, int32_t* out_tok, int32_t* n_out, double* margin,
-               int32_t* jstar_out, const float* S) {
+               int32_t* jstar_out, const float* S, double* margin_acc, double* margin_gap) {
   if ((mode != 0 && mode != 1) || R < 0 || gamma <= 0 || V <= 0) return -1;
   Stream rng(seed);
   std::vector<double> zt, p, zq;
@@ -472,7 +475,7 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
     const int32_t* xr = x + (size_t)req * gamma;
     int32_t* out = out_tok + (size_t)req * (gamma + 1);
     for (int i = 0; i <= gamma; ++i) out[i] = -1;
-    double mg = kInf;
+    double mg = kInf, mg_acc = kInf, mg_gap = kInf;
     int jstar = 0;
     int y = -1;
 
@@ -515,7 +518,8 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
           accept = true;
         } else {
           double ratio = p[(size_t)xj] / q;
-          mg = std::min(mg, std::fabs(u - ratio));
+          mg_acc = std::min(mg_acc, std::fabs(u - ratio));
+          mg = std::min(mg, mg_acc);
           accept = u < ratio;
         }
         if (!accept) {
@@ -547,6 +551,7 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
         target_probs(l + 1);
         y = gumbel_argmax(zt, rng, (uint32_t)(l + 1), rid, kBonusGumbel, &g);
       }
+      mg_gap = g;
       mg = std::min(mg, g);
     }
 
@@ -556,6 +561,8 @@ int orc_verify(int mode, int R, int gamma, int V, const float* tgt, const int32_
     accept_len[req] = acc;
     n_out[req] = acc + 1;
     if (margin) margin[req] = mg;
+    if (margin_acc) margin_acc[req] = mg_acc;
+    if (margin_gap) margin_gap[req] = mg_gap;
     if (jstar_out) jstar_out[req] = jstar;
   }
   return 0;

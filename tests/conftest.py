@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """One machine-readable line with the near-tie counts of every parity
+    test that ran (per configuration and decision kind)."""
+    import near_ties
+    line = near_ties.summary_line()
+    if line:
+        terminalreporter.write_line("NEAR_TIES " + line)

@@ -18,6 +18,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
+import near_ties
 import oracle
 
 NEAR_TIE = 1e-6
@@ -26,9 +27,52 @@ PROB_TOL = 1e-5
 
 @dataclass
 class Report:
+    """checked: decisions compared bit-exactly; near_ties: exempted decisions
+    (oracle margin below NEAR_TIE) on which the two sides disagreed; kinds:
+    per decision kind, [checked, near, differ] (see near_ties.py)."""
     checked: int = 0
     near_ties: int = 0
     notes: list = field(default_factory=list)
+    kinds: dict = field(default_factory=dict)
+
+    def count(self, kind: str, checked: int = 0, near: int = 0, differ: int = 0) -> None:
+        row = self.kinds.setdefault(kind, [0, 0, 0])
+        row[0] += int(checked)
+        row[1] += int(near)
+        row[2] += int(differ)
+
+
+def record(config: str, rep: Report) -> Report:
+    """Add a report's per-kind counts to the session's near-tie record."""
+    for kind, (checked, near, differ) in rep.kinds.items():
+        near_ties.add(config, kind, checked, near, differ)
+    return rep
+
+
+def pick_full_size_requests(ell, accept_len, R: int, n_rejected: int = 32, n_bonus: int = 12,
+                            always=(0, 1)):
+    """Requests to compare at full size: every request the GPU rejected, up
+    to n_rejected of them, taken round-robin over the rejected position j* (so
+    the residual pass's per-position tiles are all reached); n_bonus of the
+    requests that accepted every admitted position (their bonus row is
+    sampled), spread over l_r; plus `always`, the middle and the last request.
+    Returns (sorted requests, rejected among them, bonus among them)."""
+    ell, acc = np.asarray(ell), np.asarray(accept_len)
+    rej = np.flatnonzero(acc < ell)
+    by_pos = {}
+    for r in rej:
+        by_pos.setdefault(int(acc[r]) + 1, []).append(int(r))
+    picked_rej = []
+    while len(picked_rej) < min(n_rejected, len(rej)):
+        for j in sorted(by_pos):
+            if by_pos[j] and len(picked_rej) < n_rejected:
+                picked_rej.append(by_pos[j].pop(0))
+    bon = np.flatnonzero(acc == ell)
+    order = bon[np.argsort(ell[bon], kind="stable")]
+    picked_bon = [int(order[i]) for i in np.linspace(0, len(order) - 1, min(n_bonus, len(order))
+                                                    ).round().astype(int)] if len(order) else []
+    reqs = sorted(set(picked_rej) | set(picked_bon) | {int(a) for a in always} | {R // 2, R - 1})
+    return reqs, [r for r in reqs if acc[r] < ell[r]], [r for r in reqs if acc[r] == ell[r]]
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -50,6 +94,7 @@ def compare_draft(inp: dict, out: dict, seed: int, reqs, rid_base: int = 0, rep=
         assert np.all(same | tie), (r, od.x[0], x_gpu[r], od.gap[0])
         rep.near_ties += int(np.sum(~same & tie))
         rep.checked += len(same)
+        rep.count("draft_gap", len(same), np.sum(tie), np.sum(~same & tie))
         q = to_np(out["q_tok"][r])
         lse = to_np(out["lse_q"][r])
         ok = same  # values of a near-tie row refer to different tokens
@@ -75,9 +120,16 @@ def compare_schedule(inp: dict, a_gpu: torch.Tensor, sched: dict, K: int, mode: 
                           inp["b_lo"], inp["b_step"], K, mode, threshold)
     stats = to_np(sched["stats"])
     if os_.margin < NEAR_TIE:
-        rep.near_ties += 1
-        rep.notes.append(f"schedule near-tie margin {os_.margin:.3g}")
-        return rep
+        # exempt: the decision is compared with a relative Theta step below the
+        # margin, so record whether the two sides agreed but do not assert it
+        same = (to_np(sched["ell"]) == os_.ell).all()
+        rep.near_ties += 0 if same else 1
+        rep.count("theta_step", 1, 1, 0 if same else 1)
+        rep.notes.append(f"schedule near-tie margin {os_.margin:.3g} (agree: {same})")
+        if not same:
+            return rep
+    else:
+        rep.count("theta_step", 1)
     assert (to_np(sched["ell"]) == os_.ell).all()
     assert (to_np(sched["row_off"]) == os_.row_off).all()
     assert int(stats[0]) == os_.n and int(stats[1]) == os_.B
@@ -119,6 +171,7 @@ def compare_draft_rnn(inp: dict, W: torch.Tensor, S: torch.Tensor, out: dict, se
         assert np.all(same | tie), (r, od.x[0], x_gpu[r], od.gap[0])
         rep.near_ties += int(np.sum(~same & tie))
         rep.checked += len(same)
+        rep.count("draft_gap", len(same), np.sum(tie), np.sum(~same & tie))
         q, lse = to_np(out["q_tok"][r]), to_np(out["lse_q"][r])
         assert np.all(np.abs(q - od.q_tok[0])[same] < PROB_TOL), (r, q, od.q_tok[0])
         assert np.all((np.abs(lse - od.lse[0]) / np.maximum(1, np.abs(od.lse[0])))[same] < PROB_TOL)
@@ -155,7 +208,14 @@ def compare_verify(inp: dict, d_out: dict, ell: torch.Tensor, v_out: dict, seed:
                                rid_base=rid_base + r,
                                S=None if S is None else to_np(S[r:r + 1]))
         got = to_np(v_out["out_tok"][r])
-        if ov.margin[0] < NEAR_TIE and not (got == ov.out_tok[0]).all():
+        if mode == oracle.MODE_GREEDY:
+            rep.count("greedy_argmax", 1)
+        differ = not (got == ov.out_tok[0]).all()
+        near_acc, near_gap = ov.margin_acc[0] < NEAR_TIE, ov.margin_gap[0] < NEAR_TIE
+        rep.count("accept_margin", np.isfinite(ov.margin_acc[0]), near_acc, differ and near_acc)
+        rep.count("sample_gap", np.isfinite(ov.margin_gap[0]), near_gap,
+                  differ and near_gap and not near_acc)
+        if ov.margin[0] < NEAR_TIE and differ:
             rep.near_ties += 1
             rep.notes.append(f"verify near-tie r={r} margin={ov.margin[0]:.3g}")
             continue

@@ -22,7 +22,7 @@ import torch
 import oracle
 import synth
 import verify_sampling_gb300 as vs
-from parity import compare_schedule, to_np
+from parity import compare_schedule, record, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -57,6 +57,7 @@ def test_schedule_threshold_parity(R, gamma):
             torch.cuda.synchronize()
             rep = compare_schedule(inp, a, s, K, oracle.SCHED_THRESHOLD, threshold=theta)
             assert rep.near_ties == 0  # threshold decisions are exact comparisons
+            record(f"schedule_threshold_R{R}_g{gamma}", rep)
             n = int(to_np(s["stats"])[0])
             assert n == min(K, int((a_np >= theta).sum()))
             checked += 1
@@ -199,8 +200,11 @@ def test_cstar_full_size_c5_sampled():
     g = synth.make_inputs(wl, DEV, seed=wl.seed)
     d, s, v = _cstar_run(g, wl, 4243, wl.K)
     ell, x = to_np(s["ell"]), to_np(d["x"])
-    order = np.argsort(-ell, kind="stable")
-    reqs = sorted({int(order[0]), int(order[1]), 0, wl.R - 1})
+    # 32 requests spread over l_r (every verified row of each is compared)
+    order = np.argsort(ell, kind="stable")
+    reqs = sorted({int(order[i]) for i in np.linspace(0, wl.R - 1, 32).round().astype(int)}
+                  | {0, wl.R - 1})
+    assert len(reqs) >= 32 and len({int(ell[r]) for r in reqs}) >= 4
     want = _cstar_oracle(g, reqs, x, ell, to_np(g["draft_temp"]))
     _check_cstar(to_np(v["c_star"])[reqs], want)
     assert np.isnan(to_np(v["c_star"])[ell == 0]).all()
@@ -277,6 +281,7 @@ def test_async_cap_chain(mode):
         k_t = K if t < 2 else min(K, free_seen[t - 2])
         inp = {"sps": sps, "b_lo": 1.0, "b_step": 1.0}
         rep = compare_schedule(inp, a, s, k_t, mode, threshold=thr)
+        record(f"async_cap_mode{mode}", rep)
         of = oracle.schedule(a_np.astype(np.float64), sps_np, 1.0, 1.0, N, mode, thr)
         if of.margin >= 1e-6 and rep.near_ties == 0:
             assert int(word.item()) == of.n, (t, int(word.item()), of.n)
@@ -301,3 +306,4 @@ def test_schedule_unordered_survivals(R, gamma):
         torch.cuda.synchronize()
         rep = compare_schedule(inp, a, s, K, mode, threshold=0.4)
         assert rep.checked + rep.near_ties == 1
+        record(f"schedule_unordered_R{R}_g{gamma}", rep)

@@ -21,7 +21,8 @@ import torch
 import oracle
 import synth
 import verify_sampling_gb300 as vs
-from parity import PROB_TOL, compare_draft_rnn, compare_verify, to_np
+from parity import (PROB_TOL, compare_draft_rnn, compare_verify, pick_full_size_requests, record,
+                    to_np)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -69,11 +70,13 @@ def _cstar_oracle(g, reqs, x, ell, S):
                         S=to_np(S[idx]))
 
 
-def _check(g, wl, W, seed, S, d, s, v, reqs):
+def _check(g, wl, W, seed, S, d, s, v, reqs, config):
     rep = compare_draft_rnn(g, W, S, d, seed, reqs)
     assert rep.near_ties <= max(1, len(reqs) * wl.gamma // 100)
+    record(config, rep)
     rep = compare_verify(g, d, s["ell"], v, seed, oracle.MODE_SAMPLE, reqs, S=S)
     assert rep.checked >= len(reqs) - max(1, len(reqs) // 20)
+    record(config, rep)
     ell, x = to_np(s["ell"]), to_np(d["x"])
     want = _cstar_oracle(g, list(reqs), x, ell, S)
     got = to_np(v["c_star"])[list(reqs)]
@@ -93,7 +96,7 @@ def test_rnn_round_parity_small(name):
     S, d, s, v = _round(g, wl, W, seed, want_P=wl.V <= 20000)
     assert not torch.isnan(S.float()).any()
     reqs = SAMPLED.get(name, range(wl.R))
-    _check(g, wl, W, seed, S, d, s, v, list(reqs))
+    _check(g, wl, W, seed, S, d, s, v, list(reqs), "rnn_" + name)
 
 
 def test_rnn_differs_from_markov_and_reruns_identically():
@@ -119,10 +122,9 @@ def test_rnn_full_size_c5_sampled():
     seed = 4243
     S, d, s, v = _round(g, wl, W, seed, want_P=False)
     assert not torch.isnan(S.float()).any()
-    ell = to_np(s["ell"])
-    order = np.argsort(-ell, kind="stable")
-    reqs = sorted({0, 1, 255, wl.R - 1, int(order[0]), int(order[1])})
-    _check(g, wl, W, seed, S, d, s, v, reqs)
+    reqs, rejected, bonus = pick_full_size_requests(to_np(s["ell"]), to_np(v["accept_len"]), wl.R)
+    assert len(rejected) >= 8 and len(bonus) >= 8 and len(reqs) >= 32
+    _check(g, wl, W, seed, S, d, s, v, reqs, "rnn_c5")
 
 
 def test_rnn_request_sharding_is_invariant():
