@@ -41,7 +41,10 @@
  *    3 bonus Gumbel.  Results depend only on (seed, global request id,
  *    position), so a batch split into pieces with matching request_id_base
  *    gives identical results.
- *  - The library keeps no global state; calls are thread-safe.
+ *  - The library keeps no global state, with one exception: the scratch array
+ *    of spec_draft_sample_static (below) and its cached device address.
+ *    Calls are thread-safe, except that calls of that entry point which
+ *    overlap on the GPU share its scratch.
  */
 #ifndef SPEC_H
 #define SPEC_H
@@ -163,10 +166,13 @@ int spec_draft_sample(const spec_draft_args *args, uint64_t seed, spec_stream_t 
  * sizes need more scratch than that (the need is about
  * 64 * R * splits + 4 * R * (1 + gamma) bytes on the tensor-core path, two
  * slots of split partials, with at most 152 splits per 128 requests on a
- * GB300, and 32 * R * splits + 4 * R * (1 + gamma) on the generic one).  The first call on each device resolves the
- * array's device address (cudaGetSymbolAddress); make it before any stream
- * capture.  All calls share the array: calls that overlap on the GPU race and
- * give wrong results. */
+ * GB300, and 32 * R * splits + 4 * R * (1 + gamma) on the generic one; for
+ * example 4096 requests at gamma = 16 on the tensor-core path need 1.33 MB).
+ * The first call on each device resolves the array's device address
+ * (cudaGetSymbolAddress) and caches it per context; make it before any stream
+ * capture.  A context that is destroyed and created again (cudaDeviceReset)
+ * gets a fresh lookup on its next call.  All calls share the array: calls
+ * that overlap on the GPU race and give wrong results. */
 int spec_draft_sample_static(const spec_draft_args *args, uint64_t seed, spec_stream_t stream);
 
 /* --------------------------------------------------------------- schedule -

@@ -47,6 +47,24 @@ def test_static_scratch_matches_workspace_entry_point(name):
             assert torch.allclose(got[key], ref[key], rtol=0, atol=1e-5), key
 
 
+def test_static_scratch_allocates_no_device_memory():
+    """The defining property: after a first call (which resolves the scratch
+    array's address and loads the kernels), further calls leave the device's
+    free memory unchanged (cudaMemGetInfo)."""
+    wl = CASES["fused_fp32"]
+    g = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v)
+         for k, v in synth.make_inputs(wl, "cpu").items()}
+    din = synth.draft_inputs(g)
+    got = vs.draft_outputs(wl.R, wl.gamma, wl.V, "cuda")
+    _static_call(din, got, 3)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for seed in (4, 5, 6):
+        _static_call(din, got, seed)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+
+
 def test_static_scratch_rejects_oversized_batches():
     wl = synth.WORKLOADS["tiny"].scaled(R=60000, gamma=20, V=8)
     din = vs.DraftInputs(U=torch.zeros(wl.R, wl.gamma, wl.V, device="cuda"),

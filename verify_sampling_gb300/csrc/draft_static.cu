@@ -10,10 +10,16 @@
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (with
 // that device current) and caches it; make that first call before any stream
-// capture.  All calls share the one array and it keeps the last call's
-// contents: the counters are cleared at the start of every call, and two calls
-// that overlap on the GPU (different streams, or different host threads on
-// one stream without ordering) race on it and give wrong results.
+// capture.  The cache is keyed by the device's current context as well: a
+// context that is destroyed and created again (cudaDeviceReset, or a primary
+// context released and retained) loads the module again, the array can move,
+// and the next call looks the address up anew.  All calls share the one array
+// and it keeps the last call's contents: the counters are cleared at the
+// start of every call, and two calls that overlap on the GPU (different
+// streams, or different host threads on one stream without ordering) race on
+// it and give wrong results.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "draft.cuh"
@@ -24,20 +30,54 @@ namespace {
 
 using namespace spec;
 
-constexpr size_t kStaticScratchBytes = 2u << 20;  // 2 MiB: about 58000 requests
+// 2 MiB.  The need is 32 * R * s + 4 * R * (1 + gamma) bytes (the first term
+// rounded up to 256): s = 2 * splits on the tensor-core path, with splits =
+// SMs / ceil(R / 128) capped by the 64-column vocabulary tiles, and the
+// generic kernel's split count otherwise.  On a 152-SM GB300 the tensor-core
+// path at gamma = 16 fits up to about 15000 requests (4096 need 1.33 MB).
+constexpr size_t kStaticScratchBytes = 2u << 20;
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_draft_scratch[kStaticScratchBytes];
 
-// Device address of g_draft_scratch on device `dev` (looked up once).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(ptr);
+}
+
+// Unique id of the calling thread's current context (0 if there is none yet).
+bool current_context_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return !ctx || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_draft_scratch on device `dev` in its current context.
 void* scratch_address(int dev) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) return nullptr;
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
+    void* p = nullptr;  // the lookup also makes the primary context current
     if (cudaGetSymbolAddress(&p, g_draft_scratch) != cudaSuccess) return nullptr;
+    if (!current_context_id(&ctx) || ctx == 0) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   return addr[dev];
 }
