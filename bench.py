@@ -41,7 +41,7 @@ def _args():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", default="c5", choices=["c2", "c3", "c5", "c5p", "greedy"])
+    p.add_argument("--config", default="c5", choices=["tiny", "c2", "c3", "c5", "c5p", "greedy"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--sched-mode", default="workload",
@@ -56,7 +56,10 @@ def _args():
                         "recurrent state (synthetic recurrence W_k ~ N(0, 1/r))")
     p.add_argument("--async-cap", action="store_true",
                    help="cap each round's admissions by the uncapped count of the round two "
-                        "earlier, kept on the device (the first two rounds use K)")
+                        "earlier, kept on the device (the first two rounds use K); the c5 "
+                        "workload's own cap, so its default")
+    p.add_argument("--static-cap", action="store_true",
+                   help="cap every round by the fixed K only (also for c5)")
     p.add_argument("--calibration", action="store_true",
                    help="also compute c* = sum min(p, q) of every verified row and fold the "
                         "round into the reliability diagram (ECE)")
@@ -74,19 +77,33 @@ def _workload(args):
         if wl.mode == "greedy":
             raise SystemExit("--head applies to workloads with a draft stage")
         wl = dataclasses.replace(wl, head=args.head)
+    static = getattr(args, "static_cap", False)
+    if args.async_cap and static:
+        raise SystemExit("--async-cap and --static-cap exclude each other")
     if args.async_cap:
         if wl.mode == "greedy":
             raise SystemExit("--async-cap applies to workloads with a schedule")
         wl = dataclasses.replace(wl, async_cap=True)
+    elif not static and wl.name in ASYNC_CAP_WORKLOADS:
+        # the workload's stated cap: top-K from the confidences of two rounds back
+        wl = dataclasses.replace(wl, async_cap=True)
     return wl
 
 
+# Workloads whose stated top-K cap is the asynchronous one (K_t from round t-2).
+ASYNC_CAP_WORKLOADS = ("c5", "c5p")
+
+
 # DRAM bytes (read + write) of one launch of the dominant kernel, taken with
-# ncu on the same per-launch shape (profiles/draft_tc_R512_V129280_r128_fp32.md),
+# ncu on the same per-launch shape (R=512, V=129280, r=128, fp32 logits, one
+# draft position; the committed draft-kernel profile gives the command),
 # keyed by a hash of the kernel's sources: a changed kernel reports null until
 # it is profiled again.
 DRAFT_TC_SOURCES = ["draft_tc.cu", "draft_tc.cuh", "fused_tc.cuh", "tc.cuh", "common.cuh"]
 MEASURED_TRAFFIC = {("c5", "7053e00a74b75bba"): 298082048 + 3678720}
+# Tensor-pipe utilisation (%, sm__pipe_tensor_cycles_active) of the same
+# capture: the bias GEMM A_k[x] C_k on tcgen05, keyed the same way.
+MEASURED_TENSOR_PIPE = {("c5", "7053e00a74b75bba"): 7.52}
 
 
 def _source_hash(files) -> str:
@@ -291,10 +308,12 @@ def run_reference(args, wl):
             "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * tot_sec / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "R": wl.R, "gamma": wl.gamma, "V": wl.V, "r": wl.r,
-                       **_sched_config(wl), **({"head": "rnn"} if wl.head == "rnn" else {})},
+            "config": _config(wl, args.gpus),
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n} of {wl.R} requests per step ({_stages(wl, n)})"},
+                             "sample": f"{n} of {wl.R} requests per step ({_stages(wl, n)}); "
+                                       f"the schedule runs over those {n} with K scaled to "
+                                       f"them, so l_r (and B) come from a {n}-request "
+                                       "schedule"},
             "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -320,6 +339,30 @@ def combine_over_ranks(ms: float, positions: float, device, world: int) -> tuple
     tp = torch.tensor([positions], dtype=torch.float64, device=device)
     dist.all_reduce(tp, op=dist.ReduceOp.SUM)
     return float(tm.item()), float(tp.item())
+
+
+def _config(wl, world: int) -> dict:
+    """The workload as reported in the JSON line (both arms)."""
+    import torch
+    return {"workload": wl.name, "R": wl.R, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "K": wl.K,
+            "logits": str(wl.logit_dtype).replace("torch.", ""),
+            "factors": str(wl.fac_dtype).replace("torch.", ""),
+            "l2": (f"inputs per step {_step_input_bytes(wl) / 1e6:.0f} MB, larger than L2 "
+                   "(no flush)") if _step_input_bytes(wl) >= 2 * L2_BYTES else
+                  "L2 flushed between timed steps (256 MB written)",
+            "parallelism": f"replicas x{world}",
+            **_sched_config(wl), **({"head": "rnn"} if wl.head == "rnn" else {})}
+
+
+def _step_input_bytes(wl) -> int:
+    """Logit and factor bytes one step reads: the padded target rows, and for
+    workloads with a draft stage the backbone logits and C."""
+    import torch
+    es = lambda dt: 2 if dt == torch.bfloat16 else 4
+    n = wl.R * (wl.gamma + 1) * wl.V * es(wl.logit_dtype)
+    if wl.mode != "greedy":
+        n += wl.R * wl.gamma * wl.V * es(wl.logit_dtype) + wl.gamma * wl.V * wl.r * es(wl.fac_dtype)
+    return n
 
 
 def _sched_config(wl) -> dict:
@@ -362,6 +405,12 @@ def main():
         din.Wrnn = synth.rnn_weights(wl, dev, seed=seed_in)
         din.S = torch.empty(R, G, wl.r, dtype=wl.fac_dtype, device=dev)
     stats_hist = torch.zeros(max(1, args.steps), 4, dtype=torch.float64, device=dev)
+    # per timed step: l_r and accept_len (residual rows = requests rejected at j <= l_r)
+    acc_hist = torch.zeros(max(1, args.steps), 2, R, dtype=torch.int32, device=dev)
+    # inputs read per step; below twice the L2 size the L2 is flushed between
+    # timed steps (outside their events)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) \
+        if _step_input_bytes(wl) < 2 * L2_BYTES else None
 
     bufs = {}
     if not greedy:
@@ -386,9 +435,13 @@ def main():
     def step(i: int, timed: bool):
         seed = 7000 + i
         if greedy:
+            if timed:
+                ev["d0"][i].record(stream)
             bufs["verify"] = vs.verify(vs.VERIFY_GREEDY, g["tgt"].view(-1, V), g["tgt_row_off"],
                                        g["ell"], g["x"], seed, out=bufs.get("verify"),
                                        workspace=bufs["ws_verify"])
+            if timed:
+                ev["v1"][i].record(stream)
             return
         if timed:
             ev["d0"][i].record(stream)
@@ -415,6 +468,8 @@ def main():
         if timed:
             ev["v1"][i].record(stream)
             stats_hist[i].copy_(s["stats"], non_blocking=True)
+            acc_hist[i, 0].copy_(s["ell"], non_blocking=True)
+            acc_hist[i, 1].copy_(v["accept_len"], non_blocking=True)
 
     for i in range(args.warmup):
         step(-1 - i, False)
@@ -427,19 +482,27 @@ def main():
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
+        if flush is not None:  # evict the previous step's inputs (not timed)
+            flush.zero_()
         step(i, True)
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    ms = t0.elapsed_time(t1)
     stage_ms = {"draft": 0.0, "schedule": 0.0, "verify": 0.0}
-    if not greedy:
-        for i in range(args.steps):
+    step_ms = 0.0
+    for i in range(args.steps):
+        step_ms += ev["d0"][i].elapsed_time(ev["v1"][i])
+        if not greedy:
             stage_ms["draft"] += ev["d0"][i].elapsed_time(ev["d1"][i])
             stage_ms["schedule"] += ev["d1"][i].elapsed_time(ev["s1"][i])
             stage_ms["verify"] += ev["s1"][i].elapsed_time(ev["v1"][i])
+        else:
+            stage_ms["verify"] += ev["d0"][i].elapsed_time(ev["v1"][i])
+    # with inputs larger than L2 the whole region is timed; with the flush,
+    # the steps' own events (the flushes between them are left out)
+    ms = t0.elapsed_time(t1) if flush is None else step_ms
     if greedy:
         B_sum = float(args.steps * R * (G + 1))
         positions = B_sum
@@ -473,29 +536,45 @@ def main():
             kernel = "draft_step (one launch per position k; RNN head, state rows gathered)"
     achieved = per_launch / (dur_ms / 1000.0) / 1e9
     # measured on the Markov head's launch (the RNN head's gathers other rows)
-    traffic = None if greedy or rnn else MEASURED_TRAFFIC.get((wl.name, _source_hash(DRAFT_TC_SOURCES)))
+    src = _source_hash(DRAFT_TC_SOURCES)
+    traffic = None if greedy or rnn else MEASURED_TRAFFIC.get((wl.name, src))
+    tensor_pipe = None if greedy or rnn else MEASURED_TENSOR_PIPE.get((wl.name, src))
     roofline = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": per_launch,
                 # DRAM bytes the profiler counted per launch over the same
                 # event-timed duration (null with traffic)
-                "achieved_dram": None if traffic is None else round(traffic / (dur_ms / 1000.0) / 1e9, 1)}
+                "achieved_dram": None if traffic is None else round(traffic / (dur_ms / 1000.0) / 1e9, 1),
+                # tcgen05 pipe utilisation of the bias GEMM in the same capture
+                "tensor_pipe_pct": tensor_pipe}
+
+    # ---------------------------------------- round-level algorithmic bytes ----
+    stage_bytes = _round_bytes(wl, to_cpu(acc_hist), to_cpu(stats_hist), args.steps)
+    round_bytes = sum(stage_bytes.values())
+    stages = {}
+    for k in ("draft", "schedule", "verify"):
+        ms_k = stage_ms[k] / args.steps
+        st = {"ms": round(ms_k, 4)}
+        if stage_bytes.get(k):
+            st["algorithmic_bytes"] = int(stage_bytes[k])
+            st["gbs"] = round(stage_bytes[k] / (ms_k / 1000.0) / 1e9, 1)
+            st["frac"] = round(st["gbs"] / hbm, 4)
+        stages[k] = st
+    round_gbs = round_bytes / (ms_max / args.steps / 1000.0) / 1e9
+    round_logit = {"algorithmic_bytes_per_step": int(round_bytes), "gbs": round(round_gbs, 1),
+                   "frac": round(round_gbs / hbm, 4), "frac_of_8tbs": round(round_gbs / 8000.0, 4),
+                   "floor_ms": round(round_bytes / (hbm * 1e9) * 1000.0, 4)}
 
     line = {"metric": "draft+verified positions/s", "value": value, "unit": "positions/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if es_u == 4 else "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "R": R, "gamma": G, "V": V, "r": wl.r, "K": wl.K,
-                       "logits": str(wl.logit_dtype).replace("torch.", ""),
-                       "factors": str(wl.fac_dtype).replace("torch.", ""),
-                       "l2": "inputs larger than L2 (no flush)",
-                       "parallelism": f"replicas x{world}",
-                       **_sched_config(wl),
-                       **({"head": "rnn"} if rnn else {}),
+            "config": {**_config(wl, world),
                        **({"accept_stats": True} if acc_tab is not None else {}),
                        **({"calibration": True} if calib is not None else {})},
             "stage_ms_per_step": {k: round(v / args.steps, 4) for k, v in stage_ms.items()},
+            "stages": stages, "round_logit_gbs": round_logit,
             "mean_verify_rows": B_sum / args.steps,
             "roofline": roofline, "gpu_launches": launches * args.steps, "clocks": clk}
     if calib is not None:
@@ -513,6 +592,52 @@ def main():
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def to_cpu(t):
+    return t.cpu().numpy()
+
+
+def _round_bytes(wl, acc_hist, stats_hist, steps: int) -> dict:
+    """Algorithmic bytes of one round, per stage, averaged over the timed steps.
+    draft: gamma launches of the R backbone rows and C_k, plus the confidence
+    head's hidden states and W1 rows; verify: the B scheduled target rows, and
+    for every request rejected at j*: its backbone row and target row at j*,
+    plus C_{j*} once per position that has a rejection (the residual pass)."""
+    import numpy as np
+    import torch
+    es = lambda dt: 2 if dt == torch.bfloat16 else 4
+    R, G, V, r = wl.R, wl.gamma, wl.V, wl.r
+    e_u, e_f, e_c = es(wl.logit_dtype), es(wl.fac_dtype), es(wl.conf_dtype)
+    if wl.mode == "greedy":
+        return {"verify": R * (G + 1) * V * e_u}
+    draft = G * (R * V * e_u + V * r * e_f) + R * G * (wl.d + wl.e) * e_c
+    B = float(np.mean(stats_hist[:steps, 1]))
+    resid = 0.0
+    for i in range(steps):
+        ell, acc = acc_hist[i, 0], acc_hist[i, 1]
+        rej = acc < ell
+        n_rej = int(rej.sum())
+        n_pos = len(np.unique(acc[rej] + 1))
+        resid += n_rej * V * 2 * e_u + n_pos * V * r * e_f
+    return {"draft": draft, "verify": B * V * e_u + resid / steps}
+
+
+def _link_gbs(torch, src, dev) -> float:
+    """Host-to-device bandwidth of one copy of `src` (pinned) into the device."""
+    dst = torch.empty(src.shape, dtype=src.dtype, device=dev)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    e0.record(s)
+    dst.copy_(src, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1000.0) / 1e9
 
 
 def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None) -> dict:
@@ -588,9 +713,14 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None)
     sec = time.perf_counter() - t0
     pos = sum(p for p, _ in res)
     B_mean = sum(b for _, b in res) / steps
+    h2d = int(whole + B_mean * row_bytes)
+    link = _link_gbs(torch, host["U"], dev)
     return {"value": pos / sec, "unit": "positions/s",
-            "h2d_bytes_per_step": int(whole + B_mean * row_bytes),
-            "d2h_bytes_per_step": d2h, "steps": steps, "rounds_in_flight": 2,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "rounds_in_flight": 2, "ms_per_step": round(1000.0 * sec / steps, 3),
+            # one pinned copy of U's size, timed right after: the link's own rate,
+            # and the step time that rate alone would give for the step's bytes
+            "link_gbs": round(link, 1), "link_floor_ms": round(h2d / (link * 1e9) * 1000.0, 3),
             "target_rows": "the B scheduled rows of each step (mean %.1f), read from the "
                            "pinned [R, gamma+1, V] host array" % B_mean}
 
