@@ -45,14 +45,17 @@ def _to_dev(inp):
     return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def _run(g, wl, seed, want_P=False, rid_base=0, target_temp=1.0):
+def _run(g, wl, seed, want_P=False, rid_base=0, target_temp=1.0, want_p=True):
+    """One round.  want_p asks for the per-row diagnostics p_tok and lse_t,
+    which make the verifier read every scheduled row; without them it skips
+    the rows past a request's first rejection (the bench's configuration)."""
     din = synth.draft_inputs(g, request_id_base=rid_base)
     d = vs.draft_sample(din, seed, want_P=want_P)
     s = vs.schedule(d["a"], g["sps"], g["b_lo"], g["b_step"], g["K"], wl.sched_mode,
                     threshold=wl.sched_threshold, want_order=True)
     v = vs.verify(vs.VERIFY_SAMPLE, g["tgt"].view(-1, wl.V), g["tgt_row_off"], s["ell"], d["x"],
                   seed, q_tok=d["q_tok"], lse_q=d["lse_q"], target_temp=target_temp, draft=din,
-                  request_id_base=rid_base, want_p=True)
+                  request_id_base=rid_base, want_p=want_p)
     torch.cuda.synchronize()
     return d, s, v
 
@@ -79,6 +82,22 @@ def test_round_parity_small(name):
     for r in range(wl.R):
         assert (out[r, : n_out[r]] >= 0).all() and (out[r, : n_out[r]] < wl.V).all()
         assert (out[r, n_out[r]:] == -1).all()
+
+
+@pytest.mark.parametrize("name", ["tc_c5_small", "tc_c3_small_R130", "c3_small", "v3"])
+def test_skipped_rows_give_the_same_round(name):
+    """Without per-row diagnostics the verifier skips rows past a request's
+    first rejection: the round's outputs equal those of the pass that reads
+    every scheduled row, and the oracle's."""
+    wl = SMALL[name]
+    g = _to_dev(synth.make_inputs(wl, "cpu"))
+    seed = 2024
+    d, s, full = _run(g, wl, seed, want_p=True)
+    _, _, skip = _run(g, wl, seed, want_p=False)
+    for k in ("accept_len", "out_tok", "n_out"):
+        assert torch.equal(full[k], skip[k]), k
+    rep = compare_verify(g, d, s["ell"], skip, seed, oracle.MODE_SAMPLE, SAMPLED.get(name, range(wl.R)))
+    record(name + "_skip", rep)
 
 
 def test_target_temperature_parity():
@@ -117,6 +136,17 @@ def test_greedy_parity_small_with_ties():
     rep = compare_verify(g, None, g["ell"], v, 0, oracle.MODE_GREEDY, range(wl.R))
     assert rep.near_ties == 0 and rep.checked == wl.R
     record("greedy_small_planted_ties", rep)
+
+
+def test_greedy_long_draft_in_request_order():
+    """gamma >= 64 keeps the request-order row pass (no row skipping)."""
+    wl = synth.WORKLOADS["greedy"].scaled(R=5, gamma=70, V=300)
+    g = _to_dev(synth.make_inputs(wl, "cpu"))
+    v = vs.verify(vs.VERIFY_GREEDY, g["tgt"].view(-1, wl.V), g["tgt_row_off"], g["ell"], g["x"], 0)
+    torch.cuda.synchronize()
+    rep = compare_verify(g, None, g["ell"], v, 0, oracle.MODE_GREEDY, range(wl.R))
+    assert rep.near_ties == 0 and rep.checked == wl.R
+    record("greedy_gamma70", rep)
 
 
 def test_stream_bit_exact_and_neg_log_accuracy():
@@ -239,7 +269,7 @@ def test_full_size_sampled_parity(name):
     wl = synth.WORKLOADS[name]
     g = synth.make_inputs(wl, DEV, seed=wl.seed)
     seed = 4242
-    d, s, v = _run(g, wl, seed)
+    d, s, v = _run(g, wl, seed, want_p=False)  # as the bench runs it (rows skipped)
     reqs, rejected, bonus = pick_full_size_requests(to_np(s["ell"]), to_np(v["accept_len"]), wl.R)
     n_rej_gpu = int((v["accept_len"] < s["ell"]).sum())
     assert len(rejected) >= min(32, n_rej_gpu)

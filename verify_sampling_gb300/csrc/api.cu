@@ -335,6 +335,9 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   p.lse_t = a.lse_t;
   p.c_star = a.c_star;
   p.status = a.status;
+  // Rows after a request's first rejection (mismatch) influence no output
+  // unless a per-row diagnostic (p_tok, lse_t, c*) asks for them.
+  p.skip_dead = a.gamma + 1 <= 64 && !(sample && (a.p_tok || a.lse_t || a.c_star));
   {
     int dev = 0, major = 0, sms = 0;
     const bool dev_ok =

@@ -232,8 +232,11 @@ __device__ void finish_row(const VerifyParams& p, int r, int j, int l, const Rac
   (void)l;
 }
 
-// Plan: the packed list of scheduled rows, rows[b] = r * (gamma + 1) + j - 1
-// for j = 1 .. l_r + 1 in request order, and their number B (one CTA).
+// Plan: the packed list of scheduled rows, codes r * (gamma + 1) + j - 1 for
+// j = 1 .. l_r + 1, and their number B (one CTA).  Request order; with
+// skip_dead, position order (every request's row 1, then every row 2, ...),
+// so that a request's earlier rows are mostly finished before its later rows
+// are claimed and the rows past its end can be skipped.
 __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyParams p) {
   __shared__ int warp_sum[kPlanThreads / 32];
   __shared__ int carry;
@@ -241,24 +244,29 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyParams 
   const int G1 = p.gamma + 1;
   if (tid == 0) carry = 0;
   __syncthreads();
-  for (int r0 = 0; r0 < p.R; r0 += kPlanThreads) {  // uniform trip count
-    const int r = r0 + tid;
-    const int n = (r < p.R) ? clamp_ell(p, r) + 1 : 0;
-    int incl = n;  // inclusive warp scan
+  const int passes = p.skip_dead ? G1 : 1;
+  for (int pass = 0; pass < passes; ++pass) {
+    for (int r0 = 0; r0 < p.R; r0 += kPlanThreads) {  // uniform trip count
+      const int r = r0 + tid;
+      const int rows_r = (r < p.R) ? clamp_ell(p, r) + 1 : 0;
+      // request order: all rows of r; position order: row pass + 1 if scheduled
+      const int n = p.skip_dead ? (pass < rows_r ? 1 : 0) : rows_r;
+      int incl = n;  // inclusive warp scan
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (lane == 31) warp_sum[warp] = incl;
+      __syncthreads();
+      int before = carry;
+      for (int w = 0; w < warp; ++w) before += warp_sum[w];
+      const int start = before + incl - n;
+      for (int q = 0; q < n; ++q) p.ws.row_list[start + q] = r * G1 + (p.skip_dead ? pass : q);
+      __syncthreads();
+      if (tid == kPlanThreads - 1) carry = start + n;
+      __syncthreads();
     }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    int before = carry;
-    for (int w = 0; w < warp; ++w) before += warp_sum[w];
-    const int start = before + incl - n;
-    for (int q = 0; q < n; ++q) p.ws.row_list[start + q] = r * G1 + q;
-    __syncthreads();
-    if (tid == kPlanThreads - 1) carry = start + n;
-    __syncthreads();
   }
   if (tid == 0) *p.ws.n_rows = carry;
 }
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
   const unsigned long long units = (unsigned long long)(*p.ws.n_rows) * cpr;
   // A work unit: chunk c of row (r, j); row pointer L, entries [c0, c1).
   struct Unit {
-    int ok, c, r, j, l, c0, c1;
+    int ok, c, r, j, l, c0, c1, dead;
     const TT* L;
   };
   // per warp: the current unit, the one after it, and lane 0's issue state
@@ -308,6 +316,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
       d.L = reinterpret_cast<const TT*>(p.tgt) + target_row(p, d.r, d.j) * (size_t)V;
       d.c0 = d.c * kRowChunk;
       d.c1 = (long)d.c0 + kRowChunk < V ? d.c0 + kRowChunk : (int)V;
+      // a row past an end already found (a rejection, a mismatch) is not
+      // needed: its chunk is skipped (an empty range issues no copies)
+      if (p.skip_dead && (__ldcg(p.ws.term_mask + d.r) & ((1ull << (d.j - 1)) - 1ull))) {
+        d.dead = 1;
+        d.c1 = d.c0;
+      }
     }
     return d;
   };
@@ -537,6 +551,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
         if (lane == 0) issue_some();
       }
       if (__any_sync(0xffffffffu, failed)) break;
+      if (s_cur[warp].dead) goto next_unit;
       // warp merge of the unit, partial, and the row / request completion
       Partial w{};
       if (greedy) {
@@ -584,16 +599,36 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
         if (lane == 0) finish_row(p, r, j, l, acc, ks, L, sizeof(TT) == 2, bonus);
       }
       if (lane == 0) {
-        __threadfence();
-        const unsigned prev = atomicAdd(p.ws.req_cnt + r, 1u);
-        if (prev == (unsigned)l) {
-          p.ws.req_cnt[r] = 0u;
+        if (p.skip_dead) {
+          // The request ends at its first row that rejects (mismatches) or at
+          // row l + 1; it is resolved once every row up to that end is finished.
+          const unsigned long long bit = 1ull << (j - 1);
+          const int res = p.ws.row_res[rj];
+          const bool ends = (j == l + 1) || (greedy ? p.x[(size_t)r * p.gamma + (j - 1)] != res : res == 0);
+          if (ends) atomicOr(p.ws.term_mask + r, bit);
           __threadfence();
-          resolve_request(p, r, l);
+          const unsigned long long done = atomicOr(p.ws.done_mask + r, bit) | bit;
+          __threadfence();
+          const unsigned long long term = atomicOr(p.ws.term_mask + r, 0ull);
+          const int jend = __ffsll((long long)term);  // lowest ending row, 0: none yet
+          const unsigned long long need = jend >= 64 ? ~0ull : (1ull << jend) - 1ull;
+          if (jend > 0 && (done & need) == need && atomicExch(p.ws.req_cnt + r, 1u) == 0u) {
+            __threadfence();
+            resolve_request(p, r, l);
+          }
+        } else {
+          __threadfence();
+          const unsigned prev = atomicAdd(p.ws.req_cnt + r, 1u);
+          if (prev == (unsigned)l) {
+            p.ws.req_cnt[r] = 0u;
+            __threadfence();
+            resolve_request(p, r, l);
+          }
         }
       }
       }
     }
+  next_unit:
     // next unit; lane 0 moves its issue position into it
     __syncwarp();
     if (lane == 0) {
@@ -783,7 +818,8 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 // Scratch layout: arrays that need no initialisation first, then the
 // counters and flags that every call zeroes in one memset.
 enum { kRowPart, kResPart, kRowM, kRowS, kRowRes, kReqJstar, kResList, kRtPart, kRowList, kNRows,
-       kUnitCnt, kRowCnt, kReqCnt, kResCnt, kResNum, kRtCnt, kRtBest, kFallback, kLayoutN };
+       kUnitCnt, kDoneMask, kTermMask, kRowCnt, kReqCnt, kResCnt, kResNum, kRtCnt, kRtBest, kFallback,
+       kLayoutN };
 
 static size_t layout(int R, int gamma, int V, size_t off[kLayoutN]) {
   const size_t rows = (size_t)R * (gamma + 1);
@@ -793,7 +829,9 @@ static size_t layout(int R, int gamma, int V, size_t off[kLayoutN]) {
                                   rows * sizeof(float), rows * sizeof(float), rows * sizeof(int),
                                   (size_t)R * sizeof(int), (size_t)gamma * R * sizeof(int),
                                   mt * kResTileRows * kMaxDeviceSms * sizeof(Partial), rows * sizeof(int),
-                                  sizeof(int), sizeof(unsigned long long), rows * sizeof(unsigned), (size_t)R * sizeof(unsigned),
+                                  sizeof(int), sizeof(unsigned long long),
+                                  (size_t)R * sizeof(unsigned long long), (size_t)R * sizeof(unsigned long long),
+                                  rows * sizeof(unsigned), (size_t)R * sizeof(unsigned),
                                   (size_t)R * sizeof(unsigned), (size_t)gamma * sizeof(int),
                                   mt * sizeof(unsigned), (size_t)R * sizeof(unsigned),
                                   (size_t)R * sizeof(int)};
@@ -834,6 +872,8 @@ VerifyScratch verify_scratch_carve(void* base, int R, int gamma, int V, size_t* 
   s.rt_best = reinterpret_cast<unsigned*>(b + off[kRtBest]);
   s.fallback = reinterpret_cast<int*>(b + off[kFallback]);
   s.unit_cnt = reinterpret_cast<unsigned long long*>(b + off[kUnitCnt]);
+  s.done_mask = reinterpret_cast<unsigned long long*>(b + off[kDoneMask]);
+  s.term_mask = reinterpret_cast<unsigned long long*>(b + off[kTermMask]);
   *counters_offset = off[kUnitCnt];
   *counters_bytes = total - off[kUnitCnt];  // the counter block, to the end
   return s;

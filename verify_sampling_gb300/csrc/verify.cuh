@@ -31,6 +31,8 @@ struct VerifyScratch {
   unsigned* rt_best;  // [R]              }
   int* fallback;      // [R]              }
   unsigned long long* unit_cnt;  // [1] row-pass work counter }
+  unsigned long long* done_mask;  // [R] rows finished, bit j-1 }
+  unsigned long long* term_mask;  // [R] rows that end the request (reject, mismatch, last) }
 };
 
 struct VerifyParams {
@@ -61,6 +63,7 @@ struct VerifyParams {
   uint32_t* status;
   bool tc_residual;      // residual on the fused tensor-core kernel
   bool row_ring;         // row pass: per-warp bulk-copy rings in dynamic shared memory
+  bool skip_dead;        // rows in position order; rows past a request's end are skipped
   int device_sms;
   VerifyScratch ws;
 };
