@@ -442,6 +442,8 @@ def main():
                                        workspace=bufs["ws_verify"])
             if timed:
                 ev["v1"][i].record(stream)
+                acc_hist[i, 0].copy_(g["ell"], non_blocking=True)
+                acc_hist[i, 1].copy_(bufs["verify"]["accept_len"], non_blocking=True)
             return
         if timed:
             ev["d0"][i].record(stream)
@@ -516,10 +518,12 @@ def main():
     hbm, peak_kind = _peaks()
     es_u = 4 if wl.logit_dtype == torch.float32 else 2
     es_f = 4 if wl.fac_dtype == torch.float32 else 2
+    stage_bytes = _round_bytes(wl, to_cpu(acc_hist), args.steps)
     if greedy:
-        per_launch = R * (G + 1) * V * es_u
+        # the rows up to each request's first mismatch (or row l_r + 1)
+        per_launch = int(stage_bytes["verify"])
         dur_ms = ms / args.steps
-        kernel = "verify_rows (greedy argmax, all R*(gamma+1) rows)"
+        kernel = "verify_rows (greedy argmax; rows past a request's first mismatch skipped)"
         launches = 2  # row plan, row pass
     else:
         # dominant kernel: the draft step, gamma launches per round; one launch
@@ -550,7 +554,6 @@ def main():
                 "tensor_pipe_pct": tensor_pipe}
 
     # ---------------------------------------- round-level algorithmic bytes ----
-    stage_bytes = _round_bytes(wl, to_cpu(acc_hist), to_cpu(stats_hist), args.steps)
     round_bytes = sum(stage_bytes.values())
     stages = {}
     for k in ("draft", "schedule", "verify"):
@@ -601,29 +604,31 @@ def to_cpu(t):
     return t.cpu().numpy()
 
 
-def _round_bytes(wl, acc_hist, stats_hist, steps: int) -> dict:
+def _round_bytes(wl, acc_hist, steps: int) -> dict:
     """Algorithmic bytes of one round, per stage, averaged over the timed steps.
     draft: gamma launches of the R backbone rows and C_k, plus the confidence
-    head's hidden states and W1 rows; verify: the B scheduled target rows, and
-    for every request rejected at j*: its backbone row and target row at j*,
-    plus C_{j*} once per position that has a rejection (the residual pass)."""
+    head's hidden states and W1 rows; verify: the target rows a verifier must
+    read -- each request's rows up to its end, accept_len + 1 of them (its
+    first rejection or mismatch, or row l_r + 1) -- and, for every request
+    rejected at j*, its backbone row at j* plus C_{j*} once per position that
+    has a rejection (the residual pass)."""
     import numpy as np
     import torch
     es = lambda dt: 2 if dt == torch.bfloat16 else 4
     R, G, V, r = wl.R, wl.gamma, wl.V, wl.r
     e_u, e_f, e_c = es(wl.logit_dtype), es(wl.fac_dtype), es(wl.conf_dtype)
-    if wl.mode == "greedy":
-        return {"verify": R * (G + 1) * V * e_u}
-    draft = G * (R * V * e_u + V * r * e_f) + R * G * (wl.d + wl.e) * e_c
-    B = float(np.mean(stats_hist[:steps, 1]))
-    resid = 0.0
+    rows = resid = 0.0
     for i in range(steps):
         ell, acc = acc_hist[i, 0], acc_hist[i, 1]
-        rej = acc < ell
-        n_rej = int(rej.sum())
-        n_pos = len(np.unique(acc[rej] + 1))
-        resid += n_rej * V * 2 * e_u + n_pos * V * r * e_f
-    return {"draft": draft, "verify": B * V * e_u + resid / steps}
+        rows += float((acc + 1).sum())
+        if wl.mode != "greedy":
+            rej = acc < ell
+            resid += int(rej.sum()) * V * e_u + len(np.unique(acc[rej] + 1)) * V * r * e_f
+    verify = (rows * V * e_u + resid) / steps
+    if wl.mode == "greedy":
+        return {"verify": verify}
+    draft = G * (R * V * e_u + V * r * e_f) + R * G * (wl.d + wl.e) * e_c
+    return {"draft": draft, "verify": verify}
 
 
 def _link_gbs(torch, src, dev) -> float:
