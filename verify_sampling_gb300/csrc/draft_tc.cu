@@ -418,6 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         st.m += 64.f;
         nref -= 64.f;
         c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+        // the tile's weights move to the new reference too: the filter and the
+        // exact tests below compare them with the rescaled best
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = make_float2(e[i].x * 0x1p-64f, e[i].y * 0x1p-64f);
       }
       // Filter factor for the tile: the tighter of the thread's own best and
       // the best any thread of this row in the CTA has published.  An element
