@@ -345,12 +345,11 @@ int spec_calibration(const spec_calibration_args *args, spec_stream_t stream);
  * c* = 1 - TV(p, q) = sum_v min(p_v, q_v) for every verified draft row
  * j <= l_r (q recomputed from the draft arguments), NaN past l_r.  A
  * diagnostic: it costs one more pass over the admitted target and draft rows.
- * Rows read: the verifier needs a request's rows only up to its first
- * rejection (mismatch in greedy mode) or row l_r + 1.  With gamma <= 63, and
- * in sample mode when none of p_tok, lse_t and c_star is requested, rows are
- * taken in position order and a row past a request's end already found is
- * skipped (rows in flight when the end is found are still read); results
- * are the same either way.
+ * Rows read: greedy mode needs a request's rows only up to its first
+ * mismatch or row l_r + 1.  With gamma <= 63 its rows are taken in position
+ * order and a row past a request's end already found is skipped (rows in
+ * flight when the end is found are still read).  Sample mode reads every
+ * scheduled row.
  */
 typedef struct spec_verify_args {
   int mode;

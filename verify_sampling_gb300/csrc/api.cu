@@ -335,9 +335,10 @@ int spec_verify(const spec_verify_args* args, uint64_t seed, spec_stream_t strea
   p.lse_t = a.lse_t;
   p.c_star = a.c_star;
   p.status = a.status;
-  // Rows after a request's first rejection (mismatch) influence no output
-  // unless a per-row diagnostic (p_tok, lse_t, c*) asks for them.
-  p.skip_dead = a.gamma + 1 <= 64 && !(sample && (a.p_tok || a.lse_t || a.c_star));
+  // Greedy mode: rows after a request's first mismatch influence no output.
+  // (In sample mode the position order measured slower than the request order
+  // at c5 -- its bonus-row races form the tail -- so it keeps request order.)
+  p.skip_dead = !sample && a.gamma + 1 <= 64;
   {
     int dev = 0, major = 0, sms = 0;
     const bool dev_ok =
