@@ -585,8 +585,16 @@ def main():
 
     # ----------------------------------------------------- e2e (rank 0) ----
     if rank == 0 and not args.no_e2e and not greedy:
-        line["e2e"] = _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 8),
-                           cap_words=cap_words)
+        # one round at a time, and two in flight on two streams: which is faster
+        # depends on how the host link serves copy-engine transfers and the
+        # gather's loads at once (it differed between machines); both are
+        # measured and reported, the faster one as the value
+        runs = [_e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps=min(args.steps, 8),
+                     cap_words=cap_words, in_flight=n) for n in (1, 2)]
+        best = min(runs, key=lambda e: e["ms_per_step"])
+        best["ms_per_step_by_rounds_in_flight"] = {str(e["rounds_in_flight"]): e["ms_per_step"]
+                                                   for e in runs}
+        line["e2e"] = best
     if rank == 0 and not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl)
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(wl)
@@ -645,7 +653,8 @@ def _link_gbs(torch, src, dev) -> float:
     return src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1000.0) / 1e9
 
 
-def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None) -> dict:
+def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None,
+         in_flight: int = 2) -> dict:
     """Same round through the public API (one spec_round_host call per step)
     with the per-step inputs taken from pinned host memory and the results
     (tokens, lengths, stats) copied back; the model weights (A, Ct, W1, w) stay
@@ -654,17 +663,18 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None)
     schedule admits are read -- the rows a target model computes for the
     round -- by the library's gather from the mapped host buffer.
 
-    Two rounds are in flight, on two streams with their own device buffers:
-    while one round computes, the next one's inputs cross the link.  Step i's
-    results are read on the host before step i + 2 reuses its buffers."""
+    `in_flight` rounds are in flight, on as many streams with their own device
+    buffers: while one round computes, the next one's inputs cross the link.
+    Step i's results are read on the host before step i + in_flight reuses
+    its buffers."""
     names = ["U", "h", "x0", "tgt"]
     host = {n: g[n].cpu().pin_memory() for n in names}
     whole = sum(host[n].numel() * host[n].element_size() for n in ("U", "h", "x0"))
     row_bytes = wl.V * host["tgt"].element_size()
     R, G, V = wl.R, wl.gamma, wl.V
-    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(in_flight)]
     sets = []
-    for _ in range(2):
+    for _ in range(in_flight):
         devb = {n: torch.empty_like(g[n]) for n in names}
         outs = {"out_tok": torch.empty(R, G + 1, dtype=torch.int32).pin_memory(),
                 "accept_len": torch.empty(R, dtype=torch.int32).pin_memory(),
@@ -689,31 +699,31 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None)
 
     def issue(i):
         # one C-ABI call: host inputs in, host results out (asynchronous)
-        devb, outs, d_in, b = sets[i % 2]
+        devb, outs, d_in, b = sets[i % in_flight]
         vs.run_round_host(d_in, devb["tgt"].view(-1, V), g["tgt_row_off"], g["sps"], g["b_lo"],
                           g["b_step"], wl.K, 9000 + i, host_in=host, host_out=outs,
                           sched_mode=wl.sched_mode, sched_threshold=wl.sched_threshold,
                           tgt_scheduled_only=True,
                           K_dev=None if cap_words is None else cap_words[i % 2: i % 2 + 1],
                           n_free=None if cap_words is None else cap_words[i % 2: i % 2 + 1],
-                          bufs=b, stream=streams[i % 2])
+                          bufs=b, stream=streams[i % in_flight])
 
     def collect(i):
-        streams[i % 2].synchronize()
-        B = float(sets[i % 2][1]["stats"][1])
+        streams[i % in_flight].synchronize()
+        B = float(sets[i % in_flight][1]["stats"][1])
         return R * G + B, B
 
-    issue(0)
-    issue(1)
-    collect(0)
-    collect(1)  # warm-up
+    for i in range(in_flight):  # warm-up
+        issue(i)
+    for i in range(in_flight):
+        collect(i)
     t0 = time.perf_counter()
     res = []
     for i in range(steps):
-        if i >= 2:
-            res.append(collect(i - 2))
+        if i >= in_flight:
+            res.append(collect(i - in_flight))
         issue(i)
-    for i in range(max(0, steps - 2), steps):
+    for i in range(max(0, steps - in_flight), steps):
         res.append(collect(i))
     sec = time.perf_counter() - t0
     pos = sum(p for p, _ in res)
@@ -722,7 +732,7 @@ def _e2e(wl, g, din, vs, torch, dev, bufs, rid_base, steps: int, cap_words=None)
     link = _link_gbs(torch, host["U"], dev)
     return {"value": pos / sec, "unit": "positions/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "rounds_in_flight": 2, "ms_per_step": round(1000.0 * sec / steps, 3),
+            "rounds_in_flight": in_flight, "ms_per_step": round(1000.0 * sec / steps, 3),
             # one pinned copy of U's size, timed right after: the link's own rate,
             # and the step time that rate alone would give for the step's bytes
             "link_gbs": round(link, 1), "link_floor_ms": round(h2d / (link * 1e9) * 1000.0, 3),
