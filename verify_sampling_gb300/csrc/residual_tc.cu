@@ -408,7 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float res[8];  // p - q of the 8 columns
 #pragma unroll
       for (int i = 0; i < 8; ++i) res[i] = tc::ex2(fmaf(L[i], kt, nt)) * inv_s - qv[i];
-      const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
       // Both Philox blocks and the filter of the 8 columns in one straight-line
       // block; one branch to the rare exact tests.
       uint32_t words[8];
@@ -420,6 +419,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         words[4 * q + 2] = bits.z;
         words[4 * q + 3] = bits.w;
       }
+      if (!(c_res < CUDART_INF_F)) {
+        // No own candidate yet: seed the race with the largest positive residual
+        // of these 8 columns (one exact test), so that the filter has a bound
+        // from the first tile on instead of sending every element of it to the
+        // exact test.  The seed is an element of the race like any other.
+        float rm = 0.f;
+        int im = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (res[i] > rm && colbase + i < V) {
+            rm = res[i];
+            im = i;
+          }
+        if (im >= 0) {
+          uint32_t wm = words[0];
+#pragma unroll
+          for (int j = 1; j < 8; ++j) wm = (im == j) ? words[j] : wm;
+          const float E = -logf(uniform_from_word(wm));
+          if (race_beats(rm, E, colbase + im, rres.bw, rres.bE, rres.idx)) {
+            rres = WRace{rm, E, colbase + im};
+            c_res = __fdividef(E, rm) * kFilterUp;
+            atomicMax(row_best, ordered_key(lg2(rm) - lg2(E) - kPublishMargin));
+          }
+        }
+      }
+      const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
       uint32_t mask = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
