@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
   __shared__ int s_tile[5];  // M, k, first list index, rows, splits
   __shared__ int s_req[128];
+  __shared__ uint32_t s_rbest[kResTileRows];  // per request slot: best published score (ordered key)
   __shared__ int s_trow[128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     s_req[i] = r;
     s_trow[i] = trow;
+    if (i < kResTileRows) s_rbest[i] = 0u;
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < Sc; ++s) {
@@ -363,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const uint32_t shared_now = shared_key;
+      // the request's bound: the CTA's own best so far (shared memory, every
+      // candidate of the tile's 32 thread streams raises it at once) and the
+      // best of all CTAs (global, read one own tile late)
+      const uint32_t shared_now = max(shared_key, *reinterpret_cast<volatile uint32_t*>(&s_rbest[slot]));
       if (!kCStar && valid) shared_key = __ldcg(row_best);
       if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs)) {
         fail();
@@ -440,7 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (race_beats(rm, E, colbase + im, rres.bw, rres.bE, rres.idx)) {
             rres = WRace{rm, E, colbase + im};
             c_res = __fdividef(E, rm) * kFilterUp;
-            atomicMax(row_best, ordered_key(lg2(rm) - lg2(E) - kPublishMargin));
+            const uint32_t key = ordered_key(lg2(rm) - lg2(E) - kPublishMargin);
+            atomicMax(&s_rbest[slot], key);
+            atomicMax(row_best, key);
           }
         }
       }
@@ -465,7 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (race_beats(ri, E, colbase + i, rres.bw, rres.bE, rres.idx)) {
             rres = WRace{ri, E, colbase + i};
             c_res = __fdividef(E, ri) * kFilterUp;
-            atomicMax(row_best, ordered_key(lg2(ri) - lg2(E) - kPublishMargin));
+            const uint32_t key = ordered_key(lg2(ri) - lg2(E) - kPublishMargin);
+            atomicMax(&s_rbest[slot], key);
+            atomicMax(row_best, key);
           }
         }
       }
