@@ -408,73 +408,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 8; ++c)
           if (colbase + c < V) part += fminf(tc::ex2(fmaf(L[c], kt, nt)) * inv_s, qv[c]);
         csum += part;
-        continue;
-      }
-      float res[8];  // p - q of the 8 columns
+      } else {
+        float res[8];  // p - q of the 8 columns
 #pragma unroll
-      for (int i = 0; i < 8; ++i) res[i] = tc::ex2(fmaf(L[i], kt, nt)) * inv_s - qv[i];
-      // Both Philox blocks and the filter of the 8 columns in one straight-line
-      // block; one branch to the rare exact tests.
-      uint32_t words[8];
+        for (int i = 0; i < 8; ++i) res[i] = tc::ex2(fmaf(L[i], kt, nt)) * inv_s - qv[i];
+        // Both Philox blocks and the filter of the 8 columns in one straight-line
+        // block; one branch to the rare exact tests.
+        uint32_t words[8];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint4 bits = philox_in_row((uint32_t)((colbase >> 2) + q), prow, p.rk);
-        words[4 * q] = bits.x;
-        words[4 * q + 1] = bits.y;
-        words[4 * q + 2] = bits.z;
-        words[4 * q + 3] = bits.w;
-      }
-      if (!(c_res < CUDART_INF_F)) {
-        // No own candidate yet: seed the race with the largest positive residual
-        // of these 8 columns (one exact test), so that the filter has a bound
-        // from the first tile on instead of sending every element of it to the
-        // exact test.  The seed is an element of the race like any other.
-        float rm = 0.f;
-        int im = -1;
+        for (int q = 0; q < 2; ++q) {
+          const uint4 bits = philox_in_row((uint32_t)((colbase >> 2) + q), prow, p.rk);
+          words[4 * q] = bits.x;
+          words[4 * q + 1] = bits.y;
+          words[4 * q + 2] = bits.z;
+          words[4 * q + 3] = bits.w;
+        }
+        if (!(c_res < CUDART_INF_F)) {
+          // No own candidate yet: seed the race with the largest positive residual
+          // of these 8 columns (one exact test), so that the filter has a bound
+          // from the first tile on instead of sending every element of it to the
+          // exact test.  The seed is an element of the race like any other.
+          float rm = 0.f;
+          int im = -1;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (res[i] > rm && colbase + i < V) {
-            rm = res[i];
-            im = i;
-          }
-        if (im >= 0) {
-          uint32_t wm = words[0];
+          for (int i = 0; i < 8; ++i)
+            if (res[i] > rm && colbase + i < V) {
+              rm = res[i];
+              im = i;
+            }
+          if (im >= 0) {
+            uint32_t wm = words[0];
 #pragma unroll
-          for (int j = 1; j < 8; ++j) wm = (im == j) ? words[j] : wm;
-          const float E = -logf(uniform_from_word(wm));
-          if (race_beats(rm, E, colbase + im, rres.bw, rres.bE, rres.idx)) {
-            rres = WRace{rm, E, colbase + im};
-            c_res = __fdividef(E, rm) * kFilterUp;
-            const uint32_t key = ordered_key(lg2(rm) - lg2(E) - kPublishMargin);
-            atomicMax(&s_rbest[slot], key);
-            atomicMax(row_best, key);
+            for (int j = 1; j < 8; ++j) wm = (im == j) ? words[j] : wm;
+            const float E = -logf(uniform_from_word(wm));
+            if (race_beats(rm, E, colbase + im, rres.bw, rres.bE, rres.idx)) {
+              rres = WRace{rm, E, colbase + im};
+              c_res = __fdividef(E, rm) * kFilterUp;
+              const uint32_t key = ordered_key(lg2(rm) - lg2(E) - kPublishMargin);
+              atomicMax(&s_rbest[slot], key);
+              atomicMax(row_best, key);
+            }
           }
         }
-      }
-      const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
-      uint32_t mask = 0;
+        const float cr = fminf(c_res, tc::ex2(-key_value(shared_now)) * kFilterUp);  // NaN: none yet
+        uint32_t mask = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        mask |= (one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f) && res[i] > 0.f) ? (1u << i) : 0u;
-      if (mask) {  // rare: exact race tests, in index order
-        if (colbase + 8 > V) mask &= (V > colbase) ? (1u << (V - colbase)) - 1u : 0u;
-        while (mask) {
-          const int i = __ffs(mask) - 1;
-          mask &= mask - 1u;
-          float ri = res[0];
-          uint32_t wi = words[0];
+        for (int i = 0; i < 8; ++i)
+          mask |= (one_plus_w(words[i]) <= fmaf(res[i], cr, 1.0f) && res[i] > 0.f) ? (1u << i) : 0u;
+        if (mask) {  // rare: exact race tests, in index order
+          if (colbase + 8 > V) mask &= (V > colbase) ? (1u << (V - colbase)) - 1u : 0u;
+          while (mask) {
+            const int i = __ffs(mask) - 1;
+            mask &= mask - 1u;
+            float ri = res[0];
+            uint32_t wi = words[0];
 #pragma unroll
-          for (int j = 1; j < 8; ++j) {
-            ri = (i == j) ? res[j] : ri;
-            wi = (i == j) ? words[j] : wi;
-          }
-          const float E = -logf(uniform_from_word(wi));
-          if (race_beats(ri, E, colbase + i, rres.bw, rres.bE, rres.idx)) {
-            rres = WRace{ri, E, colbase + i};
-            c_res = __fdividef(E, ri) * kFilterUp;
-            const uint32_t key = ordered_key(lg2(ri) - lg2(E) - kPublishMargin);
-            atomicMax(&s_rbest[slot], key);
-            atomicMax(row_best, key);
+            for (int j = 1; j < 8; ++j) {
+              ri = (i == j) ? res[j] : ri;
+              wi = (i == j) ? words[j] : wi;
+            }
+            const float E = -logf(uniform_from_word(wi));
+            if (race_beats(ri, E, colbase + i, rres.bw, rres.bE, rres.idx)) {
+              rres = WRace{ri, E, colbase + i};
+              c_res = __fdividef(E, ri) * kFilterUp;
+              const uint32_t key = ordered_key(lg2(ri) - lg2(E) - kPublishMargin);
+              atomicMax(&s_rbest[slot], key);
+              atomicMax(row_best, key);
+            }
           }
         }
       }
