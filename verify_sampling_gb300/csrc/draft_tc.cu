@@ -337,10 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&tempty[rb.idx]);
-        tc::mbar_arrive(&empty_s[r.idx]);
-      }
+      tc::mbar_arrive2_if(&tempty[rb.idx], &empty_s[r.idx], lane == 0);
       if (!valid) continue;
       const int colbase = (t_begin + t) * kNT + grp * 16;
       float2 z[8];  // U + bias (the temperature is folded into kscale)
@@ -354,29 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (colbase + 2 * i >= V) z[i].x = -CUDART_INF_F;
           if (colbase + 2 * i + 1 >= V) z[i].y = -CUDART_INF_F;
         }
-      }
-      // First tile of the row: fix the reference at the tile's maximum and seed
-      // the race with that element (without a bound every element of the
-      // first tile would take the exact test).  Its e is computed exactly as
-      // the streaming pass below computes it.
-      if (!(st.m > -CUDART_INF_F)) {
-        float mz = z[0].x;
-        int im = 0;
-#pragma unroll
-        for (int j = 1; j < 16; ++j) {
-          const float zj = (j & 1) ? z[j >> 1].y : z[j >> 1].x;
-          if (zj > mz) {
-            mz = zj;
-            im = j;
-          }
-        }
-        if (!(mz > -CUDART_INF_F)) continue;
-        st.m = mz * kscale;
-        nref = -st.m;
-        const uint4 bits = philox_in_row((uint32_t)(colbase >> 2) + (uint32_t)(im >> 2), prow, p.rk);
-        if (race_candidate(st, tc::ex2(fmaf(mz, kscale, nref)), word_of(bits, im & 3), colbase + im,
-                           row_best, *reinterpret_cast<volatile uint32_t*>(row_best), global_best))
-          c_own = __fdividef(st.bE, st.be) * kFilterUp;
       }
       // e = 2^(z kscale - ref) for the 16 columns and their sum (a tree)
       float2 e[8];
@@ -393,35 +367,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 4; ++i) s4[i] = __fadd2_rn(e[2 * i], e[2 * i + 1]);
       const float2 s2 = __fadd2_rn(__fadd2_rn(s4[0], s4[1]), __fadd2_rn(s4[2], s4[3]));
       float ts = s2.x + s2.y;
-      if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
-        float mz = fmaxf(z[0].x, z[0].y);
+      // Rare: the row's first tile (no reference yet: the weights above were
+      // taken against 0 and are redone), a logit far above the reference, or
+      // a running sum about to grow too large; one test for all three.
+      if (!(st.m > -CUDART_INF_F) || !(ts <= 1e37f) || st.s + ts > 1e30f) {
+        if (!(st.m > -CUDART_INF_F)) {
+          // First tile of the row: fix the reference at the tile's maximum and
+          // seed the race with that element (without a bound every element of
+          // the first tile would take the exact test).  Its e is computed
+          // exactly as the tile's weights are.
+          float mz = z[0].x;
+          int im = 0;
 #pragma unroll
-        for (int i = 1; i < 8; ++i) mz = fmaxf(mz, fmaxf(z[i].x, z[i].y));
-        const float mnew = fmaxf(mz * kscale, st.m);
-        const float sc = tc::ex2(st.m - mnew);
-        st.s *= sc;
-        st.be *= sc;
-        st.m = mnew;
-        nref = -mnew;
-        c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
-        ts = 0.f;
+          for (int j = 1; j < 16; ++j) {
+            const float zj = (j & 1) ? z[j >> 1].y : z[j >> 1].x;
+            if (zj > mz) {
+              mz = zj;
+              im = j;
+            }
+          }
+          if (!(mz > -CUDART_INF_F)) continue;
+          st.m = mz * kscale;
+          nref = -st.m;
+          const uint4 bits = philox_in_row((uint32_t)(colbase >> 2) + (uint32_t)(im >> 2), prow, p.rk);
+          if (race_candidate(st, tc::ex2(fmaf(mz, kscale, nref)), word_of(bits, im & 3), colbase + im,
+                             row_best, *reinterpret_cast<volatile uint32_t*>(row_best), global_best))
+            c_own = __fdividef(st.bE, st.be) * kFilterUp;
+          // the tile's weights and their sum against the new reference
+          ts = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          e[i] = make_float2(tc::ex2(fmaf(z[i].x, kscale, nref)), tc::ex2(fmaf(z[i].y, kscale, nref)));
-          ts += e[i].x + e[i].y;
+          for (int i = 0; i < 8; ++i) {
+            e[i] = make_float2(tc::ex2(fmaf(z[i].x, kscale, nref)), tc::ex2(fmaf(z[i].y, kscale, nref)));
+            ts += e[i].x + e[i].y;
+          }
+        } else if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
+          float mz = fmaxf(z[0].x, z[0].y);
+#pragma unroll
+          for (int i = 1; i < 8; ++i) mz = fmaxf(mz, fmaxf(z[i].x, z[i].y));
+          const float mnew = fmaxf(mz * kscale, st.m);
+          const float sc = tc::ex2(st.m - mnew);
+          st.s *= sc;
+          st.be *= sc;
+          st.m = mnew;
+          nref = -mnew;
+          c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+          ts = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            e[i] = make_float2(tc::ex2(fmaf(z[i].x, kscale, nref)), tc::ex2(fmaf(z[i].y, kscale, nref)));
+            ts += e[i].x + e[i].y;
+          }
         }
-      }
-      st.s += ts;
-      if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
-        st.s *= 0x1p-64f;
-        st.be *= 0x1p-64f;
-        st.m += 64.f;
-        nref -= 64.f;
-        c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
-        // the tile's weights move to the new reference too: the filter and the
-        // exact tests below compare them with the rescaled best
+        st.s += ts;
+        if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
+          st.s *= 0x1p-64f;
+          st.be *= 0x1p-64f;
+          st.m += 64.f;
+          nref -= 64.f;
+          c_own = st.be > 0.f ? (st.bE / st.be) * kFilterUp : CUDART_INF_F;
+          // the tile's weights move to the new reference too: the filter and the
+          // exact tests below compare them with the rescaled best
 #pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = make_float2(e[i].x * 0x1p-64f, e[i].y * 0x1p-64f);
+          for (int i = 0; i < 8; ++i) e[i] = make_float2(e[i].x * 0x1p-64f, e[i].y * 0x1p-64f);
+        }
+      } else {
+        st.s += ts;
       }
       // Filter factor for the tile: the tighter of the thread's own best and
       // the best any thread of this row in the CTA has published.  An element

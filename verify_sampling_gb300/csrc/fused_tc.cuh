@@ -119,18 +119,18 @@ __device__ __forceinline__ void load_u16(const unsigned char* tile, const uint32
                                          float (&u)[16], float) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float4 f = *reinterpret_cast<const float4*>(tile + off[j]);
-    u[4 * j] = f.x;
-    u[4 * j + 1] = f.y;
-    u[4 * j + 2] = f.z;
-    u[4 * j + 3] = f.w;
+    const uint4 f = tc::lds128(tile + off[j]);
+    u[4 * j] = __uint_as_float(f.x);
+    u[4 * j + 1] = __uint_as_float(f.y);
+    u[4 * j + 2] = __uint_as_float(f.z);
+    u[4 * j + 3] = __uint_as_float(f.w);
   }
 }
 __device__ __forceinline__ void load_u16(const unsigned char* tile, const uint32_t (&off)[4],
                                          float (&u)[16], __nv_bfloat16) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const uint4 q = *reinterpret_cast<const uint4*>(tile + off[j]);
+    const uint4 q = tc::lds128(tile + off[j]);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {

@@ -15,6 +15,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// 16-byte load from shared memory through its shared-window address.
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -33,6 +42,16 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Two arrivals (on a and on b) by the threads whose `pred` is set, without a
+// branch around them.
+__device__ __forceinline__ void mbar_arrive2_if(uint64_t* a, uint64_t* b, bool pred) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %2, 0;\n"
+      " @p mbarrier.arrive.shared::cta.b64 _, [%0];\n"
+      " @p mbarrier.arrive.shared::cta.b64 _, [%1];\n}\n" ::"r"(smem_u32(a)),
+      "r"(smem_u32(b)), "r"((uint32_t)pred)
+      : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
