@@ -474,13 +474,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (mask) {
           const int i = __ffs(mask) - 1;
           mask &= mask - 1u;
-          float ei = e[0].x;
-          uint32_t wi = words[0];
+          // column i's weight and word by a select tree on the bits of i
+          float e8[8], e4[4], e2[2];
+          uint32_t w8[8], w4[4], w2[2];
 #pragma unroll
-          for (int j = 1; j < 16; ++j) {
-            ei = (i == j) ? ((j & 1) ? e[j >> 1].y : e[j >> 1].x) : ei;
-            wi = (i == j) ? words[j] : wi;
+          for (int j = 0; j < 8; ++j) {
+            e8[j] = (i & 1) ? e[j].y : e[j].x;
+            w8[j] = (i & 1) ? words[2 * j + 1] : words[2 * j];
           }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            e4[j] = (i & 2) ? e8[2 * j + 1] : e8[2 * j];
+            w4[j] = (i & 2) ? w8[2 * j + 1] : w8[2 * j];
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            e2[j] = (i & 4) ? e4[2 * j + 1] : e4[2 * j];
+            w2[j] = (i & 4) ? w4[2 * j + 1] : w4[2 * j];
+          }
+          const float ei = (i & 8) ? e2[1] : e2[0];
+          const uint32_t wi = (i & 8) ? w2[1] : w2[0];
           if (race_candidate(st, ei, wi, colbase + i, row_best, *reinterpret_cast<volatile uint32_t*>(row_best),
                              global_best)) {
             c_own = __fdividef(st.bE, st.be) * kFilterUp;

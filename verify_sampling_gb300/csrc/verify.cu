@@ -464,36 +464,40 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
             const float2 t = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
             ts = t.x + t.y;
           }
-          if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
-            float mz = x[0];
+          if (!(ts <= 1e37f) || st.s + ts > 1e30f) {  // rare: one test for both guards below
+            if (!(ts <= 1e37f)) {  // a logit far above the reference (or a NaN): re-reference
+              float mz = x[0];
 #pragma unroll
-            for (int q = 1; q < 8; ++q) mz = fmaxf(mz, x[q]);
-            const float mnew = fmaxf(mz * ks, st.m);
-            const float sc = tc::ex2(st.m - mnew);
-            st.s *= sc;
-            st.be *= sc;
-            st.m = mnew;
-            if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
-            cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
-            ts = 0.f;
+              for (int q = 1; q < 8; ++q) mz = fmaxf(mz, x[q]);
+              const float mnew = fmaxf(mz * ks, st.m);
+              const float sc = tc::ex2(st.m - mnew);
+              st.s *= sc;
+              st.be *= sc;
+              st.m = mnew;
+              if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
+              cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
+              ts = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              e[q] = make_float2(tc::ex2(fmaf(x[2 * q], ks, -st.m)), tc::ex2(fmaf(x[2 * q + 1], ks, -st.m)));
-              ts += e[q].x + e[q].y;
+              for (int q = 0; q < 4; ++q) {
+                e[q] = make_float2(tc::ex2(fmaf(x[2 * q], ks, -st.m)), tc::ex2(fmaf(x[2 * q + 1], ks, -st.m)));
+                ts += e[q].x + e[q].y;
+              }
             }
-          }
-          st.s += ts;
-          if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
-            st.s *= 0x1p-64f;
-            st.be *= 0x1p-64f;
-            st.m += 64.f;
-            if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
-            cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
+            st.s += ts;
+            if (st.s > 1e30f) {  // keep the sum far from overflow: exact rescale by 2^-64
+              st.s *= 0x1p-64f;
+              st.be *= 0x1p-64f;
+              st.m += 64.f;
+              if (st.be > 0.f) c_own = (st.bE / st.be) * fused::kFilterUp;
+              cf = fminf(c_own, tc::ex2(st.m - gbest) * fused::kFilterUp);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              e[q].x *= 0x1p-64f;
-              e[q].y *= 0x1p-64f;
+              for (int q = 0; q < 4; ++q) {
+                e[q].x *= 0x1p-64f;
+                e[q].y *= 0x1p-64f;
+              }
             }
+          } else {
+            st.s += ts;
           }
           if (!bonus) continue;
           // ---- bonus race over this group ----
