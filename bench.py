@@ -30,7 +30,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -125,6 +125,13 @@ def _peaks():
 
 
 class ClockSampler:
+    """nvidia-smi sampling SM clocks and throttle reasons every 10 ms.  It is
+    started before the warm-up steps (so that it is running when the timed
+    region starts) and keeps only the samples whose timestamps fall inside the
+    timed region's wall-clock window."""
+
+    INTERVAL_MS = 10
+
     def __init__(self, gpu_index: int):
         self.proc = None
         import tempfile
@@ -133,22 +140,27 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_QUERY}", "--format=csv",
-                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.INTERVAL_MS)], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
             self.f.close()
             os.remove(self.path)
 
-    def stop(self):
+    def stop(self, t_start, t_end):
+        """Samples taken between the datetimes t_start and t_end (local time,
+        as nvidia-smi stamps them); the first one after t_start if the window
+        holds none."""
         if self.proc is None:
             return None
+        time.sleep(2.5 * self.INTERVAL_MS / 1000.0)  # let the sample after t_end arrive
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        import datetime
+        rows = []
         with open(self.path) as f:
             lines = f.read().strip().splitlines()[1:]
         try:
@@ -157,20 +169,30 @@ class ClockSampler:
             pass
         for ln in lines:
             c = [x.strip() for x in ln.split(",")]
-            if len(c) < 9:
+            if len(c) < 10:
                 continue
             try:
-                sm.append(float(c[1].split()[0]))
-                mx.append(float(c[2].split()[0]))
+                ts = datetime.datetime.strptime(c[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(c[2].split()[0]), float(c[3].split()[0]), c))
             except ValueError:
                 continue
-            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6),
-                              ("sw_thermal_slowdown", 7), ("sw_power_cap", 8)):
+        inside = [r for r in rows if t_start <= r[0] <= t_end]
+        if not inside:
+            inside = [r for r in rows if r[0] >= t_start][:1]
+        if not inside:
+            return None
+        sm = [r[1] for r in inside]
+        mx = [r[2] for r in inside]
+        reasons = set()
+        for r in inside:
+            c = r[3]
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7),
+                              ("sw_thermal_slowdown", 8), ("sw_power_cap", 9)):
                 if c[col].lower().startswith("active"):
                     reasons.add(name)
-        if not sm:
-            return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "interval_ms": self.INTERVAL_MS,
+                "window_ms": round((t_end - t_start).total_seconds() * 1000.0, 1),
                 "reasons": sorted(reasons)}
 
 
@@ -473,25 +495,33 @@ def main():
             acc_hist[i, 0].copy_(s["ell"], non_blocking=True)
             acc_hist[i, 1].copy_(v["accept_len"], non_blocking=True)
 
-    for i in range(args.warmup):
-        step(-1 - i, False)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    import datetime
     clocks = ClockSampler(local) if rank == 0 else None
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(args.steps):
-        if flush is not None:  # evict the previous step's inputs (not timed)
-            flush.zero_()
-        step(i, True)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    try:
+        for i in range(args.warmup):
+            step(-1 - i, False)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        wall0 = datetime.datetime.now()
+        t0.record(stream)
+        for i in range(args.steps):
+            if flush is not None:  # evict the previous step's inputs (not timed)
+                flush.zero_()
+            step(i, True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        wall1 = datetime.datetime.now()
+    except BaseException:
+        if clocks is not None and clocks.proc is not None:
+            clocks.proc.kill()
+        raise
     if world > 1:
         dist.barrier()
-    clk = clocks.stop() if clocks else None
+    clk = clocks.stop(wall0, wall1) if clocks else None
     stage_ms = {"draft": 0.0, "schedule": 0.0, "verify": 0.0}
     step_ms = 0.0
     for i in range(args.steps):

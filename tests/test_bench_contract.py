@@ -64,3 +64,49 @@ def test_workload_options():
             bench._workload(args(config="greedy", **kw))
     with pytest.raises(SystemExit):
         bench._workload(args(async_cap=True, static_cap=True))
+
+
+def test_clock_sampler_keeps_the_timed_window(monkeypatch):
+    """The clock record holds only the samples stamped inside the timed
+    region, and reports the throttle reasons seen there (a stand-in for
+    nvidia-smi writes the CSV)."""
+    import datetime
+    sys.path.insert(0, ROOT)
+    import bench
+
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5, 100000)
+    t1 = t0 + datetime.timedelta(milliseconds=40)
+
+    def row(dt, mhz, reason):
+        stamp = dt.strftime("%Y/%m/%d %H:%M:%S.") + f"{dt.microsecond // 1000:03d}"
+        return (f"{stamp}, 0, {mhz} MHz, 2070 MHz, 600.00 W, 0x0, Not Active, Not Active, Not Active, "
+                f"{reason}\n")
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+        def kill(self):
+            pass
+
+    def fake_popen(cmd, stdout=None, stderr=None):
+        assert cmd[0] == "nvidia-smi" and "-lms" in cmd
+        stdout.write("timestamp, index, clocks.current.sm [MHz], ...\n")
+        stdout.write(row(t0 - datetime.timedelta(milliseconds=30), 900, "Not Active"))  # idle, before
+        for i, mhz in enumerate((2070, 2055, 2040)):
+            stdout.write(row(t0 + datetime.timedelta(milliseconds=5 + 10 * i), mhz,
+                             "Active" if i == 1 else "Not Active"))
+        stdout.write(row(t1 + datetime.timedelta(milliseconds=8), 1000, "Not Active"))  # after
+        stdout.flush()
+        return FakeProc()
+
+    monkeypatch.setattr(bench.subprocess, "Popen", fake_popen)
+    clk = bench.ClockSampler(0).stop(t0, t1)
+    assert clk["samples"] == 3 and clk["sm_mhz"] == 2055.0 and clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["sw_power_cap"] and clk["interval_ms"] == 10 and clk["window_ms"] == 40.0
+    # a window shorter than the interval takes the first sample after its start
+    clk = bench.ClockSampler(0).stop(t0, t0 + datetime.timedelta(milliseconds=1))
+    assert clk["samples"] == 1 and clk["sm_mhz"] == 2070.0
