@@ -104,8 +104,10 @@ __device__ __forceinline__ bool race_candidate(Race& st, float e, uint32_t word,
 
 using namespace fused;
 
-template <typename TL, int KC>
-// 576 threads per CTA leave at most 96 registers per thread.
+// kIdleWarps: R is not a multiple of 128, so a lane quadrant of the last
+// request tile may lie wholly past R (such a warp only keeps the pipeline
+// going).  576 threads per CTA leave at most 96 registers per thread.
+template <typename TL, int KC, bool kIdleWarps>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_tc_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_c,
                     DraftTCParams p) {
@@ -312,14 +314,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     float nref = 0.f;  // -st.m once the reference is set
     const PhiloxRow prow = philox_row((uint32_t)k, p.rid_base + (uint32_t)m, kPurposeDraft, p.rk);
     uint32_t* row_best = &s_best[row];
-    unsigned* global_best = p.row_best + (size_t)(k - 1) * p.R + (valid ? m : 0);
+    // rows past R race on zeros like any other row (their results are never
+    // written); their publications go to their own shared word only
+    unsigned* global_best = valid ? p.row_best + (size_t)(k - 1) * p.R + m : row_best;
     uint32_t global_seen = 0;  // one thread per row imports the global bound, one tile late
     uint32_t uoff[4];
     u_offsets(row, grp, uoff, TL());
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * 16);
     Ring r{0, 0u}, rb{0, 0u};
-    for (int t = 0; t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
-      if (abort_flag) break;
+    // (no abort test in these loops: every wait is bounded, and a failed one
+    // ends the loop)
+    bool warp_idle = false;
+    if constexpr (kIdleWarps) {
+      warp_idle = !__any_sync(0xffffffffu, valid);
+      for (int t = 0; warp_idle && t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
+        if (!tc::mbar_wait(&tfull[rb.idx], rb.phase, kWaitNs) ||
+            !tc::mbar_wait(&full_u[r.idx], r.phase, kWaitNs)) {
+          fail();
+          break;
+        }
+        __syncwarp();
+        tc::mbar_arrive2_if(&tempty[rb.idx], &empty_s[r.idx], lane == 0);
+      }
+    }
+    for (int t = 0; !warp_idle && t < T; ++t, r.next(S), rb.next(kTmemBufs)) {
       if (grp == 0 && valid) {  // the row's bound from the other CTAs (loaded last tile)
         if (global_seen) atomicMax(row_best, global_seen);
         global_seen = __ldcg(global_best);
@@ -338,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       tc::mbar_arrive2_if(&tempty[rb.idx], &empty_s[r.idx], lane == 0);
-      if (!valid) continue;
       const int colbase = (t_begin + t) * kNT + grp * 16;
       float2 z[8];  // U + bias (the temperature is folded into kscale)
 #pragma unroll
@@ -571,7 +588,7 @@ cudaError_t launch_typed(const DraftTCParams& base, const void* U, const void* C
   p.rk = philox_round_keys(p.key);
   p.stages = pick_stages<TL, KC>();
   const size_t smem = smem_bytes<TL, KC>(p.stages);
-  auto kern = draft_tc_kernel<TL, KC>;
+  auto kern = (p.R % 128 != 0) ? draft_tc_kernel<TL, KC, true> : draft_tc_kernel<TL, KC, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
