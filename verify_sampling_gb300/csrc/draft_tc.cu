@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       // two 16-column halves; the tile's TMEM and U stage are released once
       // the second half is loaded
-#pragma unroll 1
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t uoff[4];
         u_offsets(row, (grp & 1) * 2 + h, uoff, TL());
