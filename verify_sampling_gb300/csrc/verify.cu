@@ -540,19 +540,23 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_rows_kernel(VerifyPa
         }
       };
       for (int b0 = c0; b0 < c1; b0 += kBatch) {
-        if (!bulk) {
-          batch(b0, nullptr);
-          continue;
+        // one call site, so that the batch code is inlined once
+        const unsigned char* sx = nullptr;
+        int slot = 0;
+        if (bulk) {
+          slot = (int)(con % kRingStages);
+          if (!tc::mbar_wait(&ring_bar[warp][slot], (uint32_t)(con / kRingStages) & 1u, fused::kWaitNs)) {
+            failed = true;
+            break;
+          }
+          sx = ring + (size_t)slot * kStageB;
         }
-        const int slot = (int)(con % kRingStages);
-        if (!tc::mbar_wait(&ring_bar[warp][slot], (uint32_t)(con / kRingStages) & 1u, fused::kWaitNs)) {
-          failed = true;
-          break;
+        batch(b0, sx);
+        if (bulk) {
+          __syncwarp();  // every lane is done with the stage
+          ++con;
+          if (lane == 0) issue_some();
         }
-        batch(b0, ring + (size_t)slot * kStageB);
-        __syncwarp();  // every lane is done with the stage
-        ++con;
-        if (lane == 0) issue_some();
       }
       if (__any_sync(0xffffffffu, failed)) break;
       if (s_cur[warp].dead) goto next_unit;
